@@ -1,0 +1,397 @@
+"""Benchmark of the per-MoE-layer hot path on GB300.
+
+One step = one decode token through all 40 MoE layers of the
+Qwen3.6-35B-A3B-shaped workload (256 experts, top-8, hidden 2048,
+intermediate 512, bf16 experts, full 64.4 GB bank pinned in host memory,
+3072-slot GPU cache = 30% of the bank, correlated Zipf routing): per layer
+route_classify (top-k, dedup, hit/miss, LRU victims), the miss fetch on the
+copy stream one layer ahead, and the expert FFN reading the slots.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica (the path has no data-parallel exchange): value = all ranks' tokens /
+the slowest rank's time.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth import workloads as W  # noqa: E402
+
+METRIC = "MoE decode tokens/s (35B-A3B shape, 1 GB300); expert-GEMM HBM GB/s; miss rate"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=496)
+    p.add_argument("--warmup", type=int, default=16)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=W.QWEN35B_DECODE.name, choices=sorted(W.ALL))
+    p.add_argument("--fetch-mode", type=int, default=1, help="0 copy engine, 1 SM pull")
+    p.add_argument("--pull-ctas", type=int, default=0)
+    p.add_argument("--copy-streams", type=int, default=1)
+    p.add_argument("--serial", action="store_true", help="double buffering off")
+    p.add_argument("--bank-blobs", type=int, default=0, help="0 = full bank; fewer = aliased bank")
+    p.add_argument("--slots", type=int, default=0, help="override the cache size")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------- helpers
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gateup_bytes(w: W.Workload) -> int:
+    """Algorithmic bytes the gate/up kernel reads per unique expert: Wg and Wu
+    (and their fp8 block scales); x is re-read from shared memory."""
+    wsize = {synth.W_F32: 4, synth.W_BF16: 2, synth.W_FP8: 1}[w.wdtype]
+    scales = 2 * 2 * (w.hidden // 128) * (w.inter // 128) if w.wdtype == synth.W_FP8 else 0
+    return 2 * w.hidden * w.inter * wsize + scales
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, local, world
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------- oracle arm
+
+def oracle_sample(w: W.Workload, seconds: float, logits=None):
+    """Time the CPU oracle (routing, LRU simulation, fp64 FFN) on consecutive
+    steps of workload w until `seconds` of oracle time have passed (at least
+    one step).  Input generation (the expert blobs, hidden states) is not
+    timed.  The cache simulation starts cold at step 0.  Returns (tokens/s,
+    steps, oracle seconds)."""
+    from oracle import ffn as offn
+    from oracle import routing as orouting
+    from oracle.cache import ExpertCacheOracle
+    if logits is None:
+        logits = W.router_logits(w.replace(steps=min(w.steps, 64)))
+    ref = ExpertCacheOracle(w.num_layers, w.num_experts, w.num_slots)
+    spent = 0.0
+    steps = 0
+    while steps < logits.shape[0]:
+        for l in range(w.num_layers):
+            topk = orouting.topk(logits[steps, l], w.top_k)
+            raw = {e: synth.expert_blobs(w.seed, w.hidden, w.inter, w.wdtype, [w.blob_of(l, e)])
+                   for e in sorted({int(v) for v in topk.ravel()})}
+            x = W.hidden_states(w, steps, l)
+            t0 = time.perf_counter()
+            idx, gw = orouting.route(logits[steps, l], w.top_k)
+            ref.event(l, idx)
+            blobs = {e: offn.dequant_blob(b, w.hidden, w.inter, w.wdtype) for e, b in raw.items()}
+            offn.moe_ffn(x, idx, gw, lambda e: blobs[e])
+            spent += time.perf_counter() - t0
+        steps += 1
+        if spent >= seconds:
+            break
+    return steps * w.tokens / spent, steps, spent
+
+
+def cpu_baseline_subprocess(w: W.Workload, seconds: float):
+    """Run the oracle sample in a child process pinned to one BLAS thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; from synth import workloads as W; "
+            "v, s, dt = bench.oracle_sample(W.ALL[%r], %r); print(json.dumps([v, s, dt]))") % (ROOT, w.name, seconds)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        raise RuntimeError("oracle baseline failed: " + r.stderr[-2000:])
+    v, s, dt = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {s} decode steps x {w.num_layers} layers of {w.name} (routing, LRU simulation, "
+                      f"fp64 SwiGLU FFN), {dt:.1f} s on 1 host thread"}
+
+
+def run_reference(args, w):
+    rank, _, world = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    # each step: the oracle over a bounded sample of steps of the same workload
+    per = []
+    total_steps = 0
+    seconds = max(1.0, min(args.cpu_seconds, 20.0) / max(1, args.steps))
+    logits = W.router_logits(w.replace(steps=min(w.steps, 64)))
+    for i in range(args.warmup + args.steps):
+        v, s, dt = oracle_sample(w, seconds, logits)
+        if i >= args.warmup:
+            per.append(dt / max(1, s))
+            total_steps += s
+    ms = 1e3 * statistics.mean(per)
+    value = w.tokens / (ms / 1e3)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "global_batch": w.tokens, "layers": w.num_layers,
+                       "experts": w.num_experts, "top_k": w.top_k, "slots": w.num_slots},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{total_steps} decode steps (cold cache start) of {w.name}, "
+                                       "single host thread"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- our arm
+
+def run_ours(args, w):
+    import torch
+
+    rank, local, world = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import expert_cache_host_layer_gb300 as ft
+    from expert_cache_host_layer_gb300.pipeline import ExpertCache, pinned_bank
+
+    if args.slots:
+        w = w.replace(num_slots=args.slots)
+    n_blobs = args.bank_blobs or w.blobs
+    t_setup = time.perf_counter()
+    bank = pinned_bank(n_blobs * w.expert_bytes)
+    synth.expert_blobs(w.seed, w.hidden, w.inter, w.wdtype, np.arange(n_blobs), out_ptr=bank.data_ptr())
+    gen_s = time.perf_counter() - t_setup
+
+    steps_total = args.warmup + args.steps
+    wl = w.replace(steps=steps_total, seed=w.seed + rank)  # independent replicas per rank
+    logits_h = W.router_logits(wl)                             # [S][L][T][E]
+    x_h = np.stack([np.stack([W.hidden_states(wl, s, l) for l in range(w.num_layers)]) for s in range(steps_total)])
+    act = torch.float32 if w.wdtype == synth.W_F32 else torch.bfloat16
+    logits_d = torch.from_numpy(logits_h).to(dev)
+    x_d = torch.from_numpy(x_h).to(dev, act)
+    L, T = w.num_layers, w.tokens
+    y_d = torch.empty((L, T, w.hidden), dtype=act, device=dev)
+
+    cache = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots, T, bank,
+                        n_blobs, fetch_mode=args.fetch_mode, pull_ctas=args.pull_ctas,
+                        copy_streams=args.copy_streams, device=dev)
+    stream = cache.stream
+    double = not args.serial
+
+    def step(s):
+        cache.run_step(logits_d[s], x_d[s], y_d, double_buffer=double)
+
+    for s in range(args.warmup):
+        step(s)
+    cache.synchronize()
+    st0 = cache.stats()
+    cache.timing_enable(True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for s in range(args.warmup, steps_total):
+        step(s)
+    ev1.record(stream)
+    cache.synchronize()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    tm = cache.timing()
+    st1 = cache.stats()
+    cache.timing_enable(False)
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    tokens = world * args.steps * T
+    value = tokens / (elapsed_ms / 1e3)
+
+    d = {k: st1[k] - st0[k] for k in st1}
+    eb = w.expert_bytes
+    gemv_bytes_per_launch = d["unique_experts"] * gateup_bytes(w) / max(1, tm["gemv_n"])
+    gemv_ms = tm["gemv_ms"] / max(1, tm["gemv_n"])
+    ffn_bytes_per_launch = d["unique_experts"] * eb / max(1, tm["ffn_n"])
+    ffn_ms = tm["ffn_ms"] / max(1, tm["ffn_n"])
+    peak, peak_kind = measured_peaks()
+    achieved = gemv_bytes_per_launch / (gemv_ms / 1e3) / 1e9
+    fetch_gbs = d["bytes_fetched"] / max(1e-9, tm["fetch_ms"] / 1e3) / 1e9 if tm["fetch_n"] else None
+
+    # ---- end to end through the C ABI with host buffers -------------------
+    e2e = None
+    if not args.no_e2e:
+        lg_pin = torch.from_numpy(logits_h[args.warmup:]).pin_memory()
+        x_pin = torch.from_numpy(x_h[args.warmup:]).to(act).pin_memory()
+        y_pin = torch.empty((args.steps, L, T, w.hidden), dtype=act).pin_memory()
+        lg_dev = torch.empty_like(logits_d[0])
+        x_dev = torch.empty_like(x_d[0])
+        cache2 = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots, T,
+                             bank, n_blobs, fetch_mode=args.fetch_mode, pull_ctas=args.pull_ctas,
+                             copy_streams=args.copy_streams, device=dev, stream=stream)
+        for s in range(args.warmup):  # same warm state as the device-timed run
+            cache2.run_step(logits_d[s], x_d[s], y_d, double_buffer=double)
+        cache2.synchronize()
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                lg_dev.copy_(lg_pin[i], non_blocking=True)
+                x_dev.copy_(x_pin[i], non_blocking=True)
+                cache2.run_step(lg_dev, x_dev, y_d, double_buffer=double)
+                y_pin[i].copy_(y_d, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+        cache2.close()
+        e2e = {"value": world * args.steps * T / e2e_s, "unit": "tokens/s",
+               "h2d_bytes_per_step": int(lg_pin[0].numel() * 4 + x_pin[0].numel() * x_pin.element_size()),
+               "d2h_bytes_per_step": int(y_d.numel() * y_d.element_size())}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            cpu = cpu_baseline_subprocess(w, args.cpu_seconds)
+        except Exception as ex:  # reported, not fatal
+            cpu = {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": f"failed: {ex}"[:300]}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.wdtype == synth.W_BF16 else
+            ("f32" if w.wdtype == synth.W_F32 else "fp8e4m3"), "data": "synthetic",
+            "config": {"workload": w.name, "global_batch": world * T, "layers": L, "experts": w.num_experts,
+                       "top_k": w.top_k, "hidden": w.hidden, "inter": w.inter, "slots": w.num_slots,
+                       "bank_blobs": n_blobs, "bank_gb": round(n_blobs * eb / 1e9, 2),
+                       "fetch_mode": ["copy_engine", "sm_pull"][args.fetch_mode],
+                       "double_buffer": double, "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (each step reads ~2 GB of expert slots)"},
+            "miss_rate": d["misses"] / max(1, d["unique_experts"]),
+            "expert_gemm_gbs": d["unique_experts"] * eb / max(1e-9, tm["ffn_ms"] / 1e3) / 1e9,
+            "miss_copy": {"gbs": fetch_gbs, "bytes_per_step": d["bytes_fetched"] / args.steps,
+                          "mode": ["copy_engine", "sm_pull"][args.fetch_mode]},
+            "phase_ms_per_step": {k: tm[f"{k}_ms"] / args.steps for k in ("route", "fetch", "ffn", "gemv", "down")},
+            "roofline": {"kernel": "gateup_kernel (decode expert GEMV, gate+up+SwiGLU)", "bound": "hbm",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_kind": peak_kind, "traffic": None,
+                         "bytes_per_launch": gemv_bytes_per_launch, "launch_us": gemv_ms * 1e3,
+                         "ffn_achieved_gbs": ffn_bytes_per_launch / (ffn_ms / 1e3) / 1e9},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": d["kernel_launches"],
+            "clocks": clocks,
+            "setup_s": {"bank_generate": round(gen_s, 1)},
+        }
+        print(json.dumps(line), flush=True)
+    cache.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    w = W.ALL[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,741 @@
+// Host side of libft: the C ABI declared in include/ft.h.
+//
+// One ft_cache owns the device slot tables, one plan per layer, the routing
+// scratch, a mapped pinned mirror of each layer's miss list, the copy
+// stream(s) and the per-layer events that order the pipeline:
+//
+//   compute stream:  route(l+1) -> [cls(l+1)] ... wait(ready(l)) -> FFN(l)
+//   copy stream:     wait(cls(l+1)) -> miss copies of l+1 -> [ready(l+1)]
+//
+// so the misses of layer l+1 stream in while layer l computes ("FreeToken:
+// Efficient Edge-Native MoE Serving ...", ablation paragraph: double
+// buffering).  In copy-engine mode a library thread waits for cls(l), reads
+// the mirrored miss list and issues one cudaMemcpyAsync per miss; in SM-pull
+// mode a kernel on the copy stream reads the device plan itself.
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <condition_variable>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <deque>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "ft_internal.h"
+
+using namespace ft;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+ft_status fail(ft_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+#define CU(call)                                                                                  \
+  do {                                                                                            \
+    cudaError_t e_ = (call);                                                                      \
+    if (e_ != cudaSuccess)                                                                        \
+      return fail(e_ == cudaErrorMemoryAllocation ? FT_ERR_OOM : FT_ERR_CUDA, "%s: %s (%s:%d)", #call, \
+                  cudaGetErrorString(e_), __FILE__, __LINE__);                                    \
+  } while (0)
+
+size_t blob_bytes(int H, int I, int wdtype) {
+  if (H <= 0 || I <= 0) return 0;
+  const size_t n = 3ull * H * I;
+  switch (wdtype) {
+    case FT_W_F32: return (H % 4 || I % 4) ? 0 : 4 * n;
+    case FT_W_BF16: return (H % 8 || I % 8) ? 0 : 2 * n;
+    case FT_W_FP8E4M3_B128: return (H % 128 || I % 128) ? 0 : n + 2ull * 3 * (H / 128) * (I / 128);
+    default: return 0;
+  }
+}
+
+// Event-pair timer for one phase.  Pairs are folded into the total when the
+// pool fills, starting with the oldest (long finished) half.
+struct PhaseTimer {
+  std::vector<cudaEvent_t> ev;  // 2 per pair
+  int used = 0;
+  double total_ms = 0.0;
+  long long n = 0;
+  static constexpr int kPairs = 2048;
+  ~PhaseTimer() {
+    for (auto e : ev) cudaEventDestroy(e);
+  }
+  bool ensure() {
+    if (!ev.empty()) return true;
+    ev.resize(2 * kPairs);
+    for (auto& e : ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return false;
+    return true;
+  }
+  void fold(int pairs) {
+    for (int i = 0; i < pairs; ++i) {
+      float ms = 0.0f;
+      cudaEventSynchronize(ev[2 * i + 1]);
+      if (cudaEventElapsedTime(&ms, ev[2 * i], ev[2 * i + 1]) == cudaSuccess) {
+        total_ms += ms;
+        ++n;
+      }
+    }
+    // move the unfolded pairs to the front
+    for (int i = pairs; i < used; ++i) {
+      std::swap(ev[2 * (i - pairs)], ev[2 * i]);
+      std::swap(ev[2 * (i - pairs) + 1], ev[2 * i + 1]);
+    }
+    used -= pairs;
+  }
+  cudaEvent_t begin(cudaStream_t s) {
+    if (!ensure()) return nullptr;
+    if (used == kPairs) fold(kPairs / 2);
+    cudaEvent_t e = ev[2 * used];
+    cudaEventRecord(e, s);
+    return e;
+  }
+  void end(cudaStream_t s) {
+    cudaEventRecord(ev[2 * used + 1], s);
+    ++used;
+  }
+  void collect() { fold(used); }
+  void reset() {
+    collect();
+    total_ms = 0.0;
+    n = 0;
+  }
+};
+
+enum { PHASE_ROUTE = 0, PHASE_FETCH, PHASE_FFN, PHASE_GEMV, PHASE_DOWN, PHASE_COUNT };
+
+}  // namespace
+
+struct ft_cache {
+  // configuration
+  ft_cache_config cfg{};
+  int L = 0, E = 0, k = 0, H = 0, I = 0, wdtype = 0, max_tokens = 0;
+  size_t eb = 0;
+  int device = 0;
+  // memory
+  void* pool = nullptr;
+  int64_t C = 0;
+  const uint8_t* bank_host = nullptr;
+  const void* bank_dev = nullptr;
+  bool registered_bank = false;
+  Tables tab{};
+  std::vector<Plan> plans;
+  void* plan_mem = nullptr;
+  RouteScratch scr{};
+  void* scr_mem = nullptr;
+  HostMirror* mirror_host = nullptr;  // mapped pinned [L]
+  HostMirror* mirror_dev = nullptr;
+  float* h_buf = nullptr;             // decode intermediate [max_rows][I]
+  // streams and events
+  cudaStream_t compute = nullptr;
+  cudaStream_t copy[2] = {nullptr, nullptr};
+  int ncopy = 1;
+  cudaEvent_t copy_join = nullptr;
+  std::vector<cudaEvent_t> cls_ev, ready_ev;
+  // host-side state of the event stream
+  int next_event = 0;
+  bool pin_previous = false;          // false on the first event and right after a resize
+  std::vector<int> layer_event;       // event of the layer's current plan (-1 none)
+  std::vector<int> layer_tokens;
+  std::vector<int> fetch_event;       // event whose fetch was issued (-1 none)
+  std::vector<int> forward_event;     // event whose FFN was enqueued (-1 none)
+  // copy-engine helper thread
+  std::thread helper;
+  std::mutex mu;
+  std::condition_variable cv_job, cv_done;
+  std::deque<std::pair<int, int>> jobs;  // (layer, event)
+  std::vector<int> done_event;           // per layer: event whose copies are issued
+  std::vector<int> job_status;
+  bool stop = false;
+  int busy = 0;
+  // counters
+  std::atomic<long long> launches{0}, memcpys{0};
+  // timing
+  bool timing = false;
+  PhaseTimer timers[PHASE_COUNT];
+};
+
+namespace {
+
+void helper_loop(ft_cache* c) {
+  cudaSetDevice(c->device);
+  for (;;) {
+    std::pair<int, int> job;
+    {
+      std::unique_lock<std::mutex> lk(c->mu);
+      c->cv_job.wait(lk, [&] { return c->stop || !c->jobs.empty(); });
+      if (c->jobs.empty()) return;
+      job = c->jobs.front();
+      c->jobs.pop_front();
+      ++c->busy;
+    }
+    const int l = job.first, ev = job.second;
+    int st = FT_OK;
+    if (cudaEventSynchronize(c->cls_ev[l]) != cudaSuccess) st = FT_ERR_CUDA;
+    const HostMirror* m = c->mirror_host + l;
+    if (st == FT_OK && m->event != ev) st = FT_ERR_STATE;
+    const bool tm = c->timing;
+    if (st == FT_OK) {
+      const int n = m->n_miss;
+      if (tm) c->timers[PHASE_FETCH].begin(c->copy[0]);
+      if (c->ncopy > 1) {  // second stream starts with the first
+        cudaEventRecord(c->copy_join, c->copy[0]);
+        cudaStreamWaitEvent(c->copy[1], c->copy_join, 0);
+      }
+      for (int i = 0; i < n && st == FT_OK; ++i) {
+        const int e = m->miss_expert[i], s = m->miss_slot[i];
+        if (e < 0 || e >= c->E || s < 0 || s >= c->C) {
+          st = FT_ERR_CHECKED;
+          break;
+        }
+        const int64_t blob = ((int64_t)l * c->E + e) % c->cfg.bank_blobs;
+        if (cudaMemcpyAsync(static_cast<uint8_t*>(c->pool) + (size_t)s * c->eb, c->bank_host + (size_t)blob * c->eb,
+                            c->eb, cudaMemcpyHostToDevice, c->copy[i % c->ncopy]) != cudaSuccess)
+          st = FT_ERR_CUDA;
+        ++c->memcpys;
+      }
+      if (c->ncopy > 1) {
+        cudaEventRecord(c->copy_join, c->copy[1]);
+        cudaStreamWaitEvent(c->copy[0], c->copy_join, 0);
+      }
+      if (tm) c->timers[PHASE_FETCH].end(c->copy[0]);
+    }
+    cudaEventRecord(c->ready_ev[l], c->copy[0]);
+    {
+      std::lock_guard<std::mutex> lk(c->mu);
+      c->done_event[l] = ev;
+      c->job_status[l] = st;
+      --c->busy;
+    }
+    c->cv_done.notify_all();
+  }
+}
+
+// Wait until the helper has issued the copies of (layer, event); returns the job's status.
+ft_status wait_fetch_issued(ft_cache* c, int layer, int event) {
+  std::unique_lock<std::mutex> lk(c->mu);
+  c->cv_done.wait(lk, [&] { return c->done_event[layer] == event; });
+  return (ft_status)c->job_status[layer];
+}
+
+void wait_helper_idle(ft_cache* c) {
+  std::unique_lock<std::mutex> lk(c->mu);
+  c->cv_done.wait(lk, [&] { return c->jobs.empty() && c->busy == 0; });
+}
+
+ft_status sync_all(ft_cache* c) {
+  if (c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE) wait_helper_idle(c);
+  CU(cudaStreamSynchronize(c->compute));
+  for (int i = 0; i < c->ncopy; ++i) CU(cudaStreamSynchronize(c->copy[i]));
+  return FT_OK;
+}
+
+ft_status device_status(ft_cache* c) {
+  int st = 0;
+  CU(cudaMemcpy(&st, c->tab.status, sizeof st, cudaMemcpyDeviceToHost));
+  if (st != 0) return fail((ft_status)st, "device status %d raised by an earlier call", st);
+  return FT_OK;
+}
+
+ft_status alloc_tables(Tables& t, int64_t C, int num_keys, bool with_keys) {
+  t.num_slots = (int32_t)C;
+  if (with_keys) CU(cudaMalloc(&t.key_to_slot, sizeof(int32_t) * num_keys));
+  CU(cudaMalloc(&t.slot_key, sizeof(int32_t) * C));
+  CU(cudaMalloc(&t.slot_ts, sizeof(int32_t) * C));
+  CU(cudaMalloc(&t.order[0], sizeof(int32_t) * C));
+  CU(cudaMalloc(&t.order[1], sizeof(int32_t) * C));
+  CU(cudaMalloc(&t.order_cur, sizeof(int32_t) * 2));
+  t.status = t.order_cur + 1;
+  CU(cudaMalloc(&t.stats, sizeof(long long) * ST_COUNT));
+  return FT_OK;
+}
+
+void free_tables(Tables& t, bool with_keys) {
+  if (with_keys) cudaFree(t.key_to_slot);
+  cudaFree(t.slot_key);
+  cudaFree(t.slot_ts);
+  cudaFree(t.order[0]);
+  cudaFree(t.order[1]);
+  cudaFree(t.order_cur);
+  cudaFree(t.stats);
+  Tables z{};
+  z.key_to_slot = with_keys ? nullptr : t.key_to_slot;
+  t = z;
+}
+
+int capacity_bound(const ft_cache* c) {
+  const long long rows = (long long)c->max_tokens * c->k;
+  return (int)(2 * std::min<long long>(rows, c->E));
+}
+
+}  // namespace
+
+// ============================================================== the C ABI
+extern "C" {
+
+size_t ft_expert_bytes(int32_t hidden, int32_t inter, int32_t wdtype) { return blob_bytes(hidden, inter, wdtype); }
+
+const char* ft_status_str(ft_status s) {
+  switch (s) {
+    case FT_OK: return "FT_OK";
+    case FT_ERR_INVALID_ARG: return "FT_ERR_INVALID_ARG";
+    case FT_ERR_CUDA: return "FT_ERR_CUDA";
+    case FT_ERR_OOM: return "FT_ERR_OOM";
+    case FT_ERR_CAPACITY: return "FT_ERR_CAPACITY";
+    case FT_ERR_STATE: return "FT_ERR_STATE";
+    case FT_ERR_TIMEOUT: return "FT_ERR_TIMEOUT";
+    case FT_ERR_CHECKED: return "FT_ERR_CHECKED";
+    case FT_ERR_UNSUPPORTED: return "FT_ERR_UNSUPPORTED";
+  }
+  return "FT_ERR_UNKNOWN";
+}
+
+const char* ft_last_error(void) { return g_last_error.c_str(); }
+
+ft_status ft_cache_destroy(ft_cache* c) {
+  if (!c) return FT_OK;
+  cudaSetDevice(c->device);
+  if (c->helper.joinable()) {
+    {
+      std::lock_guard<std::mutex> lk(c->mu);
+      c->stop = true;
+    }
+    c->cv_job.notify_all();
+    c->helper.join();
+  }
+  if (c->compute || c->copy[0]) {
+    if (c->compute) cudaStreamSynchronize(c->compute);
+    for (int i = 0; i < 2; ++i)
+      if (c->copy[i]) cudaStreamSynchronize(c->copy[i]);
+  }
+  for (auto e : c->cls_ev) cudaEventDestroy(e);
+  for (auto e : c->ready_ev) cudaEventDestroy(e);
+  if (c->copy_join) cudaEventDestroy(c->copy_join);
+  for (int i = 0; i < 2; ++i)
+    if (c->copy[i]) cudaStreamDestroy(c->copy[i]);
+  free_tables(c->tab, true);
+  cudaFree(c->plan_mem);
+  cudaFree(c->scr_mem);
+  cudaFree(c->h_buf);
+  if (c->mirror_host) cudaFreeHost(c->mirror_host);
+  if (c->registered_bank) cudaHostUnregister(const_cast<uint8_t*>(c->bank_host));
+  delete c;
+  return FT_OK;
+}
+
+ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t num_slots, void* compute_stream,
+                          ft_cache** out) {
+  if (!cfg || !out) return fail(FT_ERR_INVALID_ARG, "null config or output pointer");
+  *out = nullptr;
+  const ft_cache_config& g = *cfg;
+  if (g.num_layers < 1 || g.num_experts < 1 || g.num_experts > kMaxExperts)
+    return fail(FT_ERR_INVALID_ARG, "num_layers must be >= 1 and num_experts in 1..%d", kMaxExperts);
+  if (g.top_k < 1 || g.top_k > kMaxTopK || g.top_k > g.num_experts)
+    return fail(FT_ERR_INVALID_ARG, "top_k must be in 1..min(num_experts, %d)", kMaxTopK);
+  const size_t eb = blob_bytes(g.hidden, g.inter, g.wdtype);
+  if (eb == 0) return fail(FT_ERR_INVALID_ARG, "unsupported hidden/inter/wdtype (%d, %d, %d)", g.hidden, g.inter, g.wdtype);
+  if (eb % 16) return fail(FT_ERR_INVALID_ARG, "expert_bytes %zu is not a multiple of 16", eb);
+  if (g.wdtype != FT_W_F32 && (g.hidden % 128 || g.inter % 128))
+    return fail(FT_ERR_INVALID_ARG, "bf16/fp8 experts need hidden and inter multiples of 128");
+  if (g.max_tokens < 1) return fail(FT_ERR_INVALID_ARG, "max_tokens must be >= 1");
+  if ((long long)g.max_tokens * g.top_k > (1LL << 30)) return fail(FT_ERR_INVALID_ARG, "max_tokens * top_k too large");
+  if (g.fetch_mode != FT_FETCH_COPY_ENGINE && g.fetch_mode != FT_FETCH_SM_PULL)
+    return fail(FT_ERR_INVALID_ARG, "unknown fetch_mode %d", g.fetch_mode);
+  if (g.copy_streams < 0 || g.copy_streams > 2) return fail(FT_ERR_INVALID_ARG, "copy_streams must be 0, 1 or 2");
+  if (!g.host_bank || g.bank_blobs < 1 || g.bank_blobs > (int64_t)g.num_layers * g.num_experts)
+    return fail(FT_ERR_INVALID_ARG, "host_bank null or bank_blobs outside 1..L*E");
+  if (g.host_bank_bytes < (uint64_t)g.bank_blobs * eb)
+    return fail(FT_ERR_INVALID_ARG, "host_bank_bytes %llu < bank_blobs * expert_bytes", (unsigned long long)g.host_bank_bytes);
+  if (!slot_pool || (reinterpret_cast<uintptr_t>(slot_pool) & 255))
+    return fail(FT_ERR_INVALID_ARG, "slot_pool must be a non-null 256-byte aligned device pointer");
+  if (num_slots < 1 || num_slots > INT32_MAX / 2) return fail(FT_ERR_INVALID_ARG, "num_slots out of range");
+
+  ft_cache* c = new ft_cache();
+  c->cfg = g;
+  c->L = g.num_layers; c->E = g.num_experts; c->k = g.top_k; c->H = g.hidden; c->I = g.inter;
+  c->wdtype = g.wdtype; c->max_tokens = g.max_tokens; c->eb = eb;
+  c->pool = slot_pool; c->C = num_slots;
+  c->compute = static_cast<cudaStream_t>(compute_stream);
+  c->ncopy = g.copy_streams == 2 ? 2 : 1;
+  if (num_slots < capacity_bound(c)) {
+    delete c;
+    return fail(FT_ERR_CAPACITY, "num_slots %lld < 2 * min(max_tokens * top_k, num_experts) = %d", (long long)num_slots,
+                2 * std::min<long long>((long long)g.max_tokens * g.top_k, g.num_experts));
+  }
+  ft_status st = [&]() -> ft_status {
+    CU(cudaGetDevice(&c->device));
+    cudaPointerAttributes pa{};
+    CU(cudaPointerGetAttributes(&pa, slot_pool));
+    if (pa.type != cudaMemoryTypeDevice) return fail(FT_ERR_INVALID_ARG, "slot_pool is not device memory");
+    // host bank: pinned (registered) and mapped
+    c->bank_host = static_cast<const uint8_t*>(g.host_bank);
+    cudaPointerAttributes ha{};
+    CU(cudaPointerGetAttributes(&ha, g.host_bank));
+    if (ha.type == cudaMemoryTypeDevice || ha.type == cudaMemoryTypeManaged)
+      return fail(FT_ERR_INVALID_ARG, "host_bank must be host memory");
+    if (ha.type != cudaMemoryTypeHost) {
+      CU(cudaHostRegister(const_cast<void*>(g.host_bank), g.host_bank_bytes, cudaHostRegisterMapped));
+      c->registered_bank = true;
+    }
+    void* dptr = nullptr;
+    CU(cudaHostGetDevicePointer(&dptr, const_cast<void*>(g.host_bank), 0));
+    c->bank_dev = dptr;
+    // tables
+    if (alloc_tables(c->tab, num_slots, c->L * c->E, true) != FT_OK) return FT_ERR_OOM;
+    // plans
+    const long long rows = (long long)g.max_tokens * g.top_k;
+    const size_t per_plan = sizeof(int32_t) * (PH_WORDS + 9 * (size_t)c->E + 1 + 2 * rows) + sizeof(float) * rows;
+    const size_t per_plan_al = (per_plan + 255) & ~size_t(255);
+    CU(cudaMalloc(&c->plan_mem, per_plan_al * c->L));
+    CU(cudaMemset(c->plan_mem, 0, per_plan_al * c->L));
+    c->plans.resize(c->L);
+    for (int l = 0; l < c->L; ++l) {
+      int32_t* p = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(c->plan_mem) + per_plan_al * l);
+      Plan& pl = c->plans[l];
+      pl.hdr = p; p += PH_WORDS;
+      pl.unique_expert = p; p += c->E;
+      pl.unique_slot = p; p += c->E;
+      pl.hit = p; p += c->E;
+      pl.miss_expert = p; p += c->E;
+      pl.miss_slot = p; p += c->E;
+      pl.evicted_key = p; p += c->E;
+      pl.e2u = p; p += c->E;
+      pl.u_count = p; p += c->E;
+      pl.u_offset = p; p += c->E + 1;
+      pl.rows_by_u = p; p += rows;
+      pl.topk_idx = p; p += rows;
+      pl.topk_w = reinterpret_cast<float*>(p);
+    }
+    // routing scratch (zero; the kernel leaves it zero)
+    const size_t scr_bytes = sizeof(uint32_t) * (kMaxExperts / 32) + sizeof(int32_t) * kMaxExperts + 64;
+    CU(cudaMalloc(&c->scr_mem, scr_bytes));
+    CU(cudaMemset(c->scr_mem, 0, scr_bytes));
+    c->scr.bits = static_cast<uint32_t*>(c->scr_mem);
+    c->scr.counts = reinterpret_cast<int32_t*>(c->scr.bits + kMaxExperts / 32);
+    c->scr.ticket = reinterpret_cast<uint32_t*>(c->scr.counts + kMaxExperts);
+    // decode intermediate
+    const long long drows = (long long)std::min(g.max_tokens, kDecodeMaxTokens) * g.top_k;
+    CU(cudaMalloc(&c->h_buf, sizeof(float) * drows * c->I));
+    // miss-list mirror in mapped pinned memory
+    CU(cudaHostAlloc(reinterpret_cast<void**>(&c->mirror_host), sizeof(HostMirror) * c->L, cudaHostAllocMapped));
+    memset(c->mirror_host, 0, sizeof(HostMirror) * c->L);
+    for (int l = 0; l < c->L; ++l) c->mirror_host[l].event = -1;
+    CU(cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->mirror_dev), c->mirror_host, 0));
+    // streams and events
+    for (int i = 0; i < c->ncopy; ++i) CU(cudaStreamCreateWithFlags(&c->copy[i], cudaStreamNonBlocking));
+    CU(cudaEventCreateWithFlags(&c->copy_join, cudaEventDisableTiming));
+    c->cls_ev.assign(c->L, nullptr);
+    c->ready_ev.assign(c->L, nullptr);
+    for (int l = 0; l < c->L; ++l) {
+      CU(cudaEventCreateWithFlags(&c->cls_ev[l], cudaEventDisableTiming));
+      CU(cudaEventCreateWithFlags(&c->ready_ev[l], cudaEventDisableTiming));
+    }
+    c->layer_event.assign(c->L, -1);
+    c->layer_tokens.assign(c->L, 0);
+    c->fetch_event.assign(c->L, -1);
+    c->forward_event.assign(c->L, -1);
+    c->done_event.assign(c->L, -1);
+    c->job_status.assign(c->L, FT_OK);
+    CU(launch_init_tables(c->tab, c->L * c->E, c->compute));
+    ++c->launches;
+    CU(cudaStreamSynchronize(c->compute));
+    if (g.fetch_mode == FT_FETCH_COPY_ENGINE) c->helper = std::thread(helper_loop, c);
+    return FT_OK;
+  }();
+  if (st != FT_OK) {
+    std::string msg = g_last_error;
+    ft_cache_destroy(c);
+    g_last_error = msg;
+    return st;
+  }
+  *out = c;
+  return FT_OK;
+}
+
+ft_status ft_route_classify(ft_cache* c, int32_t layer, const float* logits, int32_t T, int32_t* topk_idx,
+                            float* topk_w) {
+  if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
+  if (layer < 0 || layer >= c->L) return fail(FT_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (T < 0 || T > c->max_tokens) return fail(FT_ERR_INVALID_ARG, "T=%d outside 0..max_tokens=%d", T, c->max_tokens);
+  if (T > 0 && !logits) return fail(FT_ERR_INVALID_ARG, "null logits");
+  const int t = c->next_event;
+  // a fetched plan must be consumed by its FFN before the layer is re-planned
+  if (c->fetch_event[layer] >= 0 && c->fetch_event[layer] == c->layer_event[layer] &&
+      c->forward_event[layer] != c->layer_event[layer])
+    return fail(FT_ERR_STATE, "layer %d: fetched plan not yet forwarded", layer);
+  // pipelining depth: every fetched event older than t-1 must have its FFN enqueued
+  for (int l = 0; l < c->L; ++l)
+    if (c->fetch_event[l] >= 0 && c->fetch_event[l] <= t - 2 && c->forward_event[l] != c->fetch_event[l])
+      return fail(FT_ERR_STATE, "layer %d (event %d) fetched but not forwarded; only one layer may run ahead", l,
+                  c->fetch_event[l]);
+  RouteArgs a{};
+  a.logits = logits; a.T = T; a.E = c->E; a.k = c->k; a.layer = layer; a.event = t;
+  a.pin_ts = c->pin_previous ? t - 1 : INT_MIN;
+  a.out_idx = topk_idx; a.out_w = topk_w;
+  a.tab = c->tab; a.plan = c->plans[layer]; a.scr = c->scr;
+  a.mirror = c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE ? c->mirror_dev + layer : nullptr;
+  a.expert_bytes = (long long)c->eb;
+  a.build_rows = (long long)T * c->k <= kMaxExperts;
+  if (c->timing) c->timers[PHASE_ROUTE].begin(c->compute);
+  CU(launch_route_classify(a, c->compute));
+  if (c->timing) c->timers[PHASE_ROUTE].end(c->compute);
+  ++c->launches;
+  CU(cudaEventRecord(c->cls_ev[layer], c->compute));
+  c->layer_event[layer] = t;
+  c->layer_tokens[layer] = T;
+  c->next_event = t + 1;
+  c->pin_previous = true;
+  return FT_OK;
+}
+
+ft_status ft_fetch_misses(ft_cache* c, int32_t layer) {
+  if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
+  if (layer < 0 || layer >= c->L) return fail(FT_ERR_INVALID_ARG, "layer %d out of range", layer);
+  const int ev = c->layer_event[layer];
+  if (ev < 0 || c->fetch_event[layer] == ev) return fail(FT_ERR_STATE, "layer %d has no classification awaiting fetch", layer);
+  if (c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE) {
+    {
+      std::lock_guard<std::mutex> lk(c->mu);
+      c->jobs.emplace_back(layer, ev);
+    }
+    c->cv_job.notify_one();
+  } else {
+    CU(cudaStreamWaitEvent(c->copy[0], c->cls_ev[layer], 0));
+    PullArgs p{};
+    const Plan& pl = c->plans[layer];
+    p.hdr = pl.hdr; p.miss_expert = pl.miss_expert; p.miss_slot = pl.miss_slot;
+    p.layer = layer; p.E = c->E; p.bank_blobs = c->cfg.bank_blobs; p.bank = c->bank_dev;
+    p.pool = c->pool; p.expert_bytes = (long long)c->eb;
+    const int ctas = c->cfg.pull_ctas > 0 ? c->cfg.pull_ctas : 32;
+    if (c->timing) c->timers[PHASE_FETCH].begin(c->copy[0]);
+    CU(launch_pull_misses(p, ctas, c->copy[0]));
+    if (c->timing) c->timers[PHASE_FETCH].end(c->copy[0]);
+    ++c->launches;
+    CU(cudaEventRecord(c->ready_ev[layer], c->copy[0]));
+  }
+  c->fetch_event[layer] = ev;
+  return FT_OK;
+}
+
+ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, void* y) {
+  if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
+  if (layer < 0 || layer >= c->L) return fail(FT_ERR_INVALID_ARG, "layer %d out of range", layer);
+  const int ev = c->layer_event[layer];
+  if (ev < 0 || c->fetch_event[layer] != ev || c->forward_event[layer] == ev)
+    return fail(FT_ERR_STATE, "layer %d: forward needs a classified and fetched plan", layer);
+  if (T != c->layer_tokens[layer]) return fail(FT_ERR_INVALID_ARG, "T=%d differs from the plan's T=%d", T, c->layer_tokens[layer]);
+  if (T > 0 && (!x || !y)) return fail(FT_ERR_INVALID_ARG, "null x or y");
+  if (c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE) {
+    const ft_status js = wait_fetch_issued(c, layer, ev);
+    if (js != FT_OK) return fail(js, "layer %d: miss copy failed (%s)", layer, ft_status_str(js));
+  }
+  CU(cudaStreamWaitEvent(c->compute, c->ready_ev[layer], 0));
+  c->forward_event[layer] = ev;
+  if (T == 0) return FT_OK;
+  if (T > kDecodeMaxTokens) return fail(FT_ERR_UNSUPPORTED, "T=%d > %d needs the grouped GEMM path", T, kDecodeMaxTokens);
+  const Plan& pl = c->plans[layer];
+  FfnArgs f{};
+  f.hdr = pl.hdr; f.unique_slot = pl.unique_slot; f.u_offset = pl.u_offset; f.rows_by_u = pl.rows_by_u;
+  f.topk_w = pl.topk_w; f.x = x; f.y = y; f.pool = static_cast<const uint8_t*>(c->pool);
+  f.expert_bytes = (long long)c->eb; f.H = c->H; f.I = c->I; f.k = c->k; f.T = T; f.wdtype = c->wdtype; f.h = c->h_buf;
+  const bool tm = c->timing;
+  if (tm) {
+    c->timers[PHASE_FFN].begin(c->compute);
+    c->timers[PHASE_GEMV].begin(c->compute);
+  }
+  cudaError_t e = launch_decode_gateup(f, c->compute);
+  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "gate/up launch: %s", cudaGetErrorString(e));
+  ++c->launches;
+  if (tm) {
+    c->timers[PHASE_GEMV].end(c->compute);
+    c->timers[PHASE_DOWN].begin(c->compute);
+  }
+  e = launch_decode_down(f, c->compute);
+  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "down launch: %s", cudaGetErrorString(e));
+  ++c->launches;
+  if (tm) {
+    c->timers[PHASE_DOWN].end(c->compute);
+    c->timers[PHASE_FFN].end(c->compute);
+  }
+  return FT_OK;
+}
+
+ft_status ft_cache_resize(ft_cache* c, void* new_pool, int64_t new_num_slots) {
+  if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
+  if (!new_pool || (reinterpret_cast<uintptr_t>(new_pool) & 255))
+    return fail(FT_ERR_INVALID_ARG, "new_pool must be a non-null 256-byte aligned device pointer");
+  if (new_num_slots < 1 || new_num_slots > INT32_MAX / 2) return fail(FT_ERR_INVALID_ARG, "new_num_slots out of range");
+  if (new_num_slots < capacity_bound(c))
+    return fail(FT_ERR_CAPACITY, "new_num_slots %lld below the capacity bound %d", (long long)new_num_slots, capacity_bound(c));
+  for (int l = 0; l < c->L; ++l)
+    if (c->fetch_event[l] >= 0 && c->fetch_event[l] == c->layer_event[l] && c->forward_event[l] != c->fetch_event[l])
+      return fail(FT_ERR_STATE, "layer %d has a fetched plan whose FFN was not enqueued", l);
+  ft_status s = sync_all(c);  // the safe point
+  if (s != FT_OK) return s;
+  cudaPointerAttributes pa{};
+  CU(cudaPointerGetAttributes(&pa, new_pool));
+  if (pa.type != cudaMemoryTypeDevice) return fail(FT_ERR_INVALID_ARG, "new_pool is not device memory");
+  Tables nt{};
+  nt.key_to_slot = c->tab.key_to_slot;
+  if (alloc_tables(nt, new_num_slots, 0, false) != FT_OK) {
+    free_tables(nt, false);
+    return FT_ERR_OOM;
+  }
+  int32_t* moves = nullptr;
+  const int64_t max_moves = std::max<int64_t>(new_num_slots, 1);
+  cudaError_t e = cudaMalloc(&moves, sizeof(int32_t) * (2 * max_moves + 1));
+  if (e != cudaSuccess) {
+    free_tables(nt, false);
+    return fail(FT_ERR_OOM, "resize move list: %s", cudaGetErrorString(e));
+  }
+  ResizeArgs ra{};
+  ra.old_tab = c->tab; ra.new_tab = nt; ra.num_keys = c->L * c->E; ra.E = c->E;
+  ra.moves = moves + 1; ra.n_moves = moves; ra.copy_all = new_pool != c->pool;
+  int n = 0;
+  e = launch_resize_tables(ra, c->compute, &n);
+  c->launches += n;
+  if (e == cudaSuccess) {
+    e = launch_move_blobs(ra.moves, ra.n_moves, (int)max_moves, c->pool, new_pool, (long long)c->eb, c->compute);
+    ++c->launches;
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(c->compute);
+  cudaFree(moves);
+  if (e != cudaSuccess) {
+    free_tables(nt, false);
+    return fail(FT_ERR_CUDA, "resize: %s", cudaGetErrorString(e));
+  }
+  free_tables(c->tab, false);
+  c->tab = nt;
+  c->pool = new_pool;
+  c->C = new_num_slots;
+  c->pin_previous = false;  // the safe point: nothing is in flight
+  for (int l = 0; l < c->L; ++l) {
+    c->layer_event[l] = -1;
+    c->fetch_event[l] = -1;
+    c->forward_event[l] = -1;
+  }
+  return FT_OK;
+}
+
+ft_status ft_synchronize(ft_cache* c) {
+  if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
+  ft_status s = sync_all(c);
+  if (s != FT_OK) return s;
+  return device_status(c);
+}
+
+ft_status ft_get_plan(ft_cache* c, int32_t layer, ft_plan_info* info, int32_t* unique_expert, int32_t* unique_slot,
+                      uint8_t* hit, int32_t* miss_expert, int32_t* miss_slot, int32_t* evicted_key) {
+  if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
+  if (layer < 0 || layer >= c->L) return fail(FT_ERR_INVALID_ARG, "layer %d out of range", layer);
+  ft_status s = sync_all(c);
+  if (s != FT_OK) return s;
+  const Plan& pl = c->plans[layer];
+  int32_t hdr[PH_WORDS];
+  CU(cudaMemcpy(hdr, pl.hdr, sizeof hdr, cudaMemcpyDeviceToHost));
+  if (info) {
+    info->event = hdr[PH_EVENT];
+    info->n_tokens = hdr[PH_TOKENS];
+    info->n_unique = hdr[PH_UNIQUE];
+    info->n_miss = hdr[PH_MISS];
+  }
+  const int nu = hdr[PH_UNIQUE], nm = hdr[PH_MISS];
+  if (unique_expert && nu) CU(cudaMemcpy(unique_expert, pl.unique_expert, sizeof(int32_t) * nu, cudaMemcpyDeviceToHost));
+  if (unique_slot && nu) CU(cudaMemcpy(unique_slot, pl.unique_slot, sizeof(int32_t) * nu, cudaMemcpyDeviceToHost));
+  if (hit && nu) {
+    std::vector<int32_t> h(nu);
+    CU(cudaMemcpy(h.data(), pl.hit, sizeof(int32_t) * nu, cudaMemcpyDeviceToHost));
+    for (int i = 0; i < nu; ++i) hit[i] = (uint8_t)h[i];
+  }
+  if (miss_expert && nm) CU(cudaMemcpy(miss_expert, pl.miss_expert, sizeof(int32_t) * nm, cudaMemcpyDeviceToHost));
+  if (miss_slot && nm) CU(cudaMemcpy(miss_slot, pl.miss_slot, sizeof(int32_t) * nm, cudaMemcpyDeviceToHost));
+  if (evicted_key && nm) CU(cudaMemcpy(evicted_key, pl.evicted_key, sizeof(int32_t) * nm, cudaMemcpyDeviceToHost));
+  return FT_OK;
+}
+
+ft_status ft_get_tables(ft_cache* c, int32_t* key_to_slot, int32_t* slot_key, int32_t* slot_ts) {
+  if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
+  ft_status s = sync_all(c);
+  if (s != FT_OK) return s;
+  if (key_to_slot) CU(cudaMemcpy(key_to_slot, c->tab.key_to_slot, sizeof(int32_t) * c->L * c->E, cudaMemcpyDeviceToHost));
+  if (slot_key) CU(cudaMemcpy(slot_key, c->tab.slot_key, sizeof(int32_t) * c->C, cudaMemcpyDeviceToHost));
+  if (slot_ts) CU(cudaMemcpy(slot_ts, c->tab.slot_ts, sizeof(int32_t) * c->C, cudaMemcpyDeviceToHost));
+  return FT_OK;
+}
+
+ft_status ft_get_stats(ft_cache* c, ft_stats* out) {
+  if (!c || !out) return fail(FT_ERR_INVALID_ARG, "null argument");
+  ft_status s = sync_all(c);
+  if (s != FT_OK) return s;
+  long long st[ST_COUNT];
+  CU(cudaMemcpy(st, c->tab.stats, sizeof st, cudaMemcpyDeviceToHost));
+  out->events = st[ST_EVENTS];
+  out->unique_experts = st[ST_UNIQUE];
+  out->hits = st[ST_HITS];
+  out->misses = st[ST_MISSES];
+  out->evictions = st[ST_EVICT];
+  out->bytes_fetched = st[ST_BYTES];
+  out->kernel_launches = c->launches.load();
+  out->memcpy_calls = c->memcpys.load();
+  return device_status(c);
+}
+
+ft_status ft_reset_stats(ft_cache* c) {
+  if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
+  ft_status s = sync_all(c);
+  if (s != FT_OK) return s;
+  CU(cudaMemset(c->tab.stats, 0, sizeof(long long) * ST_COUNT));
+  c->launches = 0;
+  c->memcpys = 0;
+  return FT_OK;
+}
+
+ft_status ft_get_pool(ft_cache* c, void** pool, int64_t* num_slots) {
+  if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
+  if (pool) *pool = c->pool;
+  if (num_slots) *num_slots = c->C;
+  return FT_OK;
+}
+
+ft_status ft_get_copy_stream(ft_cache* c, void** stream) {
+  if (!c || !stream) return fail(FT_ERR_INVALID_ARG, "null argument");
+  *stream = c->copy[0];
+  return FT_OK;
+}
+
+ft_status ft_timing_enable(ft_cache* c, int32_t on) {
+  if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
+  ft_status s = sync_all(c);
+  if (s != FT_OK) return s;
+  for (auto& t : c->timers) t.reset();
+  c->timing = on != 0;
+  return FT_OK;
+}
+
+ft_status ft_get_timing(ft_cache* c, ft_timing* out) {
+  if (!c || !out) return fail(FT_ERR_INVALID_ARG, "null argument");
+  ft_status s = sync_all(c);
+  if (s != FT_OK) return s;
+  for (auto& t : c->timers) t.collect();
+  out->route_ms = c->timers[PHASE_ROUTE].total_ms; out->route_n = c->timers[PHASE_ROUTE].n;
+  out->fetch_ms = c->timers[PHASE_FETCH].total_ms; out->fetch_n = c->timers[PHASE_FETCH].n;
+  out->ffn_ms = c->timers[PHASE_FFN].total_ms; out->ffn_n = c->timers[PHASE_FFN].n;
+  out->gemv_ms = c->timers[PHASE_GEMV].total_ms; out->gemv_n = c->timers[PHASE_GEMV].n;
+  out->down_ms = c->timers[PHASE_DOWN].total_ms; out->down_n = c->timers[PHASE_DOWN].n;
+  return FT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,124 @@
+// Internal declarations of libft: device-side table/plan layouts and the
+// kernel launchers each .cu file provides.  Not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ft.h"
+
+namespace ft {
+
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kDecodeMaxTokens = 8;  // T above this takes the grouped-GEMM path
+
+// Stats slots in the device counter array.
+enum { ST_EVENTS = 0, ST_UNIQUE, ST_HITS, ST_MISSES, ST_EVICT, ST_BYTES, ST_COUNT };
+
+// Plan header words.
+enum { PH_EVENT = 0, PH_TOKENS, PH_UNIQUE, PH_MISS, PH_ROWS, PH_STATUS, PH_WORDS = 8 };
+
+// Global slot tables of one cache (device memory, library-owned).
+struct Tables {
+  int32_t* key_to_slot;  // [L*E]  slot of key l*E+e, -1 = absent
+  int32_t* slot_key;     // [C]    key held by the slot, -1 = empty
+  int32_t* slot_ts;      // [C]    event of last use, -1 = never
+  int32_t* order[2];     // [C]    all slots in ascending (slot_ts, slot); ping-pong buffers
+  int32_t* order_cur;    // [1]    which order buffer is current
+  int32_t* status;       // [1]    sticky device status (ft_status), 0 = ok
+  long long* stats;      // [ST_COUNT]
+  int32_t num_slots;
+};
+
+// One layer's plan (device memory, library-owned), written by route_classify.
+struct Plan {
+  int32_t* hdr;            // [PH_WORDS]
+  int32_t* unique_expert;  // [E]  ascending
+  int32_t* unique_slot;    // [E]
+  int32_t* hit;            // [E]
+  int32_t* miss_expert;    // [E]  ascending
+  int32_t* miss_slot;      // [E]
+  int32_t* evicted_key;    // [E]
+  int32_t* e2u;            // [E]  expert -> index in U, -1 if not selected
+  int32_t* u_count;        // [E]  rows (token, pick) per unique expert
+  int32_t* u_offset;       // [E+1] exclusive prefix of u_count
+  int32_t* rows_by_u;      // [max_rows] row ids t*k+j grouped by unique expert, ascending within a group
+  int32_t* topk_idx;       // [max_rows]
+  float* topk_w;           // [max_rows]
+};
+
+// Scratch of the route_classify kernel: zero before a launch, left zero after it.
+struct RouteScratch {
+  uint32_t* bits;    // [kMaxExperts/32] union of the batch's experts
+  int32_t* counts;   // [kMaxExperts]    picks per expert
+  uint32_t* ticket;  // [1]              CTAs finished
+};
+
+// Miss list mirrored into mapped pinned host memory for the copy-engine mode.
+struct HostMirror {
+  int32_t event;
+  int32_t n_miss;
+  int32_t pad[2];
+  int32_t miss_expert[kMaxExperts];
+  int32_t miss_slot[kMaxExperts];
+};
+
+struct RouteArgs {
+  const float* logits;
+  int T, E, k, layer, event, pin_ts;
+  int32_t* out_idx;  // optional caller outputs
+  float* out_w;
+  Tables tab;
+  Plan plan;
+  RouteScratch scr;
+  HostMirror* mirror;  // device address of the layer's mirror, or null
+  long long expert_bytes;
+  int build_rows;      // 1: the kernel groups rows by expert (small T*k)
+};
+
+cudaError_t launch_route_classify(const RouteArgs& a, cudaStream_t s);
+cudaError_t launch_init_tables(Tables tab, int num_keys, cudaStream_t s);
+
+struct PullArgs {
+  const int32_t* hdr;
+  const int32_t* miss_expert;
+  const int32_t* miss_slot;
+  int layer, E;
+  long long bank_blobs;
+  const void* bank;  // device address of the host bank
+  void* pool;
+  long long expert_bytes;
+};
+cudaError_t launch_pull_misses(const PullArgs& a, int ctas, cudaStream_t s);
+
+struct FfnArgs {
+  const int32_t* hdr;
+  const int32_t* unique_slot;
+  const int32_t* u_offset;
+  const int32_t* rows_by_u;
+  const float* topk_w;
+  const void* x;
+  void* y;
+  const uint8_t* pool;
+  long long expert_bytes;
+  int H, I, k, T, wdtype;
+  float* h;  // [T*k][I] intermediate
+};
+// Decode path: the gate/up+SwiGLU kernel, then the down+combine kernel.
+cudaError_t launch_decode_gateup(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_decode_down(const FfnArgs& a, cudaStream_t s);
+
+struct ResizeArgs {
+  Tables old_tab;
+  Tables new_tab;  // num_slots = C'
+  int num_keys, E;
+  int32_t* moves;     // [2*C'] (old, new) pairs
+  int32_t* n_moves;   // [1]
+  int copy_all;       // 1: pools differ, every survivor moves
+};
+cudaError_t launch_resize_tables(const ResizeArgs& a, cudaStream_t s, int* launches);
+cudaError_t launch_move_blobs(const int32_t* moves, const int32_t* n_moves, int max_moves, const void* src_pool,
+                              void* dst_pool, long long expert_bytes, cudaStream_t s);
+
+}  // namespace ft

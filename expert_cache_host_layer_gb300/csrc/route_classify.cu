@@ -1,0 +1,389 @@
+// route_classify: one kernel per MoE layer event that does the whole routing
+// and cache-decision step with no host sync ("FreeToken: Efficient
+// Edge-Native MoE Serving with Bandwidth-Adaptive Execution", design
+// paragraph: routing dedup, hit classification and LRU victim selection in one
+// GPU kernel, avoiding a per-layer host synchronisation).
+//
+// Phase 1 (all CTAs): one warp per token computes the top-k experts by logit
+// (descending, lower index on ties; NaN ordered as -inf) with k rounds of a
+// warp-wide arg-max, and the gates softmax(selected logits).  Each CTA ORs its
+// tokens' experts into a shared bit set and counts picks per expert, then
+// merges both into global scratch with one atomic per non-zero word/count.
+//
+// Phase 2 (the last CTA to finish, found with an atomic ticket): dedup (the
+// bit set in ascending order is U), hit classification against key_to_slot,
+// global-LRU victims, table updates and the plan.  The LRU order is kept as
+// an explicit list of all slots sorted by (last use, slot).  One pass of
+// block-wide prefix sums over that list finds the first |M| candidates
+// (slots that hold neither a hit of this event nor a slot used by the
+// previous event) and compacts the list without the event's slots; the
+// event's slots, which all get last use = t, are appended in slot order.
+// That keeps the list sorted without ever sorting it.
+#include <cfloat>
+#include <climits>
+
+#include "ft_internal.h"
+
+namespace ft {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// Exclusive block-wide prefix sum of one int per thread; `total` gets the sum.
+__device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int& total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int t = lane < kWarps ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < kWarps) s_warp[lane] = t;
+  }
+  __syncthreads();
+  const int before = w > 0 ? s_warp[w - 1] : 0;
+  total = s_warp[kWarps - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+template <int PL>  // logits per lane: E <= 32 * PL
+__global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
+  __shared__ uint32_t s_bits[kMaxExperts / 32];
+  __shared__ int s_cnt[kMaxExperts];
+  __shared__ int s_warp[kWarps];
+  __shared__ int s_wpre[33];
+  __shared__ int s_uexp[kMaxExperts];
+  __shared__ int s_uslot[kMaxExperts];
+  __shared__ int s_mrank[kMaxExperts];  // miss rank of each unique expert, -1 for hits
+  __shared__ int s_missexp[kMaxExperts];
+  __shared__ int s_victim[kMaxExperts];
+  __shared__ int s_uoff[kMaxExperts];
+  __shared__ int s_flag;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = a.E, k = a.k, T = a.T;
+  const int nwords = (E + 31) >> 5;
+
+  for (int i = tid; i < nwords; i += kThreads) s_bits[i] = 0u;
+  for (int i = tid; i < E; i += kThreads) s_cnt[i] = 0;
+  __syncthreads();
+
+  // ---------------- phase 1: top-k + gates, one warp per token -------------
+  for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
+    const float* row = a.logits + (long long)t * E;
+    float v[PL];
+#pragma unroll
+    for (int q = 0; q < PL; ++q) {
+      const int e = q * 32 + lane;
+      float x = e < E ? __ldg(row + e) : -INFINITY;
+      v[q] = (x != x) ? -INFINITY : x;  // NaN ordered as -inf
+    }
+    uint32_t taken = 0u;
+    float my_v = -INFINITY;
+    int my_i = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+#pragma unroll
+      for (int q = 0; q < PL; ++q) {
+        const int e = q * 32 + lane;
+        if (e < E && !((taken >> q) & 1u) && better(v[q], e, bv, bi)) {
+          bv = v[q];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        my_v = bv;
+        my_i = bi;
+      }
+    }
+    const float m = __shfl_sync(0xffffffffu, my_v, 0);
+    float ex = lane < k ? expf(my_v - m) : 0.0f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane < k) {
+      const float w = ex / sum;
+      const long long r = (long long)t * k + lane;
+      a.plan.topk_idx[r] = my_i;
+      a.plan.topk_w[r] = w;
+      if (a.out_idx) a.out_idx[r] = my_i;
+      if (a.out_w) a.out_w[r] = w;
+      atomicOr(&s_bits[my_i >> 5], 1u << (my_i & 31));
+      atomicAdd(&s_cnt[my_i], 1);
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < nwords; i += kThreads)
+    if (s_bits[i]) atomicOr(&a.scr.bits[i], s_bits[i]);
+  for (int i = tid; i < E; i += kThreads)
+    if (s_cnt[i]) atomicAdd(&a.scr.counts[i], s_cnt[i]);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_flag = (atomicAdd(a.scr.ticket, 1u) == gridDim.x - 1);
+  __syncthreads();
+  if (!s_flag) return;
+  __threadfence();
+
+  // ---------------- phase 2 (last CTA): dedup, classify, victims -----------
+  const int layer = a.layer, C = a.tab.num_slots;
+  for (int i = tid; i < nwords; i += kThreads) s_bits[i] = __ldcg(&a.scr.bits[i]);
+  __syncthreads();
+  if (warp == 0) {
+    int c = lane < nwords ? __popc(s_bits[lane]) : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, c, o);
+      if (lane >= o) c += y;
+    }
+    s_wpre[lane + 1] = c;
+    if (lane == 0) s_wpre[0] = 0;
+  }
+  __syncthreads();
+  const int n_u = s_wpre[nwords];
+  for (int e = tid; e < E; e += kThreads) {
+    const int w = e >> 5, b = e & 31;
+    if ((s_bits[w] >> b) & 1u) {
+      const int u = s_wpre[w] + __popc(s_bits[w] & ((1u << b) - 1u));
+      s_uexp[u] = e;
+      a.plan.e2u[e] = u;
+    } else {
+      a.plan.e2u[e] = -1;
+    }
+  }
+  __syncthreads();
+
+  // hit classification and miss ranks (ascending expert order)
+  int carry = 0;
+  for (int base = 0; base < n_u; base += kThreads) {
+    const int u = base + tid;
+    int is_miss = 0;
+    if (u < n_u) {
+      const int s = a.tab.key_to_slot[layer * E + s_uexp[u]];
+      s_uslot[u] = s;
+      is_miss = s < 0;
+    }
+    int tot;
+    const int r = block_excl_scan(is_miss, s_warp, tot);
+    if (u < n_u) {
+      s_mrank[u] = is_miss ? carry + r : -1;
+      if (is_miss) s_missexp[carry + r] = s_uexp[u];
+    }
+    carry += tot;
+  }
+  const int n_miss = carry;
+
+  // one pass over the LRU order: victims = first n_miss candidates; kept
+  // entries are compacted into the other order buffer
+  const int cur = *a.tab.order_cur;
+  const int32_t* order = a.tab.order[cur];
+  int32_t* norder = a.tab.order[cur ^ 1];
+  int carry_cand = 0, carry_hit = 0;
+  for (int base = 0; base < C; base += kThreads) {
+    const int p = base + tid;
+    int s = -1, cand = 0, hs = 0;
+    if (p < C) {
+      s = order[p];
+      const int key = a.tab.slot_key[s];
+      if (key >= 0 && key / E == layer) {
+        const int e = key - layer * E;
+        hs = (s_bits[e >> 5] >> (e & 31)) & 1u;
+      }
+      cand = !hs && a.tab.slot_ts[s] != a.pin_ts;
+    }
+    int tot;
+    const int packed = block_excl_scan((cand << 16) | hs, s_warp, tot);
+    if (p < C) {
+      const int cand_before = carry_cand + (packed >> 16);
+      const int hit_before = carry_hit + (packed & 0xffff);
+      const bool victim = cand && cand_before < n_miss;
+      if (victim) s_victim[cand_before] = s;
+      if (!hs && !victim) norder[p - hit_before - min(cand_before, n_miss)] = s;
+    }
+    carry_cand += tot >> 16;
+    carry_hit += tot & 0xffff;
+  }
+  __syncthreads();
+
+  if (carry_cand < n_miss) {  // pool too small for this event: leave the tables as they are
+    if (tid == 0) {
+      atomicCAS(a.tab.status, 0, (int)FT_ERR_CAPACITY);
+      a.plan.hdr[PH_STATUS] = (int)FT_ERR_CAPACITY;
+      a.plan.hdr[PH_MISS] = 0;
+      a.plan.hdr[PH_UNIQUE] = 0;
+      if (a.mirror) {
+        a.mirror->n_miss = 0;
+        a.mirror->event = a.event;
+      }
+    }
+  } else {
+    // the event's slots (hits and victims) go to the end in slot order
+    for (int u = tid; u < n_u; u += kThreads) {
+      const int s = s_mrank[u] < 0 ? s_uslot[u] : s_victim[s_mrank[u]];
+      s_uslot[u] = s;
+    }
+    __syncthreads();
+    for (int u = tid; u < n_u; u += kThreads) {
+      const int s = s_uslot[u];
+      int rank = 0;
+      for (int q = 0; q < n_u; ++q) rank += s_uslot[q] < s;
+      norder[C - n_u + rank] = s;
+    }
+    // table updates: victims lose their key, misses take their victim
+    int n_evict = 0;
+    for (int i = tid; i < n_miss; i += kThreads) {
+      const int s = s_victim[i];
+      const int old = a.tab.slot_key[s];
+      a.plan.evicted_key[i] = old;
+      if (old >= 0) {
+        a.tab.key_to_slot[old] = -1;
+        ++n_evict;
+      }
+      const int key = layer * E + s_missexp[i];
+      a.tab.key_to_slot[key] = s;
+      a.tab.slot_key[s] = key;
+      a.plan.miss_expert[i] = s_missexp[i];
+      a.plan.miss_slot[i] = s;
+      if (a.mirror) {
+        a.mirror->miss_expert[i] = s_missexp[i];
+        a.mirror->miss_slot[i] = s;
+      }
+    }
+    for (int u = tid; u < n_u; u += kThreads) {
+      const int s = s_uslot[u];
+      a.tab.slot_ts[s] = a.event;
+      a.plan.unique_expert[u] = s_uexp[u];
+      a.plan.unique_slot[u] = s;
+      a.plan.hit[u] = s_mrank[u] < 0;
+    }
+    // rows per unique expert and their offsets
+    int off = 0;
+    for (int base = 0; base < n_u; base += kThreads) {
+      const int u = base + tid;
+      const int c = u < n_u ? __ldcg(&a.scr.counts[s_uexp[u]]) : 0;
+      int tot;
+      const int r = block_excl_scan(c, s_warp, tot);
+      if (u < n_u) {
+        a.plan.u_count[u] = c;
+        a.plan.u_offset[u] = off + r;
+        s_uoff[u] = off + r;
+      }
+      off += tot;
+    }
+    if (tid == 0) a.plan.u_offset[n_u] = off;
+    __syncthreads();
+    if (a.build_rows) {  // small T*k (<= kMaxExperts): rank each row among the rows of its expert
+      const int rows = T * k;
+      for (int r = tid; r < rows; r += kThreads) s_cnt[r] = __ldcg(&a.plan.e2u[__ldcg(&a.plan.topk_idx[r])]);
+      __syncthreads();
+      for (int r = tid; r < rows; r += kThreads) {
+        const int u = s_cnt[r];
+        int before = 0;
+        for (int q = 0; q < r; ++q) before += s_cnt[q] == u;
+        a.plan.rows_by_u[s_uoff[u] + before] = r;
+      }
+    }
+    // evictions: reduce the per-thread counts
+    int tot_evict;
+    block_excl_scan(n_evict, s_warp, tot_evict);
+    if (tid == 0) {
+      a.plan.hdr[PH_EVENT] = a.event;
+      a.plan.hdr[PH_TOKENS] = T;
+      a.plan.hdr[PH_UNIQUE] = n_u;
+      a.plan.hdr[PH_MISS] = n_miss;
+      a.plan.hdr[PH_ROWS] = T * k;
+      a.plan.hdr[PH_STATUS] = 0;
+      long long* st = a.tab.stats;
+      st[ST_EVENTS] += 1;
+      st[ST_UNIQUE] += n_u;
+      st[ST_HITS] += n_u - n_miss;
+      st[ST_MISSES] += n_miss;
+      st[ST_EVICT] += tot_evict;
+      st[ST_BYTES] += (long long)n_miss * a.expert_bytes;
+      if (a.mirror) {
+        a.mirror->n_miss = n_miss;
+        a.mirror->event = a.event;
+      }
+      *a.tab.order_cur = cur ^ 1;
+    }
+  }
+  if (a.mirror) __threadfence_system();
+  // leave the scratch zeroed for the next launch
+  for (int i = tid; i < nwords; i += kThreads) a.scr.bits[i] = 0u;
+  for (int i = tid; i < E; i += kThreads) a.scr.counts[i] = 0;
+  if (tid == 0) *a.scr.ticket = 0u;
+}
+
+__global__ void init_tables_kernel(Tables tab, int num_keys) {
+  const int stride = gridDim.x * blockDim.x;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < num_keys; i += stride) tab.key_to_slot[i] = -1;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < tab.num_slots; i += stride) {
+    tab.slot_key[i] = -1;
+    tab.slot_ts[i] = -1;
+    tab.order[0][i] = i;  // all slots empty: (ts = -1, slot) order is slot order
+    tab.order[1][i] = i;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *tab.order_cur = 0;
+    *tab.status = 0;
+    for (int i = 0; i < ST_COUNT; ++i) tab.stats[i] = 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route_classify(const RouteArgs& a, cudaStream_t s) {
+  const int warps_needed = (a.T + kWarps - 1) / kWarps;
+  int grid = warps_needed < 1 ? 1 : warps_needed;
+  if (grid > 4 * 152) grid = 4 * 152;
+  const int pl = (a.E + 31) / 32;
+  if (pl <= 1)
+    route_classify_kernel<1><<<grid, kThreads, 0, s>>>(a);
+  else if (pl <= 2)
+    route_classify_kernel<2><<<grid, kThreads, 0, s>>>(a);
+  else if (pl <= 4)
+    route_classify_kernel<4><<<grid, kThreads, 0, s>>>(a);
+  else if (pl <= 8)
+    route_classify_kernel<8><<<grid, kThreads, 0, s>>>(a);
+  else if (pl <= 16)
+    route_classify_kernel<16><<<grid, kThreads, 0, s>>>(a);
+  else
+    route_classify_kernel<32><<<grid, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_init_tables(Tables tab, int num_keys, cudaStream_t s) {
+  int n = num_keys > tab.num_slots ? num_keys : tab.num_slots;
+  int grid = (n + 255) / 256;
+  if (grid > 1024) grid = 1024;
+  if (grid < 1) grid = 1;
+  init_tables_kernel<<<grid, 256, 0, s>>>(tab, num_keys);
+  return cudaGetLastError();
+}
+
+}  // namespace ft

@@ -1,0 +1,135 @@
+"""Per-step driver over the C ABI: owns the pinned host bank, the device slot
+pool and the cache handle, and runs the layer schedule.
+
+Double-buffered schedule of one step (misses of layer l+1 stream in on the
+copy stream while layer l's FFN runs - "FreeToken: Efficient Edge-Native MoE
+Serving ...", ablation paragraph):
+
+    route(0); fetch(0)
+    for l in 0..L-1:  route(l+1); fetch(l+1); forward(l)
+
+Serial schedule (double buffering off): route(l); fetch(l); forward(l).
+
+PyTorch only allocates memory and provides the compute stream; every step of
+the path runs in libft's kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (FT_FETCH_SM_PULL, FT_W_F32, ft_cache_create, ft_cache_destroy, ft_cache_resize, ft_expert_bytes,
+               ft_fetch_misses, ft_get_copy_stream, ft_get_plan, ft_get_stats, ft_get_tables, ft_get_timing,
+               ft_moe_forward, ft_reset_stats, ft_route_classify, ft_synchronize, ft_timing_enable, make_config)
+
+
+class ExpertCache:
+    """A libft cache with its host bank and device slot pool."""
+
+    def __init__(self, num_layers, num_experts, top_k, hidden, inter, wdtype, num_slots, max_tokens, bank,
+                 bank_blobs=None, fetch_mode=FT_FETCH_SM_PULL, pull_ctas=0, copy_streams=1, device="cuda:0",
+                 stream: torch.cuda.Stream | None = None):
+        self.L, self.E, self.k, self.H, self.I = num_layers, num_experts, top_k, hidden, inter
+        self.wdtype = wdtype
+        self.eb = ft_expert_bytes(hidden, inter, wdtype)
+        if self.eb == 0:
+            raise ValueError("unsupported expert shape")
+        self.device = torch.device(device)
+        self.bank = bank  # torch uint8 tensor in (pinned) host memory, [bank_blobs * expert_bytes]
+        self.bank_blobs = bank_blobs or num_layers * num_experts
+        self.stream = stream or torch.cuda.current_stream(self.device)
+        self.act_dtype = torch.float32 if wdtype == FT_W_F32 else torch.bfloat16
+        self.pool = torch.empty(num_slots * self.eb, dtype=torch.uint8, device=self.device)
+        self.num_slots = num_slots
+        cfg = make_config(num_layers, num_experts, top_k, hidden, inter, wdtype, bank.data_ptr(),
+                          bank.numel() * bank.element_size(), self.bank_blobs, max_tokens, fetch_mode, pull_ctas,
+                          copy_streams)
+        self.handle = ft_cache_create(cfg, self.pool.data_ptr(), num_slots, self.stream.cuda_stream)
+        self.copy_stream = torch.cuda.ExternalStream(ft_get_copy_stream(self.handle), device=self.device)
+
+    # ---- thin wrappers ---------------------------------------------------
+    def route_classify(self, layer, logits: torch.Tensor, topk_idx=None, topk_w=None):
+        T = logits.shape[0] if logits.dim() == 2 else 0
+        ft_route_classify(self.handle, layer, logits.data_ptr() if T else 0, T,
+                          topk_idx.data_ptr() if topk_idx is not None else 0,
+                          topk_w.data_ptr() if topk_w is not None else 0)
+
+    def fetch_misses(self, layer):
+        ft_fetch_misses(self.handle, layer)
+
+    def moe_forward(self, layer, x: torch.Tensor, y: torch.Tensor):
+        T = x.shape[0]
+        ft_moe_forward(self.handle, layer, x.data_ptr() if T else 0, T, y.data_ptr() if T else 0)
+
+    def resize(self, new_num_slots, new_pool: torch.Tensor | None = None):
+        """Safe-point resize; shrinking keeps the same pool (in place) unless new_pool is given."""
+        if new_pool is None:
+            if new_num_slots <= self.num_slots:
+                new_pool = self.pool
+            else:
+                new_pool = torch.empty(new_num_slots * self.eb, dtype=torch.uint8, device=self.device)
+        ft_cache_resize(self.handle, new_pool.data_ptr(), new_num_slots)
+        self.pool, self.num_slots = new_pool, new_num_slots
+
+    def synchronize(self):
+        ft_synchronize(self.handle)
+
+    def plan(self, layer):
+        return ft_get_plan(self.handle, layer, self.E)
+
+    def tables(self):
+        return ft_get_tables(self.handle, self.L * self.E, self.num_slots)
+
+    def stats(self):
+        return ft_get_stats(self.handle)
+
+    def reset_stats(self):
+        ft_reset_stats(self.handle)
+
+    def timing_enable(self, on=True):
+        ft_timing_enable(self.handle, on)
+
+    def timing(self):
+        return ft_get_timing(self.handle)
+
+    def close(self):
+        if self.handle:
+            ft_cache_destroy(self.handle)
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---- one step over all layers ------------------------------------------
+    def run_step(self, logits, xs, ys, double_buffer=True, topk_idx=None, topk_w=None, after_event=None):
+        """logits[l]: [T,E] f32, xs[l], ys[l]: [T,H] device tensors for each layer l.
+
+        `after_event(layer)` (tests) is called right after each layer's
+        route_classify is enqueued.
+        """
+        L = self.L
+
+        def route(l):
+            self.route_classify(l, logits[l], None if topk_idx is None else topk_idx[l],
+                                None if topk_w is None else topk_w[l])
+            if after_event is not None:
+                after_event(l)
+            self.fetch_misses(l)
+
+        if double_buffer:
+            route(0)
+            for l in range(L):
+                if l + 1 < L:
+                    route(l + 1)
+                self.moe_forward(l, xs[l], ys[l])
+        else:
+            for l in range(L):
+                route(l)
+                self.moe_forward(l, xs[l], ys[l])
+
+
+def pinned_bank(nbytes: int) -> torch.Tensor:
+    """A pinned host byte buffer for the expert bank."""
+    return torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)

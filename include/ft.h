@@ -1,0 +1,252 @@
+/*
+ * ft.h - C ABI of libft, the GB300 (sm_103a) hot path of a two-tier MoE
+ * expert-offload engine: the full routed-expert bank stays in host memory and
+ * one GPU expert cache, shared by every MoE layer and keyed by
+ * (layer, expert), holds the experts the FFN reads.
+ *
+ * Source of the method: "FreeToken: Efficient Edge-Native MoE Serving with
+ * Bandwidth-Adaptive Execution" (paper summary page), design paragraph
+ * (two-tier expert memory; an elastic expert cache shared by all MoE layers,
+ * slots managed by logical (layer, expert) id; routing dedup, hit
+ * classification and LRU victim selection in one GPU kernel with no per-layer
+ * host sync; cache rebuilt at scheduler safe points when the VRAM budget
+ * changes; weights stored in the runtime layout) and ablation paragraph
+ * (global LRU; double buffering of expert transfers); "FreeToken: az VRAM ile
+ * büyük MoE modelleri", intro (experts in host RAM, an LRU expert cache on the
+ * GPU, misses streamed over the host link).
+ *
+ * Conventions
+ * - Every call returns ft_status; FT_OK is 0.  No call throws.  On an error
+ *   ft_last_error() returns a message for the calling thread.
+ * - Pointers named "device" must point to device memory of the cache's GPU;
+ *   "host" pointers to host memory.  The caller owns every buffer it passes;
+ *   the library owns what it allocates (tables, plans, scratch, streams,
+ *   events) and frees it in ft_cache_destroy.
+ * - Stream handles are cudaStream_t values passed as void*.
+ * - Calls that enqueue GPU work are asynchronous: they return once the work
+ *   is enqueued.  Calls marked "synchronous" wait for the cache's streams.
+ * - One host thread drives one ft_cache.  Calls on one cache must not
+ *   overlap.
+ * - Device-side failures (a capacity shortfall, a bounds check, a bounded
+ *   wait that ran out) cannot be reported by the call that enqueued them;
+ *   they set a sticky device status that the next synchronous call
+ *   (ft_synchronize, ft_get_stats, ...) returns.
+ */
+#ifndef FT_H_
+#define FT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ft_status {
+  FT_OK = 0,
+  FT_ERR_INVALID_ARG = 1, /* bad shape, pointer, layer or size */
+  FT_ERR_CUDA = 2,        /* a CUDA runtime call failed; see ft_last_error() */
+  FT_ERR_OOM = 3,         /* a library allocation failed */
+  FT_ERR_CAPACITY = 4,    /* fewer victim slots than misses (pool too small) */
+  FT_ERR_STATE = 5,       /* call out of order (forward before fetch, ...) */
+  FT_ERR_TIMEOUT = 6,     /* a bounded wait ran out */
+  FT_ERR_CHECKED = 7,     /* a device-side bounds check failed */
+  FT_ERR_UNSUPPORTED = 8  /* shape or mode this build does not implement */
+} ft_status;
+
+/* Expert weight formats.  Activations (x, y) are float32 for FT_W_F32 and
+ * bf16 for the other two. */
+typedef enum ft_wdtype {
+  FT_W_F32 = 0,
+  FT_W_BF16 = 1,
+  FT_W_FP8E4M3_B128 = 2 /* OCP e4m3 weights, one bf16 scale per 128x128 block */
+} ft_wdtype;
+
+typedef enum ft_fetch_mode {
+  FT_FETCH_COPY_ENGINE = 0, /* cudaMemcpyAsync per miss, issued by a library host thread */
+  FT_FETCH_SM_PULL = 1      /* a kernel on the copy stream loads the blobs over the host link */
+} ft_fetch_mode;
+
+/*
+ * Expert blob = the runtime layout of one routed expert, identical in the
+ * host bank and in a device slot:
+ *   Wg [inter][hidden] | Wu [inter][hidden] | Wd [hidden][inter]
+ * row-major, element type per ft_wdtype; for FT_W_FP8E4M3_B128 followed by
+ * bf16 scales, one per 128x128 block of each matrix ([out][in] blocks,
+ * row-block major) in the order Wg, Wu, Wd.
+ * The FFN of expert e on token x is  Wd (silu(Wg x) * (Wu x)).
+ */
+typedef struct ft_cache_config {
+  int32_t num_layers;  /* L: MoE layers sharing the cache */
+  int32_t num_experts; /* E: routed experts per layer, 1..1024 */
+  int32_t top_k;       /* k: experts per token, 1..min(E, 32) */
+  int32_t hidden;      /* H: multiple of 128 (of 8 for FT_W_F32) */
+  int32_t inter;       /* I: multiple of 128 (of 8 for FT_W_F32) */
+  int32_t wdtype;      /* ft_wdtype */
+  const void* host_bank;     /* host: [bank_blobs][expert_bytes]; pinned, or registered by create */
+  uint64_t host_bank_bytes;  /* >= bank_blobs * expert_bytes */
+  int64_t bank_blobs;        /* physical blobs; key (l, e) reads blob (l*E + e) mod bank_blobs.
+                                L*E for a full bank; fewer aliases blobs to save host RAM */
+  int32_t max_tokens;        /* largest T passed to ft_route_classify / ft_moe_forward */
+  int32_t fetch_mode;        /* ft_fetch_mode */
+  int32_t pull_ctas;         /* CTAs of the SM-pull fetch kernel; 0 = library default */
+  int32_t copy_streams;      /* copy-engine mode: 1 or 2 streams the misses alternate over; 0 = 1 */
+} ft_cache_config;
+
+typedef struct ft_cache ft_cache; /* opaque, library-owned */
+
+/* Counters accumulated since create (or the last ft_reset_stats). */
+typedef struct ft_stats {
+  int64_t events;          /* layer events classified */
+  int64_t unique_experts;  /* sum over events of |U| */
+  int64_t hits;            /* sum of |H| */
+  int64_t misses;          /* sum of |M| */
+  int64_t evictions;       /* misses that replaced an occupied slot, plus resize drops */
+  int64_t bytes_fetched;   /* misses * expert_bytes */
+  int64_t kernel_launches; /* kernels this library launched */
+  int64_t memcpy_calls;    /* cudaMemcpyAsync calls issued for misses */
+} ft_stats;
+
+/* Per-phase GPU time from CUDA events recorded around the library's own
+ * launches (enabled by ft_timing_enable); milliseconds and counts. */
+typedef struct ft_timing {
+  double route_ms;  int64_t route_n;   /* route_classify kernel, compute stream */
+  double fetch_ms;  int64_t fetch_n;   /* miss copies, copy stream (first to last copy of a layer) */
+  double ffn_ms;    int64_t ffn_n;     /* expert FFN kernels of one ft_moe_forward, compute stream */
+  double gemv_ms;   int64_t gemv_n;    /* decode gate/up kernel alone */
+  double down_ms;   int64_t down_n;    /* decode down/combine kernel alone */
+} ft_timing;
+
+/* Header of one layer's plan (see ft_get_plan). */
+typedef struct ft_plan_info {
+  int32_t event;     /* event number t of the classification */
+  int32_t n_tokens;  /* T */
+  int32_t n_unique;  /* |U| */
+  int32_t n_miss;    /* |M| */
+} ft_plan_info;
+
+/* Bytes of one expert blob; 0 for an unsupported shape. */
+size_t ft_expert_bytes(int32_t hidden, int32_t inter, int32_t wdtype);
+
+/*
+ * Create a cache over `num_slots` slots of the caller's device pool
+ * `slot_pool` ([num_slots][expert_bytes], device, 256-byte aligned, owned by
+ * the caller and valid until destroy or the next resize).  The cache starts
+ * empty.  `compute_stream` (cudaStream_t, may be NULL for the legacy default
+ * stream) receives the routing and FFN kernels; the library creates its own
+ * copy stream(s).  Registers the host bank with CUDA if it is not pinned
+ * (and unregisters it on destroy).  Synchronous.
+ * Errors: FT_ERR_INVALID_ARG (shapes, null pointers, bank too small,
+ * expert_bytes not a multiple of 16), FT_ERR_CAPACITY when num_slots <
+ * 2 * min(max_tokens * top_k, num_experts) (the pool could not hold one
+ * event's experts plus the previous event's pinned ones), FT_ERR_OOM,
+ * FT_ERR_CUDA.
+ */
+ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t num_slots, void* compute_stream,
+                          ft_cache** out);
+
+/* Destroy a cache: waits for its streams, frees library memory.  NULL is a
+ * no-op. */
+ft_status ft_cache_destroy(ft_cache* cache);
+
+/*
+ * Resize the cache at a safe point ("rebuilt at scheduler safe points when
+ * the VRAM budget changes").  Synchronous: waits for both streams first.
+ * Keeps the min(occupied, new_num_slots) entries that LRU would evict last;
+ * survivors in slots < new_num_slots stay put, the others move (in ascending
+ * old-slot order) to the lowest free slots; last-use times are kept.  When
+ * `new_pool` differs from the current pool every survivor is copied into it
+ * (the old pool must stay valid until the call returns); when it is the same
+ * pointer, blobs move in place.  The first event after a resize pins nothing.
+ * Errors: FT_ERR_INVALID_ARG, FT_ERR_CAPACITY (same bound as create),
+ * FT_ERR_STATE (a fetch is still pending), FT_ERR_CUDA, FT_ERR_OOM.
+ */
+ft_status ft_cache_resize(ft_cache* cache, void* new_pool, int64_t new_num_slots);
+
+/*
+ * Route one layer's token batch and update the cache, in one kernel on the
+ * compute stream: top-k + gates per token, dedup of the batch's experts,
+ * hit/miss classification, global-LRU victims for the misses, table update.
+ *   logits   device, float32 [T][E], row-major
+ *   topk_idx device, int32 [T][k] or NULL: experts per token in selection
+ *            order (logit descending, lower index first on ties)
+ *   topk_w   device, float32 [T][k] or NULL: softmax over the k selected logits
+ * The event number t increments by one per call.  Victims are the least
+ * recently used slots excluding this event's hits and the previous event's
+ * slots (which the previous layer's FFN may still read).  T may be 0.
+ * Errors: FT_ERR_INVALID_ARG (layer, T > max_tokens, null logits),
+ * FT_ERR_STATE (this layer's previous plan is still being fetched and its
+ * fetch failed), FT_ERR_CUDA.
+ */
+ft_status ft_route_classify(ft_cache* cache, int32_t layer, const float* logits, int32_t T, int32_t* topk_idx,
+                            float* topk_w);
+
+/*
+ * Copy the layer's misses (from its last ft_route_classify) from the host
+ * bank into their victim slots, on the copy stream, after the classification
+ * completes.  Asynchronous; the compute stream does not wait here (so the
+ * next layer's misses can stream while this layer computes).
+ * Errors: FT_ERR_INVALID_ARG, FT_ERR_STATE (no classification pending for
+ * this layer), FT_ERR_CUDA.
+ */
+ft_status ft_fetch_misses(ft_cache* cache, int32_t layer);
+
+/*
+ * The layer's MoE FFN on the compute stream, reading expert weights from the
+ * cache slots:  y[t] = sum_j topk_w[t][j] * Wd h,  h = silu(Wg x[t]) * (Wu x[t]).
+ *   x  device [T][H]: float32 for FT_W_F32, bf16 otherwise
+ *   y  device [T][H]: same type as x; fully overwritten
+ * T must equal the T of the layer's last ft_route_classify.  The compute
+ * stream first waits for the layer's fetch.  T <= 8 runs the decode GEMV
+ * kernels; larger T the grouped tensor-core GEMM path.
+ * Errors: FT_ERR_INVALID_ARG, FT_ERR_STATE (no fetch issued for the layer's
+ * current plan), FT_ERR_UNSUPPORTED, FT_ERR_CUDA.
+ */
+ft_status ft_moe_forward(ft_cache* cache, int32_t layer, const void* x, int32_t T, void* y);
+
+/* Wait for the compute and copy streams; returns the sticky device status
+ * (FT_ERR_CAPACITY, FT_ERR_CHECKED, FT_ERR_TIMEOUT) if one was raised.
+ * Synchronous. */
+ft_status ft_synchronize(ft_cache* cache);
+
+/*
+ * Copy a layer's current plan to host (synchronous; test and debug use).
+ * Any array pointer may be NULL.  Host arrays must hold num_experts entries.
+ *   unique_expert  ascending experts of U        unique_slot  slot of each after the event
+ *   hit            1 = hit, 0 = miss             miss_expert  ascending misses
+ *   miss_slot      victim slot of each miss      evicted_key  key (l*E+e) the victim held, -1 if empty
+ */
+ft_status ft_get_plan(ft_cache* cache, int32_t layer, ft_plan_info* info, int32_t* unique_expert,
+                      int32_t* unique_slot, uint8_t* hit, int32_t* miss_expert, int32_t* miss_slot,
+                      int32_t* evicted_key);
+
+/* Copy the slot tables to host (synchronous).  key_to_slot: [L*E] (-1 =
+ * absent); slot_key, slot_ts: [num_slots] (-1 = empty / never used).  Any
+ * pointer may be NULL. */
+ft_status ft_get_tables(ft_cache* cache, int32_t* key_to_slot, int32_t* slot_key, int32_t* slot_ts);
+
+/* Counters (synchronous). */
+ft_status ft_get_stats(ft_cache* cache, ft_stats* out);
+ft_status ft_reset_stats(ft_cache* cache);
+
+/* Current number of slots and pool pointer. */
+ft_status ft_get_pool(ft_cache* cache, void** pool, int64_t* num_slots);
+
+/* The copy stream (cudaStream_t as void*) the miss copies run on (the
+ * first one when copy_streams is 2). */
+ft_status ft_get_copy_stream(ft_cache* cache, void** stream);
+
+/* Enable (1) or disable (0) per-phase CUDA-event timing; enabling clears the
+ * totals.  ft_get_timing waits for the streams and returns the totals. */
+ft_status ft_timing_enable(ft_cache* cache, int32_t on);
+ft_status ft_get_timing(ft_cache* cache, ft_timing* out);
+
+const char* ft_status_str(ft_status s);
+/* Message of the calling thread's last error ("" if none). */
+const char* ft_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FT_H_ */

@@ -144,10 +144,12 @@ static void* range_thread(void* p) {
   j->fn(j->ctx, j->lo, j->hi);
   return NULL;
 }
-static void parallel_for(range_fn fn, void* ctx, int64_t n, int threads) {
+/* Runs fn over [0, n) split into `threads` ranges; below `min_items` items
+ * the call stays on the calling thread (thread start-up would dominate). */
+static void parallel_for(range_fn fn, void* ctx, int64_t n, int threads, int64_t min_items) {
   if (threads < 1) threads = 1;
   if (threads > 256) threads = 256;
-  if (n < 2 || threads == 1) { fn(ctx, 0, n); return; }
+  if (n < min_items || n < 2 || threads == 1) { fn(ctx, 0, n); return; }
   if (threads > n) threads = (int)n;
   pthread_t tid[256];
   range_job jobs[256];
@@ -173,7 +175,7 @@ static void normal_range(void* p, int64_t lo, int64_t hi) {
 /* out[i] = scale * N_(start+i) of stream `key` */
 void synth_normal_f32(uint64_t key, uint64_t start, int64_t n, float scale, float* out, int threads) {
   normal_ctx c = {key, start, scale, out};
-  parallel_for(normal_range, &c, n, threads);
+  parallel_for(normal_range, &c, n, threads, 1 << 16);
 }
 
 /* ---- expert weight blobs ------------------------------------------------ */
@@ -269,7 +271,7 @@ int synth_expert_blobs(uint64_t seed, int hidden, int inter, int wdtype, const i
   int64_t eb = synth_expert_bytes(hidden, inter, wdtype);
   if (eb <= 0) return -1;
   bank_ctx c = {seed, hidden, inter, wdtype, blob_ids, out, eb};
-  parallel_for(bank_range, &c, n_blobs, threads);
+  parallel_for(bank_range, &c, n_blobs, threads, 2);
   return 0;
 }
 
@@ -370,7 +372,7 @@ void synth_router_iid(uint64_t seed, int stream, int layer, int T, int E, double
     synth_zipf_bias(seed, layer, E, zipf_a, bias);
   }
   iid_ctx c = {synth_key(seed, 0x11D0, (uint64_t)stream, (uint64_t)layer, 0), E, bias, out};
-  parallel_for(iid_range, &c, (int64_t)T * E, threads);
+  parallel_for(iid_range, &c, (int64_t)T * E, threads, 1 << 16);
   free(bias);
 }
 
@@ -385,7 +387,7 @@ void synth_hidden(uint64_t seed, int stream, int step, int layer, int T, int H, 
                   int threads) {
   uint64_t key = synth_key(seed, 0x4AD0, (uint64_t)stream, (uint64_t)step, (uint64_t)layer);
   normal_ctx c = {key, 0, 1.0f, out};
-  parallel_for(normal_range, &c, (int64_t)T * H, threads);
+  parallel_for(normal_range, &c, (int64_t)T * H, threads, 1 << 16);
   if (round_bf16)
     for (int64_t i = 0; i < (int64_t)T * H; ++i) out[i] = bf16_to_f32(f32_to_bf16(out[i]));
 }

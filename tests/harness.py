@@ -1,0 +1,173 @@
+"""Side-by-side runner for the GPU parity tests: the CUDA path through the C
+ABI on one side, the CPU oracle on the other, on the same seeded inputs.
+
+Nothing here feeds a GPU result into the oracle: the oracle sees only the
+generated logits, hidden states and host-bank bytes.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+import synth
+from oracle import ffn as offn
+from oracle import routing as orouting
+from oracle.cache import ExpertCacheOracle
+from synth import workloads as W
+
+TOL = {synth.W_F32: 1e-4, synth.W_BF16: 2e-2, synth.W_FP8: 2e-2}
+
+
+def make_bank(w: W.Workload, blobs: int | None = None) -> tuple[torch.Tensor, int]:
+    """Pinned host bank of `blobs` generated expert blobs (aliased when < L*E)."""
+    from expert_cache_host_layer_gb300.pipeline import pinned_bank
+    n = blobs or w.blobs
+    bank = pinned_bank(n * w.expert_bytes)
+    synth.expert_blobs(w.seed, w.hidden, w.inter, w.wdtype, np.arange(n), out_ptr=bank.data_ptr())
+    return bank, n
+
+
+def bank_blob(bank: torch.Tensor, w: W.Workload, n_blobs: int, layer: int, expert: int) -> np.ndarray:
+    b = (layer * w.num_experts + expert) % n_blobs
+    eb = w.expert_bytes
+    return bank.numpy()[b * eb:(b + 1) * eb]
+
+
+def to_act(x: np.ndarray, w: W.Workload, device) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(device=device, dtype=torch.float32 if w.wdtype == synth.W_F32 else torch.bfloat16)
+
+
+@dataclasses.dataclass
+class Mismatch:
+    what: str
+    event: int
+    detail: str
+
+
+def compare_event(plan, ev, gpu_idx, ref_idx, gpu_w, ref_w):
+    errs = []
+    if not np.array_equal(gpu_idx, ref_idx):
+        errs.append(("topk_idx", f"{gpu_idx.tolist()} != {ref_idx.tolist()}"))
+    if gpu_w is not None and not np.allclose(gpu_w, ref_w, rtol=0, atol=2e-6):
+        errs.append(("topk_w", f"max diff {np.abs(gpu_w - ref_w).max()}"))
+    for name, g, r in (("event", plan["event"], ev.t), ("unique", plan["unique"], ev.unique),
+                       ("hit", plan["hit"], ev.hit), ("unique_slot", plan["unique_slot"], ev.unique_slot),
+                       ("miss_expert", plan["miss_expert"], ev.miss_expert),
+                       ("miss_slot", plan["miss_slot"], ev.miss_slot),
+                       ("evicted_key", plan["evicted_key"], ev.evicted_key)):
+        if not np.array_equal(np.asarray(g), np.asarray(r)):
+            errs.append((name, f"gpu {np.asarray(g).tolist()} vs oracle {np.asarray(r).tolist()}"))
+    return errs
+
+
+def ffn_error(y_gpu: np.ndarray, y_ref: np.ndarray) -> tuple[float, float]:
+    """(max |diff| / RMS(ref), RMS(diff) / RMS(ref))."""
+    rms = float(np.sqrt(np.mean(y_ref ** 2))) or 1.0
+    d = y_gpu.astype(np.float64) - y_ref
+    return float(np.abs(d).max() / rms), float(np.sqrt(np.mean(d ** 2)) / rms)
+
+
+def oracle_ffn(w: W.Workload, bank, n_blobs, layer, x, idx, gates):
+    cache = {}
+
+    def weights_of(e):
+        if e not in cache:
+            cache[e] = offn.dequant_blob(bank_blob(bank, w, n_blobs, layer, e), w.hidden, w.inter, w.wdtype)
+        return cache[e]
+
+    return offn.moe_ffn(x.astype(np.float64), idx, gates, weights_of)
+
+
+def run_parity(w: W.Workload, steps: int | None = None, fetch_mode: int = 1, double_buffer: bool = True,
+               bank_blobs: int | None = None, check_tables_every: int = 1, ffn_every: int = 1,
+               check_slots: bool = True, copy_streams: int = 1, logits=None, device="cuda:0"):
+    """Run `steps` decode steps of workload w through libft and the oracle.
+
+    Returns a report dict; raises AssertionError on the first decision mismatch.
+    """
+    from expert_cache_host_layer_gb300.pipeline import ExpertCache
+    steps = steps or w.steps
+    dev = torch.device(device)
+    bank, n_blobs = make_bank(w, bank_blobs)
+    if logits is None:
+        logits = W.router_logits(w.replace(steps=steps))
+    cache = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots,
+                        max(w.tokens, 1), bank, n_blobs, fetch_mode=fetch_mode, copy_streams=copy_streams,
+                        device=device)
+    ref = ExpertCacheOracle(w.num_layers, w.num_experts, w.num_slots)
+    L, T, k = w.num_layers, w.tokens, w.top_k
+    idx_d = [torch.empty((T, k), dtype=torch.int32, device=dev) for _ in range(L)]
+    wt_d = [torch.empty((T, k), dtype=torch.float32, device=dev) for _ in range(L)]
+    ys = [torch.empty((T, w.hidden), dtype=cache.act_dtype, device=dev) for _ in range(L)]
+    report = {"events": 0, "ffn_checked": 0, "max_err": 0.0, "max_rms_err": 0.0, "slots_checked": 0}
+    ev_counter = [0]
+    step_state = {}
+
+    try:
+        for s in range(steps):
+            if s == w.resize_step:
+                cache.resize(w.resize_slots)
+                moves = ref.resize(w.resize_slots)
+                k2s, sk, ts = cache.tables()
+                rk2s, rsk, rts = ref.tables()
+                assert np.array_equal(k2s, rk2s) and np.array_equal(sk, rsk) and np.array_equal(ts, rts), \
+                    "tables differ after resize"
+                report["resize_moves"] = len(moves)
+            lg_d = [torch.from_numpy(np.ascontiguousarray(logits[s, l])).to(dev) for l in range(L)]
+            xs_h = [W.hidden_states(w, s, l) for l in range(L)]
+            xs = [to_act(xs_h[l], w, dev) for l in range(L)]
+            refs = {}
+
+            def after_event(l, s=s):
+                t = ev_counter[0]
+                ridx, rw = orouting.route(logits[s, l], k)
+                ev = ref.event(l, ridx)
+                refs[l] = (ridx, rw, ev)
+                plan = cache.plan(l)
+                torch.cuda.synchronize(dev)
+                errs = compare_event(plan, ev, idx_d[l].cpu().numpy(), ridx, wt_d[l].cpu().numpy(), rw)
+                assert not errs, f"event {t} (step {s}, layer {l}): {errs[:3]}"
+                if check_tables_every and t % check_tables_every == 0:
+                    k2s, sk, ts = cache.tables()
+                    rk2s, rsk, rts = ref.tables()
+                    assert np.array_equal(k2s, rk2s), f"event {t}: key_to_slot differs"
+                    assert np.array_equal(sk, rsk), f"event {t}: slot_key differs"
+                    assert np.array_equal(ts, rts), f"event {t}: slot_ts differs"
+                ev_counter[0] += 1
+
+            cache.run_step(lg_d, xs, ys, double_buffer=double_buffer, topk_idx=idx_d, topk_w=wt_d,
+                           after_event=after_event)
+            cache.synchronize()
+            for l in range(L):
+                t = refs[l][2].t
+                if ffn_every and t % ffn_every == 0:
+                    ridx, rw, ev = refs[l]
+                    yr = oracle_ffn(w, bank, n_blobs, l, xs_h[l], ridx, rw)
+                    yg = ys[l].float().cpu().numpy()
+                    mx, rm = ffn_error(yg, yr)
+                    report["max_err"] = max(report["max_err"], mx)
+                    report["max_rms_err"] = max(report["max_rms_err"], rm)
+                    report["ffn_checked"] += 1
+                    assert mx <= TOL[w.wdtype], f"event {t}: FFN max err {mx:.3e} x RMS > {TOL[w.wdtype]}"
+            if check_slots:  # slots filled this step hold their key's blob, byte for byte
+                _, rsk, rts = ref.tables()
+                first = refs[0][2].t
+                touched = np.flatnonzero(rts >= first)
+                for slot in touched[:: max(1, len(touched) // 3)][:4].tolist():
+                    key = int(rsk[slot])
+                    got = cache.pool[slot * w.expert_bytes:(slot + 1) * w.expert_bytes].cpu().numpy()
+                    want = bank_blob(bank, w, n_blobs, key // w.num_experts, key % w.num_experts)
+                    assert np.array_equal(got, want), f"step {s}: slot {slot} bytes differ from key {key}'s blob"
+                    report["slots_checked"] += 1
+        st = cache.stats()
+        report["events"] = ev_counter[0]
+        report["stats"] = st
+        report["miss_rate"] = st["misses"] / max(1, st["unique_experts"])
+        assert st["misses"] == ref.n_miss and st["hits"] == ref.n_hit and st["unique_experts"] == ref.n_unique
+        assert st["evictions"] == ref.n_evict, (st["evictions"], ref.n_evict)
+    finally:
+        cache.close()
+    return report

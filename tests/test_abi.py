@@ -1,0 +1,62 @@
+"""CPU checks of the C-ABI boundary: the library builds, loads without a GPU,
+exports every function include/ft.h declares, and the Python binding exposes
+the same names.  No compute call is made here."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ft.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(ft_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    if not shutil.which("nvcc") and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    import __graft_entry__
+    return __graft_entry__._build_module().build()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("ft_cache_create", "ft_cache_resize", "ft_route_classify", "ft_fetch_misses",
+                     "ft_moe_forward", "ft_cache_destroy"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_has_the_same_names(lib_path):
+    import expert_cache_host_layer_gb300 as ft
+    for n in declared_functions():
+        assert hasattr(ft, n), n
+
+
+def test_host_only_calls(lib_path):
+    import expert_cache_host_layer_gb300 as ft
+    assert ft.ft_expert_bytes(2048, 512, ft.FT_W_BF16) == 6291456
+    assert ft.ft_expert_bytes(4096, 2048, ft.FT_W_FP8E4M3_B128) == 25168896
+    assert ft.ft_expert_bytes(256, 128, ft.FT_W_F32) == 393216
+    assert ft.ft_expert_bytes(100, 128, ft.FT_W_FP8E4M3_B128) == 0
+    lib = ft.library()
+    assert lib.ft_status_str(ft.FT_ERR_CAPACITY) == b"FT_ERR_CAPACITY"
+    # argument validation happens before any CUDA call
+    cfg = ft.ft_cache_config()
+    out = ctypes.c_void_p()
+    assert lib.ft_cache_create(ctypes.byref(cfg), None, 0, None, ctypes.byref(out)) == ft.FT_ERR_INVALID_ARG
+    assert b"num_layers" in lib.ft_last_error()
+    assert lib.ft_route_classify(None, 0, None, 0, None, None) == ft.FT_ERR_INVALID_ARG
+    assert lib.ft_cache_destroy(None) == ft.FT_OK

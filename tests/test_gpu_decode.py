@@ -1,0 +1,63 @@
+"""GPU parity of the decode path through the C ABI against the CPU oracle.
+
+Decisions (top-k indices, unique set, hit flags, victims, evicted keys, slot
+tables, counters) must be bit-exact at every event; FFN outputs within
+max|diff| <= tol * RMS(ref) per layer event (1e-4 for fp32, 2e-2 for
+bf16/fp8); gates within 2e-6.  The fetched slots must hold their blob's bytes.
+"""
+import pytest
+import torch
+
+import synth
+from synth import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from tests.harness import run_parity
+
+
+@pytest.mark.parametrize("fetch_mode", [0, 1])
+@pytest.mark.parametrize("double_buffer", [True, False])
+def test_tiny_full_parity(fetch_mode, double_buffer):
+    rep = run_parity(W.TINY, fetch_mode=fetch_mode, double_buffer=double_buffer)
+    assert rep["events"] == 128 and rep["ffn_checked"] == 128
+    assert rep["max_err"] <= 1e-4
+
+
+def test_tiny_two_copy_streams():
+    rep = run_parity(W.TINY, fetch_mode=0, copy_streams=2, steps=32)
+    assert rep["events"] == 64
+
+
+def test_tiny_tie_heavy_logits():
+    w = W.TINY
+    lg = synth.router_ties(w.seed, 3, (64, w.num_layers, w.tokens, w.num_experts))
+    rep = run_parity(w, logits=lg)
+    assert rep["events"] == 128
+
+
+def test_qwen35b_decode_full_512_steps():
+    """Full 512-step decode decision stream at the 35B-A3B shape (aliased 1024-blob bank)."""
+    rep = run_parity(W.QWEN35B_DECODE, bank_blobs=1024, check_tables_every=41, ffn_every=53)
+    assert rep["events"] == 512 * 40
+    print("qwen35b decode:", rep)
+
+
+def test_qwen35b_decode_copy_engine_mode():
+    rep = run_parity(W.QWEN35B_DECODE, steps=48, fetch_mode=0, bank_blobs=512, check_tables_every=7, ffn_every=5)
+    assert rep["events"] == 48 * 40
+
+
+@pytest.mark.parametrize("w", [W.QWEN35B_DECODE_B4, W.QWEN35B_DECODE_B8], ids=["b4", "b8"])
+def test_qwen35b_multistream(w):
+    rep = run_parity(w, steps=96, bank_blobs=1024, check_tables_every=13, ffn_every=7)
+    assert rep["events"] == 96 * 40
+
+
+def test_dsv4_fp8_with_resize():
+    """fp8 block-scaled experts, 1024 steps, shrink 2383 -> 1191 slots before step 512."""
+    w = W.DSV4_DECODE
+    rep = run_parity(w, check_tables_every=97, ffn_every=61)
+    assert rep["events"] == 1024 * 24 and rep["resize_moves"] > 0
+    print("dsv4:", rep)
