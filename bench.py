@@ -264,7 +264,7 @@ def run_ours(args, w):
     logits_d = torch.from_numpy(logits_h).to(dev)
     x_d = torch.from_numpy(x_h).to(dev, act)
     L, T = w.num_layers, w.tokens
-    y_d = torch.empty((L, T, w.hidden), dtype=act, device=dev)
+    y_d = torch.empty((L, T, w.hidden), dtype=torch.float32, device=dev)
 
     cache = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots, T, bank,
                         n_blobs, fetch_mode=args.fetch_mode, pull_ctas=args.pull_ctas,
@@ -317,7 +317,7 @@ def run_ours(args, w):
     if not args.no_e2e:
         lg_pin = torch.from_numpy(logits_h[args.warmup:]).pin_memory()
         x_pin = torch.from_numpy(x_h[args.warmup:]).to(act).pin_memory()
-        y_pin = torch.empty((args.steps, L, T, w.hidden), dtype=act).pin_memory()
+        y_pin = torch.empty((args.steps, L, T, w.hidden), dtype=torch.float32).pin_memory()
         lg_dev = torch.empty_like(logits_d[0])
         x_dev = torch.empty_like(x_d[0])
         cache2 = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots, T,

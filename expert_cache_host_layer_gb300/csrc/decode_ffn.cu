@@ -3,7 +3,7 @@
 //
 //   gate_up:  h[row][r] = silu(Wg[r] . x_t) * (Wu[r] . x_t)   for every row
 //             (t, j) of every unique expert u and every r < I
-//   down:     y[t][c]  = sum_u sum_(rows (t,j) of u) w_tj * (Wd[c] . h[row])
+//   down:     y[t][c]  = sum_u sum_(rows (t,j) of u) w_tj * (Wd[c] . h[row])   (fp32 y)
 //
 // One warp per task: a (unique expert, intermediate row) pair for gate_up, an
 // output column c for down.  Each lane streams 16-byte chunks of the weight
@@ -186,7 +186,6 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(FfnArgs a) {
 // ---------------------------------------------------------------- down
 template <int WT, int CPL>
 __global__ void __launch_bounds__(kThreads) down_kernel(FfnArgs a) {
-  constexpr bool kF32 = WT == FT_W_F32;
   constexpr int EPC = W<WT>::kEPC;
   constexpr int UG = 4;  // experts whose chunks are in flight together
   const int H = a.H, I = a.I, T = a.T;
@@ -262,12 +261,7 @@ __global__ void __launch_bounds__(kThreads) down_kernel(FfnArgs a) {
     for (int t = 0; t < kMaxRows; ++t) {
       if (t < T) {
         const float v = warp_sum(acc[t]);
-        if (lane == 0) {
-          if (kF32)
-            static_cast<float*>(a.y)[(long long)t * H + c_out] = v;
-          else
-            static_cast<__nv_bfloat16*>(a.y)[(long long)t * H + c_out] = __float2bfloat16_rn(v);
-        }
+        if (lane == 0) static_cast<float*>(a.y)[(long long)t * H + c_out] = v;
       }
     }
   }

@@ -37,7 +37,8 @@ class ExpertCache:
         self.bank = bank  # torch uint8 tensor in (pinned) host memory, [bank_blobs * expert_bytes]
         self.bank_blobs = bank_blobs or num_layers * num_experts
         self.stream = stream or torch.cuda.current_stream(self.device)
-        self.act_dtype = torch.float32 if wdtype == FT_W_F32 else torch.bfloat16
+        self.act_dtype = torch.float32 if wdtype == FT_W_F32 else torch.bfloat16  # x
+        self.out_dtype = torch.float32                                              # y
         self.pool = torch.empty(num_slots * self.eb, dtype=torch.uint8, device=self.device)
         self.num_slots = num_slots
         cfg = make_config(num_layers, num_experts, top_k, hidden, inter, wdtype, bank.data_ptr(),
@@ -104,7 +105,7 @@ class ExpertCache:
 
     # ---- one step over all layers ------------------------------------------
     def run_step(self, logits, xs, ys, double_buffer=True, topk_idx=None, topk_w=None, after_event=None):
-        """logits[l]: [T,E] f32, xs[l], ys[l]: [T,H] device tensors for each layer l.
+        """logits[l]: [T,E] f32, xs[l]: [T,H] act_dtype, ys[l]: [T,H] f32 device tensors per layer l.
 
         `after_event(layer)` (tests) is called right after each layer's
         route_classify is enqueued.

@@ -54,8 +54,9 @@ typedef enum ft_status {
   FT_ERR_UNSUPPORTED = 8  /* shape or mode this build does not implement */
 } ft_status;
 
-/* Expert weight formats.  Activations (x, y) are float32 for FT_W_F32 and
- * bf16 for the other two. */
+/* Expert weight formats.  The FFN input x is float32 for FT_W_F32 and bf16
+ * for the other two; the FFN output y is always float32 (the accumulation
+ * precision; the caller rounds it into its residual stream). */
 typedef enum ft_wdtype {
   FT_W_F32 = 0,
   FT_W_BF16 = 1,
@@ -195,7 +196,7 @@ ft_status ft_fetch_misses(ft_cache* cache, int32_t layer);
  * The layer's MoE FFN on the compute stream, reading expert weights from the
  * cache slots:  y[t] = sum_j topk_w[t][j] * Wd h,  h = silu(Wg x[t]) * (Wu x[t]).
  *   x  device [T][H]: float32 for FT_W_F32, bf16 otherwise
- *   y  device [T][H]: same type as x; fully overwritten
+ *   y  device [T][H]: float32; fully overwritten
  * T must equal the T of the layer's last ft_route_classify.  The compute
  * stream first waits for the layer's fetch.  T <= 8 runs the decode GEMV
  * kernels; larger T the grouped tensor-core GEMM path.

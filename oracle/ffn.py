@@ -68,7 +68,9 @@ def dequant_blob(blob: np.ndarray, hidden: int, inter: int, wdtype: int):
         for mat, scales in ((Wg, s[0:g]), (Wu, s[g:2 * g]), (Wd, s[2 * g:3 * g])):
             rows, cols = mat.shape
             grid = scales.reshape(rows // BLOCK, cols // BLOCK)
-            mat *= np.kron(grid, np.ones((BLOCK, BLOCK)))
+            # weight (r, c) times the scale of block (r // 128, c // 128)
+            blocks = mat.reshape(rows // BLOCK, BLOCK, cols // BLOCK, BLOCK)
+            blocks *= grid[:, None, :, None]
     return Wg, Wu, Wd
 
 

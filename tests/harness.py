@@ -101,7 +101,7 @@ def run_parity(w: W.Workload, steps: int | None = None, fetch_mode: int = 1, dou
     L, T, k = w.num_layers, w.tokens, w.top_k
     idx_d = [torch.empty((T, k), dtype=torch.int32, device=dev) for _ in range(L)]
     wt_d = [torch.empty((T, k), dtype=torch.float32, device=dev) for _ in range(L)]
-    ys = [torch.empty((T, w.hidden), dtype=cache.act_dtype, device=dev) for _ in range(L)]
+    ys = [torch.empty((T, w.hidden), dtype=cache.out_dtype, device=dev) for _ in range(L)]
     report = {"events": 0, "ffn_checked": 0, "max_err": 0.0, "max_rms_err": 0.0, "slots_checked": 0}
     ev_counter = [0]
     step_state = {}

@@ -58,6 +58,6 @@ def test_qwen35b_multistream(w):
 def test_dsv4_fp8_with_resize():
     """fp8 block-scaled experts, 1024 steps, shrink 2383 -> 1191 slots before step 512."""
     w = W.DSV4_DECODE
-    rep = run_parity(w, check_tables_every=97, ffn_every=61)
+    rep = run_parity(w, check_tables_every=97, ffn_every=197)
     assert rep["events"] == 1024 * 24 and rep["resize_moves"] > 0
     print("dsv4:", rep)

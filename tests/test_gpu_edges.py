@@ -109,7 +109,7 @@ def test_nan_logits_ordered_as_minus_inf():
     dev = torch.device("cuda:0")
     row = np.array([[np.nan, 0.5, np.nan, -0.0, 0.0, 3.0] + [-np.inf] * 10], dtype=np.float32)
     idx = torch.empty((1, 2), dtype=torch.int32, device=dev)
-    c.route_classify(0, torch.from_numpy(row).to(dev), idx)
+    c.route_classify(0, torch.from_numpy(row).to(dev), idx)  # noqa
     torch.cuda.synchronize()
     assert idx.cpu().numpy().tolist() == orouting.topk(row, 2).tolist() == [[5, 1]]
     c.close()
