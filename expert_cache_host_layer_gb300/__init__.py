@@ -87,6 +87,7 @@ def _load():
         "ft_get_copy_stream": (st, [P, ctypes.POINTER(P)]),
         "ft_timing_enable": (st, [P, I32]),
         "ft_get_timing": (st, [P, ctypes.POINTER(ft_timing)]),
+        "ft_moe_decode_ffn_static": (st, [I32, I32, I32, I32, I32, P, I64, P, P, P, P, I32, P, P]),
         "ft_status_str": (ctypes.c_char_p, [st]),
         "ft_last_error": (ctypes.c_char_p, []),
     }
@@ -214,6 +215,15 @@ def make_config(num_layers, num_experts, top_k, hidden, inter, wdtype, host_bank
                 max_tokens, fetch_mode=FT_FETCH_SM_PULL, pull_ctas=0, copy_streams=1) -> ft_cache_config:
     return ft_cache_config(num_layers, num_experts, top_k, hidden, inter, wdtype, host_bank_ptr, host_bank_bytes,
                            bank_blobs, max_tokens, fetch_mode, pull_ctas, copy_streams)
+
+
+def ft_moe_decode_ffn_static(hidden: int, inter: int, wdtype: int, num_experts: int, top_k: int, slot_pool: int,
+                             num_slots: int, expert_slot: int, topk_idx: int, topk_w: int, x: int, T: int, y: int,
+                             stream: int = 0):
+    """Decode FFN whose working memory is a static device array (no allocation)."""
+    _check(_lib.ft_moe_decode_ffn_static(hidden, inter, wdtype, num_experts, top_k, slot_pool or None, num_slots,
+                                         expert_slot or None, topk_idx or None, topk_w or None, x or None, T,
+                                         y or None, stream or None), "ft_moe_decode_ffn_static")
 
 
 def ft_status_str(status: int) -> str:

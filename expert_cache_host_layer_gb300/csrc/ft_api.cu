@@ -119,6 +119,16 @@ enum { PHASE_ROUTE = 0, PHASE_FETCH, PHASE_FFN, PHASE_GEMV, PHASE_DOWN, PHASE_CO
 
 }  // namespace
 
+ft_status ft::set_error(ft_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
 struct ft_cache {
   // configuration
   ft_cache_config cfg{};

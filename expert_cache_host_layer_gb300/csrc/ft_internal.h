@@ -77,6 +77,9 @@ struct RouteArgs {
   int build_rows;      // 1: the kernel groups rows by expert (small T*k)
 };
 
+// Sets the calling thread's ft_last_error() message and returns `s`.
+ft_status set_error(ft_status s, const char* fmt, ...);
+
 cudaError_t launch_route_classify(const RouteArgs& a, cudaStream_t s);
 cudaError_t launch_init_tables(Tables tab, int num_keys, cudaStream_t s);
 

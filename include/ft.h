@@ -242,6 +242,36 @@ ft_status ft_get_copy_stream(ft_cache* cache, void** stream);
 ft_status ft_timing_enable(ft_cache* cache, int32_t on);
 ft_status ft_get_timing(ft_cache* cache, ft_timing* out);
 
+/*
+ * Decode expert FFN that allocates nothing (no counterpart in the paper: an
+ * addition for callers that cannot allocate device memory, such as an engine
+ * whose memory planner owns all device memory, or a serving loop where a
+ * cudaMalloc/cudaFree stall is not acceptable; ft_moe_forward needs a cache,
+ * and ft_cache_create allocates).  Same result as ft_moe_forward's decode path
+ * for the same weights and routing:
+ *   y[t] = sum_j topk_w[t][j] * Wd h,  h = silu(Wg x[t]) * (Wu x[t]),
+ * with expert e's blob read from slot expert_slot[e] of slot_pool.
+ *   slot_pool    device [num_slots][expert_bytes] expert blobs (layout above)
+ *   expert_slot  device int32 [num_experts]: slot of each expert; a pick whose
+ *                expert id or slot is out of range contributes nothing
+ *   topk_idx     device int32 [T][top_k], distinct experts within a row;
+ *                topk_w device float32 [T][top_k]
+ *   x            device [T][hidden], float32 for FT_W_F32 else bf16
+ *   y            device [T][hidden] float32
+ *   stream       cudaStream_t (void*), NULL = legacy default stream
+ * Asynchronous on `stream`.  Working memory is one static 1 MiB device array
+ * per GPU, reserved when the library loads and kept until the process exits;
+ * the first call on a device looks up its address (make that first call
+ * before any stream capture).  Limits: T <= 8, and T*top_k*inter*4 bytes of
+ * intermediate within 1,032,192 bytes (T*top_k <= 64 at inter 4096); larger
+ * sizes return FT_ERR_INVALID_ARG with a message.  All calls share the array:
+ * calls whose kernels overlap on the GPU (other streams or threads) race.
+ */
+ft_status ft_moe_decode_ffn_static(int32_t hidden, int32_t inter, int32_t wdtype, int32_t num_experts,
+                                   int32_t top_k, const void* slot_pool, int64_t num_slots,
+                                   const int32_t* expert_slot, const int32_t* topk_idx, const float* topk_w,
+                                   const void* x, int32_t T, void* y, void* stream);
+
 const char* ft_status_str(ft_status s);
 /* Message of the calling thread's last error ("" if none). */
 const char* ft_last_error(void);
