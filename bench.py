@@ -45,7 +45,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=16)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=W.QWEN35B_DECODE.name, choices=sorted(W.ALL))
-    p.add_argument("--fetch-mode", type=int, default=1, help="0 copy engine, 1 SM pull")
+    p.add_argument("--fetch-mode", type=int, default=0, help="0 copy engine, 1 SM pull")
     p.add_argument("--pull-ctas", type=int, default=0)
     p.add_argument("--copy-streams", type=int, default=1)
     p.add_argument("--serial", action="store_true", help="double buffering off")
@@ -53,6 +53,8 @@ def parse():
     p.add_argument("--slots", type=int, default=0, help="override the cache size")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-link", action="store_true")
+    p.add_argument("--trace", action="store_true", help="print one step's per-layer timeline to stderr")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     return p.parse_args()
 
@@ -110,14 +112,6 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
-
-
-def gateup_bytes(w: W.Workload) -> int:
-    """Algorithmic bytes the gate/up kernel reads per unique expert: Wg and Wu
-    (and their fp8 block scales); x is re-read from shared memory."""
-    wsize = {synth.W_F32: 4, synth.W_BF16: 2, synth.W_FP8: 1}[w.wdtype]
-    scales = 2 * 2 * (w.hidden // 128) * (w.inter // 128) if w.wdtype == synth.W_FP8 else 0
-    return 2 * w.hidden * w.inter * wsize + scales
 
 
 def measured_peaks():
@@ -239,14 +233,63 @@ def run_reference(args, w):
 
 # --------------------------------------------------------------------- our arm
 
+def link_ceilings(cache, w, dev, bank):
+    """Host-link ceilings measured on this machine, outside the timed region:
+    the copy engine (one cudaMemcpyAsync per blob, as the copy-engine fetch
+    does) and the SM-pull fetch kernel alone on a cold cache (T=32 i.i.d.
+    tokens: ~100+ misses per layer event)."""
+    import torch
+
+    import synth as S
+    from expert_cache_host_layer_gb300.pipeline import ExpertCache
+    eb = w.expert_bytes
+    n = 32
+    d = torch.empty(n * eb, dtype=torch.uint8, device=dev)
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    best_ce = 0.0
+    for _ in range(3):
+        s0.record()
+        for i in range(n):
+            d[i * eb:(i + 1) * eb].copy_(bank[i * eb:(i + 1) * eb], non_blocking=True)
+        s1.record()
+        torch.cuda.synchronize(dev)
+        best_ce = max(best_ce, n * eb / (s0.elapsed_time(s1) / 1e3) / 1e9)
+    del d
+    c = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, 1024, 32, bank,
+                    cache.bank_blobs, fetch_mode=1, device=dev)
+    best_pull = 0.0
+    try:
+        for l in range(4):
+            lg = torch.from_numpy(S.router_iid(7, 0, l, 32, w.num_experts)).to(dev)
+            st0 = c.stats()
+            c.route_classify(l, lg)
+            c.synchronize()
+            c.timing_enable(True)
+            c.fetch_misses(l)
+            c.synchronize()
+            tm = c.timing()
+            st1 = c.stats()
+            c.timing_enable(False)
+            if l > 0:
+                best_pull = max(best_pull, (st1["bytes_fetched"] - st0["bytes_fetched"]) / (tm["fetch_ms"] / 1e3) / 1e9)
+            c.close()
+            c = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, 1024, 32, bank,
+                            cache.bank_blobs, fetch_mode=1, device=dev)
+    finally:
+        c.close()
+    return {"copy_engine_gbs": best_ce, "sm_pull_gbs": best_pull,
+            "how": "best of a few isolated runs: 32 x one-blob cudaMemcpyAsync H2D from pinned memory; "
+                   "pull_misses_kernel on a cold cache"}
+
+
 def run_ours(args, w):
     import torch
 
     rank, local, world = dist_setup(args.gpus)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    import expert_cache_host_layer_gb300 as ft
-    from expert_cache_host_layer_gb300.pipeline import ExpertCache, pinned_bank
+    from expert_cache_host_layer_gb300.pipeline import ExpertCache, StepGraph, pinned_bank
 
     if args.slots:
         w = w.replace(num_slots=args.slots)
@@ -264,22 +307,39 @@ def run_ours(args, w):
     logits_d = torch.from_numpy(logits_h).to(dev)
     x_d = torch.from_numpy(x_h).to(dev, act)
     L, T = w.num_layers, w.tokens
-    y_d = torch.empty((L, T, w.hidden), dtype=torch.float32, device=dev)
-
-    cache = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots, T, bank,
-                        n_blobs, fetch_mode=args.fetch_mode, pull_ctas=args.pull_ctas,
-                        copy_streams=args.copy_streams, device=dev)
-    stream = cache.stream
+    # fixed per-layer buffers the captured step reads and writes
+    lg_buf = torch.empty_like(logits_d[0])
+    x_buf = torch.empty_like(x_d[0])
+    y_buf = torch.empty((L, T, w.hidden), dtype=torch.float32, device=dev)
     double = not args.serial
 
-    def step(s):
-        cache.run_step(logits_d[s], x_d[s], y_d, double_buffer=double)
+    def make_cache():
+        return ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots, T, bank,
+                           n_blobs, fetch_mode=args.fetch_mode, pull_ctas=args.pull_ctas,
+                           copy_streams=args.copy_streams, device=dev)
+
+    use_graph = True
+    cache = make_cache()
+    stream = cache.stream
+    graphs = []
+    if use_graph:
+        graphs = [StepGraph(cache, list(lg_buf), list(x_buf), list(y_buf), double, timing=True) for _ in range(2)]
+
+    def step(s, i):
+        lg_buf.copy_(logits_d[s], non_blocking=True)
+        x_buf.copy_(x_d[s], non_blocking=True)
+        if use_graph:
+            graphs[i % 2].launch()
+        else:
+            cache.run_step(list(lg_buf), list(x_buf), list(y_buf), double_buffer=double)
 
     for s in range(args.warmup):
-        step(s)
+        step(s, s)
     cache.synchronize()
     st0 = cache.stats()
-    cache.timing_enable(True)
+    if not use_graph or args.fetch_mode == 0:  # copy-engine fetches are timed by the library's copy thread
+        cache.timing_enable(True)
+    acc = {"route": 0.0, "fetch": 0.0, "ffn": 0.0, "n": 0}
     sampler = ClockSampler(local)
     sampler.start()
     barrier(world)
@@ -287,30 +347,48 @@ def run_ours(args, w):
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for s in range(args.warmup, steps_total):
-        step(s)
+    for i, s in enumerate(range(args.warmup, steps_total)):
+        step(s, i)
+        if use_graph and i > 0:  # the previous step's per-layer event times (it is done or nearly so)
+            r, fe, f, _ = graphs[(i - 1) % 2].timing()
+            acc["route"] += r.sum(); acc["fetch"] += fe.sum(); acc["ffn"] += f.sum(); acc["n"] += 1
     ev1.record(stream)
     cache.synchronize()
     torch.cuda.synchronize(dev)
     barrier(world)
     clocks = sampler.stop()
     elapsed_ms = ev0.elapsed_time(ev1)
-    tm = cache.timing()
+    if use_graph and args.trace and rank == 0:
+        tr = graphs[(args.steps - 1) % 2].trace()
+        print("layer  route_b route_e  fetch_b fetch_e  ffn_b  ffn_e  (us from step start)", file=sys.stderr)
+        for l in range(L):
+            print(f"{l:5d} " + " ".join(f"{1e3 * v:7.1f}" for v in tr[l]), file=sys.stderr)
+    if use_graph:
+        r, fe, f, _ = graphs[(args.steps - 1) % 2].timing()
+        acc["route"] += r.sum(); acc["fetch"] += fe.sum(); acc["ffn"] += f.sum(); acc["n"] += 1
+        tm = {"route_ms": acc["route"], "fetch_ms": acc["fetch"], "ffn_ms": acc["ffn"],
+              "route_n": acc["n"] * L, "fetch_n": acc["n"] * L, "ffn_n": acc["n"] * L}
+        if args.fetch_mode == 0:
+            ct = cache.timing()
+            tm["fetch_ms"], tm["fetch_n"] = ct["fetch_ms"], ct["fetch_n"]
+            cache.timing_enable(False)
+    else:
+        tm = cache.timing()
+        cache.timing_enable(False)
     st1 = cache.stats()
-    cache.timing_enable(False)
     elapsed_ms = max_over_ranks(elapsed_ms, world)
     tokens = world * args.steps * T
     value = tokens / (elapsed_ms / 1e3)
 
     d = {k: st1[k] - st0[k] for k in st1}
     eb = w.expert_bytes
-    gemv_bytes_per_launch = d["unique_experts"] * gateup_bytes(w) / max(1, tm["gemv_n"])
-    gemv_ms = tm["gemv_ms"] / max(1, tm["gemv_n"])
     ffn_bytes_per_launch = d["unique_experts"] * eb / max(1, tm["ffn_n"])
     ffn_ms = tm["ffn_ms"] / max(1, tm["ffn_n"])
     peak, peak_kind = measured_peaks()
-    achieved = gemv_bytes_per_launch / (gemv_ms / 1e3) / 1e9
+    achieved = ffn_bytes_per_launch / (ffn_ms / 1e3) / 1e9
     fetch_gbs = d["bytes_fetched"] / max(1e-9, tm["fetch_ms"] / 1e3) / 1e9 if tm["fetch_n"] else None
+    for g in graphs:
+        g.close()
 
     # ---- end to end through the C ABI with host buffers -------------------
     e2e = None
@@ -318,29 +396,36 @@ def run_ours(args, w):
         lg_pin = torch.from_numpy(logits_h[args.warmup:]).pin_memory()
         x_pin = torch.from_numpy(x_h[args.warmup:]).to(act).pin_memory()
         y_pin = torch.empty((args.steps, L, T, w.hidden), dtype=torch.float32).pin_memory()
-        lg_dev = torch.empty_like(logits_d[0])
-        x_dev = torch.empty_like(x_d[0])
-        cache2 = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots, T,
-                             bank, n_blobs, fetch_mode=args.fetch_mode, pull_ctas=args.pull_ctas,
-                             copy_streams=args.copy_streams, device=dev, stream=stream)
+        cache2 = make_cache()
+        g2 = StepGraph(cache2, list(lg_buf), list(x_buf), list(y_buf), double) if use_graph else None
         for s in range(args.warmup):  # same warm state as the device-timed run
-            cache2.run_step(logits_d[s], x_d[s], y_d, double_buffer=double)
+            lg_buf.copy_(logits_d[s]); x_buf.copy_(x_d[s])
+            g2.launch() if g2 else cache2.run_step(list(lg_buf), list(x_buf), list(y_buf), double_buffer=double)
         cache2.synchronize()
         barrier(world)
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            for i in range(args.steps):
-                lg_dev.copy_(lg_pin[i], non_blocking=True)
-                x_dev.copy_(x_pin[i], non_blocking=True)
-                cache2.run_step(lg_dev, x_dev, y_d, double_buffer=double)
-                y_pin[i].copy_(y_d, non_blocking=True)
+        for i in range(args.steps):
+            lg_buf.copy_(lg_pin[i], non_blocking=True)
+            x_buf.copy_(x_pin[i], non_blocking=True)
+            g2.launch() if g2 else cache2.run_step(list(lg_buf), list(x_buf), list(y_buf), double_buffer=double)
+            y_pin[i].copy_(y_buf, non_blocking=True)
+        cache2.synchronize()  # polls: the copy thread may still have copies to enqueue
         torch.cuda.synchronize(dev)
         e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+        if g2:
+            g2.close()
         cache2.close()
         e2e = {"value": world * args.steps * T / e2e_s, "unit": "tokens/s",
                "h2d_bytes_per_step": int(lg_pin[0].numel() * 4 + x_pin[0].numel() * x_pin.element_size()),
-               "d2h_bytes_per_step": int(y_d.numel() * y_d.element_size())}
+               "d2h_bytes_per_step": int(y_buf.numel() * 4)}
+
+    link = None
+    if rank == 0 and not args.no_link:
+        try:
+            link = link_ceilings(cache, w, dev, bank)
+        except Exception as ex:
+            link = {"error": str(ex)[:200]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -359,18 +444,17 @@ def run_ours(args, w):
                        "top_k": w.top_k, "hidden": w.hidden, "inter": w.inter, "slots": w.num_slots,
                        "bank_blobs": n_blobs, "bank_gb": round(n_blobs * eb / 1e9, 2),
                        "fetch_mode": ["copy_engine", "sm_pull"][args.fetch_mode],
-                       "double_buffer": double, "parallelism": f"replicas{world}",
+                       "double_buffer": double, "step_graph": use_graph, "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2 (each step reads ~2 GB of expert slots)"},
             "miss_rate": d["misses"] / max(1, d["unique_experts"]),
-            "expert_gemm_gbs": d["unique_experts"] * eb / max(1e-9, tm["ffn_ms"] / 1e3) / 1e9,
+            "expert_gemm_gbs": achieved,
             "miss_copy": {"gbs": fetch_gbs, "bytes_per_step": d["bytes_fetched"] / args.steps,
-                          "mode": ["copy_engine", "sm_pull"][args.fetch_mode]},
-            "phase_ms_per_step": {k: tm[f"{k}_ms"] / args.steps for k in ("route", "fetch", "ffn", "gemv", "down")},
-            "roofline": {"kernel": "gateup_kernel (decode expert GEMV, gate+up+SwiGLU)", "bound": "hbm",
-                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                         "peak_kind": peak_kind, "traffic": None,
-                         "bytes_per_launch": gemv_bytes_per_launch, "launch_us": gemv_ms * 1e3,
-                         "ffn_achieved_gbs": ffn_bytes_per_launch / (ffn_ms / 1e3) / 1e9},
+                          "mode": ["copy_engine", "sm_pull"][args.fetch_mode], "link": link},
+            "phase_ms_per_step": {k: tm[f"{k}_ms"] / args.steps for k in ("route", "fetch", "ffn")},
+            "roofline": {"kernel": "decode expert FFN: gateup_kernel + down_kernel (PDL pair), one ft_moe_forward",
+                         "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_kind": peak_kind, "traffic": None, "bytes_per_launch": ffn_bytes_per_launch,
+                         "launch_us": ffn_ms * 1e3},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": d["kernel_launches"],

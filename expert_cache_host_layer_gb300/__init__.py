@@ -47,9 +47,7 @@ class ft_stats(ctypes.Structure):
 class ft_timing(ctypes.Structure):
     _fields_ = [("route_ms", ctypes.c_double), ("route_n", ctypes.c_int64),
                 ("fetch_ms", ctypes.c_double), ("fetch_n", ctypes.c_int64),
-                ("ffn_ms", ctypes.c_double), ("ffn_n", ctypes.c_int64),
-                ("gemv_ms", ctypes.c_double), ("gemv_n", ctypes.c_int64),
-                ("down_ms", ctypes.c_double), ("down_n", ctypes.c_int64)]
+                ("ffn_ms", ctypes.c_double), ("ffn_n", ctypes.c_int64)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -87,6 +85,11 @@ def _load():
         "ft_get_copy_stream": (st, [P, ctypes.POINTER(P)]),
         "ft_timing_enable": (st, [P, I32]),
         "ft_get_timing": (st, [P, ctypes.POINTER(ft_timing)]),
+        "ft_step_graph_create": (st, [P, P, P, P, I32, I32, I32, ctypes.POINTER(P)]),
+        "ft_step_graph_launch": (st, [P]),
+        "ft_step_graph_timing": (st, [P, P, P, P, P]),
+        "ft_step_graph_trace": (st, [P, P]),
+        "ft_step_graph_destroy": (st, [P]),
         "ft_moe_decode_ffn_static": (st, [I32, I32, I32, I32, I32, P, I64, P, P, P, P, I32, P, P]),
         "ft_status_str": (ctypes.c_char_p, [st]),
         "ft_last_error": (ctypes.c_char_p, []),
@@ -215,6 +218,44 @@ def make_config(num_layers, num_experts, top_k, hidden, inter, wdtype, host_bank
                 max_tokens, fetch_mode=FT_FETCH_SM_PULL, pull_ctas=0, copy_streams=1) -> ft_cache_config:
     return ft_cache_config(num_layers, num_experts, top_k, hidden, inter, wdtype, host_bank_ptr, host_bank_bytes,
                            bank_blobs, max_tokens, fetch_mode, pull_ctas, copy_streams)
+
+
+def ft_step_graph_create(cache: int, logits_ptrs, x_ptrs, y_ptrs, T: int, double_buffer: bool = True,
+                         timing: bool = False) -> int:
+    """Capture one step over all layers into a CUDA graph; pointer lists hold one buffer per layer."""
+    arr = ctypes.c_void_p * len(logits_ptrs)
+    out = ctypes.c_void_p()
+    _check(_lib.ft_step_graph_create(cache, arr(*logits_ptrs), arr(*x_ptrs), arr(*y_ptrs), T, int(bool(double_buffer)),
+                                     int(bool(timing)), ctypes.byref(out)), "ft_step_graph_create")
+    return out.value
+
+
+def ft_step_graph_launch(graph: int):
+    _check(_lib.ft_step_graph_launch(graph), "ft_step_graph_launch")
+
+
+def ft_step_graph_timing(graph: int, num_layers: int):
+    """(route_ms[L], fetch_ms[L], ffn_ms[L], step_ms) of the graph's last launch (waits for it)."""
+    import numpy as np
+    r = np.zeros(num_layers, dtype=np.float64)
+    fe = np.zeros(num_layers, dtype=np.float64)
+    f = np.zeros(num_layers, dtype=np.float64)
+    st = ctypes.c_double()
+    _check(_lib.ft_step_graph_timing(graph, r.ctypes.data, fe.ctypes.data, f.ctypes.data, ctypes.byref(st)),
+           "ft_step_graph_timing")
+    return r, fe, f, st.value
+
+
+def ft_step_graph_trace(graph: int, num_layers: int):
+    """[L][6] ms from the step start: route, fetch, FFN begin/end per layer (last launch)."""
+    import numpy as np
+    t = np.zeros(6 * num_layers, dtype=np.float64)
+    _check(_lib.ft_step_graph_trace(graph, t.ctypes.data), "ft_step_graph_trace")
+    return t.reshape(num_layers, 6)
+
+
+def ft_step_graph_destroy(graph: int):
+    _check(_lib.ft_step_graph_destroy(graph), "ft_step_graph_destroy")
 
 
 def ft_moe_decode_ffn_static(hidden: int, inter: int, wdtype: int, num_experts: int, top_k: int, slot_pool: int,

@@ -6,16 +6,17 @@
 // misses streamed from host RAM; "FreeToken: Efficient Edge-Native MoE Serving
 // ...", ablation paragraph: double buffering of the expert transfers).
 //
-// Work items are 64 KB chunks of the n_miss blobs; each CTA copies one chunk
-// per round with 8 independent 16-byte loads in flight per thread.
+// Work items are 32 KB chunks of the n_miss blobs; each CTA copies one chunk
+// per round with 8 independent 16-byte loads in flight per thread (256
+// threads: a small CTA that fits beside an FFN CTA on the same SM).
 #include "ft_internal.h"
 
 namespace ft {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kUnroll = 8;
-constexpr long long kChunk16 = (long long)kThreads * kUnroll;  // 16-byte words per chunk (64 KB)
+constexpr long long kChunk16 = (long long)kThreads * kUnroll;  // 16-byte words per chunk (32 KB)
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;

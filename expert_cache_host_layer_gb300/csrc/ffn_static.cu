@@ -16,6 +16,7 @@
 // nothing has to start at zero; but two calls whose kernels overlap on the
 // GPU (different streams, or different host threads) race on it and produce
 // garbage.  Serialise them on one stream.
+#include <algorithm>
 #include <mutex>
 #include <string>
 
@@ -158,8 +159,11 @@ extern "C" ft_status ft_moe_decode_ffn_static(int32_t hidden, int32_t inter, int
   if (e != cudaSuccess) return set_error(FT_ERR_CUDA, "plan kernel launch: %s", cudaGetErrorString(e));
   FfnArgs f{};
   f.hdr = hdr; f.unique_slot = unique_slot; f.u_offset = u_offset; f.rows_by_u = rows_by_u; f.topk_w = topk_w;
-  f.x = x; f.y = y; f.pool = static_cast<const uint8_t*>(slot_pool); f.expert_bytes = (long long)eb;
+  f.x = x; f.y = static_cast<float*>(y); f.pool = static_cast<const uint8_t*>(slot_pool);
+  f.expert_bytes = (long long)eb;
   f.H = hidden; f.I = inter; f.k = top_k; f.T = T; f.wdtype = wdtype; f.h = h;
+  f.max_unique = (int)std::min<long long>(rows, num_experts);
+  f.status = hdr + PH_STATUS;
   if ((e = launch_decode_gateup(f, s)) != cudaSuccess)
     return set_error(FT_ERR_CUDA, "gate/up launch: %s", cudaGetErrorString(e));
   if ((e = launch_decode_down(f, s)) != cudaSuccess)

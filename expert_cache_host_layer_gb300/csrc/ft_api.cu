@@ -1,7 +1,7 @@
 // Host side of libft: the C ABI declared in include/ft.h.
 //
 // One ft_cache owns the device slot tables, one plan per layer, the routing
-// scratch, a mapped pinned mirror of each layer's miss list, the copy
+// scratch, (copy-engine mode) a mapped pinned ring of the events' miss lists, the copy
 // stream(s) and the per-layer events that order the pipeline:
 //
 //   compute stream:  route(l+1) -> [cls(l+1)] ... wait(ready(l)) -> FFN(l)
@@ -9,9 +9,13 @@
 //
 // so the misses of layer l+1 stream in while layer l computes ("FreeToken:
 // Efficient Edge-Native MoE Serving ...", ablation paragraph: double
-// buffering).  In copy-engine mode a library thread waits for cls(l), reads
-// the mirrored miss list and issues one cudaMemcpyAsync per miss; in SM-pull
-// mode a kernel on the copy stream reads the device plan itself.
+// buffering).  In copy-engine mode the route kernel appends each event's miss
+// list to a ring in mapped host memory; a library thread polls the ring,
+// issues one cudaMemcpyAsync per miss on the copy stream and then a 4-byte
+// copy that sets the event's ready flag in device memory; the FFN kernel waits
+// (bounded) for that flag.  No host synchronisation sits between the GPU
+// work, so a whole step can be captured in a CUDA graph in either mode.  In
+// SM-pull mode a kernel on the copy stream reads the device plan itself.
 #include <algorithm>
 #include <atomic>
 #include <climits>
@@ -19,7 +23,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
-#include <deque>
+#include <chrono>
 #include <mutex>
 #include <string>
 #include <thread>
@@ -115,7 +119,7 @@ struct PhaseTimer {
   }
 };
 
-enum { PHASE_ROUTE = 0, PHASE_FETCH, PHASE_FFN, PHASE_GEMV, PHASE_DOWN, PHASE_COUNT };
+enum { PHASE_ROUTE = 0, PHASE_FETCH, PHASE_FFN, PHASE_COUNT };
 
 }  // namespace
 
@@ -146,110 +150,140 @@ struct ft_cache {
   void* plan_mem = nullptr;
   RouteScratch scr{};
   void* scr_mem = nullptr;
-  HostMirror* mirror_host = nullptr;  // mapped pinned [L]
-  HostMirror* mirror_dev = nullptr;
+  RingEntry* ring_host = nullptr;     // copy-engine mode: mapped pinned [kRing]
+  RingEntry* ring_dev = nullptr;
+  int32_t* ready_flags = nullptr;     // device [kRing], set on the copy stream after an event's copies
+  int32_t* flag_src = nullptr;        // pinned host [kRing], sources of those 4-byte copies
+  int32_t* counter_host = nullptr;    // pinned host word for reading the device event counter
   float* h_buf = nullptr;             // decode intermediate [max_rows][I]
+  unsigned* gbar = nullptr;           // grid-barrier words of the fused FFN kernel
+  bool fused_ok = true;               // false once the fused FFN kernel reported it cannot run
   // streams and events
   cudaStream_t compute = nullptr;
+  cudaStream_t route = nullptr;        // route_classify kernels (off the FFN's critical path)
+  cudaEvent_t route_join = nullptr;    // compute -> route ordering at each ft_route_classify
   cudaStream_t copy[2] = {nullptr, nullptr};
   int ncopy = 1;
   cudaEvent_t copy_join = nullptr;
   std::vector<cudaEvent_t> cls_ev, ready_ev;
   // host-side state of the event stream
   int next_event = 0;
-  bool pin_previous = false;          // false on the first event and right after a resize
   std::vector<int> layer_event;       // event of the layer's current plan (-1 none)
   std::vector<int> layer_tokens;
   std::vector<int> fetch_event;       // event whose fetch was issued (-1 none)
   std::vector<int> forward_event;     // event whose FFN was enqueued (-1 none)
-  // copy-engine helper thread
+  // copy-engine thread: processes ring events 0, 1, 2, ... in order
   std::thread helper;
-  std::mutex mu;
-  std::condition_variable cv_job, cv_done;
-  std::deque<std::pair<int, int>> jobs;  // (layer, event)
-  std::vector<int> done_event;           // per layer: event whose copies are issued
-  std::vector<int> job_status;
-  bool stop = false;
-  int busy = 0;
+  std::atomic<bool> stop{false};
+  std::atomic<long long> copied_events{0};  // events whose copies (and ready flag) are enqueued
+  std::atomic<int> copy_status{0};          // first error of the copy thread (ft_status)
+  std::mutex pool_mu;                       // guards pool and C against a resize while copies are issued
   // counters
   std::atomic<long long> launches{0}, memcpys{0};
   // timing
   bool timing = false;
   PhaseTimer timers[PHASE_COUNT];
+  // step-graph capture: while set, ft_route_classify / ft_moe_forward record
+  // external event nodes around their kernels into these arrays
+  cudaStream_t capture_stream = nullptr;
+  cudaEvent_t* cap_route_ev = nullptr;  // [2*L] begin/end per layer
+  cudaEvent_t* cap_ffn_ev = nullptr;    // [2*L]
+  cudaEvent_t* cap_fetch_ev = nullptr;  // [2*L] on the copy stream
 };
 
 namespace {
 
+// Copy-engine thread.  Polls the stamp of ring entry e % kRing until it
+// reads e (the route kernel writes every field first), copies the event's
+// misses from the host bank into their victim slots on the copy stream(s),
+// then copies e into ready_flags[e % kRing] after them.  A ring entry is not
+// overwritten before it is read: event e + kRing can only be routed after the
+// FFN of event e + kRing - 2 ran, which waited for this thread's flag of that
+// event.
 void helper_loop(ft_cache* c) {
   cudaSetDevice(c->device);
-  for (;;) {
-    std::pair<int, int> job;
-    {
-      std::unique_lock<std::mutex> lk(c->mu);
-      c->cv_job.wait(lk, [&] { return c->stop || !c->jobs.empty(); });
-      if (c->jobs.empty()) return;
-      job = c->jobs.front();
-      c->jobs.pop_front();
-      ++c->busy;
+  long long e = 0;
+  int idle = 0;
+  while (!c->stop.load(std::memory_order_relaxed)) {
+    RingEntry* r = c->ring_host + (e % kRing);
+    const int stamp = __atomic_load_n(&r->event, __ATOMIC_ACQUIRE);
+    if (stamp != (int)e) {
+      if (++idle > 2000) std::this_thread::sleep_for(std::chrono::microseconds(20));
+      continue;
     }
-    const int l = job.first, ev = job.second;
+    idle = 0;
     int st = FT_OK;
-    if (cudaEventSynchronize(c->cls_ev[l]) != cudaSuccess) st = FT_ERR_CUDA;
-    const HostMirror* m = c->mirror_host + l;
-    if (st == FT_OK && m->event != ev) st = FT_ERR_STATE;
+    const int l = r->layer, n = r->n_miss;
     const bool tm = c->timing;
-    if (st == FT_OK) {
-      const int n = m->n_miss;
-      if (tm) c->timers[PHASE_FETCH].begin(c->copy[0]);
-      if (c->ncopy > 1) {  // second stream starts with the first
-        cudaEventRecord(c->copy_join, c->copy[0]);
-        cudaStreamWaitEvent(c->copy[1], c->copy_join, 0);
-      }
-      for (int i = 0; i < n && st == FT_OK; ++i) {
-        const int e = m->miss_expert[i], s = m->miss_slot[i];
-        if (e < 0 || e >= c->E || s < 0 || s >= c->C) {
-          st = FT_ERR_CHECKED;
-          break;
-        }
-        const int64_t blob = ((int64_t)l * c->E + e) % c->cfg.bank_blobs;
-        if (cudaMemcpyAsync(static_cast<uint8_t*>(c->pool) + (size_t)s * c->eb, c->bank_host + (size_t)blob * c->eb,
-                            c->eb, cudaMemcpyHostToDevice, c->copy[i % c->ncopy]) != cudaSuccess)
-          st = FT_ERR_CUDA;
-        ++c->memcpys;
-      }
-      if (c->ncopy > 1) {
-        cudaEventRecord(c->copy_join, c->copy[1]);
-        cudaStreamWaitEvent(c->copy[0], c->copy_join, 0);
-      }
-      if (tm) c->timers[PHASE_FETCH].end(c->copy[0]);
+    std::lock_guard<std::mutex> pool_lock(c->pool_mu);
+    if (tm) c->timers[PHASE_FETCH].begin(c->copy[0]);
+    if (c->ncopy > 1) {  // the second stream starts with the first
+      cudaEventRecord(c->copy_join, c->copy[0]);
+      cudaStreamWaitEvent(c->copy[1], c->copy_join, 0);
     }
-    cudaEventRecord(c->ready_ev[l], c->copy[0]);
-    {
-      std::lock_guard<std::mutex> lk(c->mu);
-      c->done_event[l] = ev;
-      c->job_status[l] = st;
-      --c->busy;
+    for (int i = 0; i < n; ++i) {
+      const int ex = r->miss_expert[i], sl = r->miss_slot[i];
+      if (l < 0 || l >= c->L || ex < 0 || ex >= c->E || sl < 0 || sl >= c->C) {
+        st = FT_ERR_CHECKED;
+        break;
+      }
+      const int64_t blob = ((int64_t)l * c->E + ex) % c->cfg.bank_blobs;
+      if (cudaMemcpyAsync(static_cast<uint8_t*>(c->pool) + (size_t)sl * c->eb, c->bank_host + (size_t)blob * c->eb,
+                          c->eb, cudaMemcpyHostToDevice, c->copy[i % c->ncopy]) != cudaSuccess)
+        st = FT_ERR_CUDA;
+      ++c->memcpys;
     }
-    c->cv_done.notify_all();
+    if (c->ncopy > 1) {
+      cudaEventRecord(c->copy_join, c->copy[1]);
+      cudaStreamWaitEvent(c->copy[0], c->copy_join, 0);
+    }
+    c->flag_src[e % kRing] = (int)e;
+    if (cudaMemcpyAsync(c->ready_flags + (e % kRing), c->flag_src + (e % kRing), sizeof(int32_t),
+                        cudaMemcpyHostToDevice, c->copy[0]) != cudaSuccess)
+      st = FT_ERR_CUDA;
+    if (tm) c->timers[PHASE_FETCH].end(c->copy[0]);
+    if (st != FT_OK) {
+      int zero = 0;
+      c->copy_status.compare_exchange_strong(zero, st);
+    }
+    c->copied_events.store(e + 1, std::memory_order_release);
+    ++e;
   }
 }
 
-// Wait until the helper has issued the copies of (layer, event); returns the job's status.
-ft_status wait_fetch_issued(ft_cache* c, int layer, int event) {
-  std::unique_lock<std::mutex> lk(c->mu);
-  c->cv_done.wait(lk, [&] { return c->done_event[layer] == event; });
-  return (ft_status)c->job_status[layer];
+// Waits for a stream by polling: the copy thread may still have to enqueue
+// the copies (and ready flags) that work on this stream waits for, so the
+// waiting thread must not sit inside a blocking runtime call meanwhile.
+cudaError_t wait_stream(cudaStream_t s) {
+  for (;;) {
+    const cudaError_t e = cudaStreamQuery(s);
+    if (e != cudaErrorNotReady) return e;
+    std::this_thread::sleep_for(std::chrono::microseconds(10));
+  }
 }
 
-void wait_helper_idle(ft_cache* c) {
-  std::unique_lock<std::mutex> lk(c->mu);
-  c->cv_done.wait(lk, [&] { return c->jobs.empty() && c->busy == 0; });
+cudaError_t wait_event(cudaEvent_t ev) {
+  for (;;) {
+    const cudaError_t e = cudaEventQuery(ev);
+    if (e != cudaErrorNotReady) return e;
+    std::this_thread::sleep_for(std::chrono::microseconds(10));
+  }
 }
 
 ft_status sync_all(ft_cache* c) {
-  if (c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE) wait_helper_idle(c);
-  CU(cudaStreamSynchronize(c->compute));
-  for (int i = 0; i < c->ncopy; ++i) CU(cudaStreamSynchronize(c->copy[i]));
+  CU(wait_stream(c->compute));  // FFNs (and graph replays) done
+  CU(wait_stream(c->route));
+  if (c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE) {  // every routed event's copies must be enqueued
+    CU(cudaMemcpyAsync(c->counter_host, c->tab.event_ctr, sizeof(int32_t), cudaMemcpyDeviceToHost, c->route));
+    CU(wait_stream(c->route));
+    const int routed = *c->counter_host;
+    while (c->copied_events.load(std::memory_order_acquire) < routed)
+      std::this_thread::sleep_for(std::chrono::microseconds(10));
+  }
+  for (int i = 0; i < c->ncopy; ++i) CU(wait_stream(c->copy[i]));
+  CU(wait_stream(c->compute));
+  const int cs = c->copy_status.load();
+  if (cs != FT_OK) return fail((ft_status)cs, "a miss copy failed (%s)", ft_status_str((ft_status)cs));
   return FT_OK;
 }
 
@@ -265,10 +299,13 @@ ft_status alloc_tables(Tables& t, int64_t C, int num_keys, bool with_keys) {
   if (with_keys) CU(cudaMalloc(&t.key_to_slot, sizeof(int32_t) * num_keys));
   CU(cudaMalloc(&t.slot_key, sizeof(int32_t) * C));
   CU(cudaMalloc(&t.slot_ts, sizeof(int32_t) * C));
-  CU(cudaMalloc(&t.order[0], sizeof(int32_t) * C));
-  CU(cudaMalloc(&t.order[1], sizeof(int32_t) * C));
-  CU(cudaMalloc(&t.order_cur, sizeof(int32_t) * 2));
+  CU(cudaMalloc(&t.order[0], sizeof(int2) * C));
+  CU(cudaMalloc(&t.order[1], sizeof(int2) * C));
+  CU(cudaMalloc(&t.order_cur, sizeof(int32_t) * 8));
   t.status = t.order_cur + 1;
+  t.last_nu = t.order_cur + 2;
+  t.event_ctr = t.order_cur + 3;
+  t.pin_next = t.order_cur + 4;
   CU(cudaMalloc(&t.stats, sizeof(long long) * ST_COUNT));
   return FT_OK;
 }
@@ -319,15 +356,12 @@ ft_status ft_cache_destroy(ft_cache* c) {
   if (!c) return FT_OK;
   cudaSetDevice(c->device);
   if (c->helper.joinable()) {
-    {
-      std::lock_guard<std::mutex> lk(c->mu);
-      c->stop = true;
-    }
-    c->cv_job.notify_all();
+    c->stop = true;
     c->helper.join();
   }
   if (c->compute || c->copy[0]) {
-    if (c->compute) cudaStreamSynchronize(c->compute);
+    if (c->compute) wait_stream(c->compute);
+    if (c->route) wait_stream(c->route);
     for (int i = 0; i < 2; ++i)
       if (c->copy[i]) cudaStreamSynchronize(c->copy[i]);
   }
@@ -336,11 +370,18 @@ ft_status ft_cache_destroy(ft_cache* c) {
   if (c->copy_join) cudaEventDestroy(c->copy_join);
   for (int i = 0; i < 2; ++i)
     if (c->copy[i]) cudaStreamDestroy(c->copy[i]);
+  if (c->capture_stream) cudaStreamDestroy(c->capture_stream);
+  if (c->route) cudaStreamDestroy(c->route);
+  if (c->route_join) cudaEventDestroy(c->route_join);
   free_tables(c->tab, true);
   cudaFree(c->plan_mem);
   cudaFree(c->scr_mem);
   cudaFree(c->h_buf);
-  if (c->mirror_host) cudaFreeHost(c->mirror_host);
+  cudaFree(c->gbar);
+  if (c->ring_host) cudaFreeHost(c->ring_host);
+  if (c->flag_src) cudaFreeHost(c->flag_src);
+  if (c->counter_host) cudaFreeHost(c->counter_host);
+  cudaFree(c->ready_flags);
   if (c->registered_bank) cudaHostUnregister(const_cast<uint8_t*>(c->bank_host));
   delete c;
   return FT_OK;
@@ -439,13 +480,22 @@ ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t n
     // decode intermediate
     const long long drows = (long long)std::min(g.max_tokens, kDecodeMaxTokens) * g.top_k;
     CU(cudaMalloc(&c->h_buf, sizeof(float) * drows * c->I));
-    // miss-list mirror in mapped pinned memory
-    CU(cudaHostAlloc(reinterpret_cast<void**>(&c->mirror_host), sizeof(HostMirror) * c->L, cudaHostAllocMapped));
-    memset(c->mirror_host, 0, sizeof(HostMirror) * c->L);
-    for (int l = 0; l < c->L; ++l) c->mirror_host[l].event = -1;
-    CU(cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->mirror_dev), c->mirror_host, 0));
+    CU(cudaMalloc(&c->gbar, 2 * sizeof(unsigned)));
+    CU(cudaMemset(c->gbar, 0, 2 * sizeof(unsigned)));
+    if (g.fetch_mode == FT_FETCH_COPY_ENGINE) {  // event ring (mapped host) and ready flags (device)
+      CU(cudaHostAlloc(reinterpret_cast<void**>(&c->ring_host), sizeof(RingEntry) * kRing, cudaHostAllocMapped));
+      memset(c->ring_host, 0, sizeof(RingEntry) * kRing);
+      for (int i = 0; i < kRing; ++i) c->ring_host[i].event = -1;
+      CU(cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->ring_dev), c->ring_host, 0));
+      CU(cudaHostAlloc(reinterpret_cast<void**>(&c->flag_src), sizeof(int32_t) * kRing, cudaHostAllocDefault));
+      CU(cudaHostAlloc(reinterpret_cast<void**>(&c->counter_host), sizeof(int32_t), cudaHostAllocDefault));
+      CU(cudaMalloc(&c->ready_flags, sizeof(int32_t) * kRing));
+      CU(cudaMemset(c->ready_flags, 0xff, sizeof(int32_t) * kRing));  // -1: no event yet
+    }
     // streams and events
     for (int i = 0; i < c->ncopy; ++i) CU(cudaStreamCreateWithFlags(&c->copy[i], cudaStreamNonBlocking));
+    CU(cudaStreamCreateWithFlags(&c->route, cudaStreamNonBlocking));
+    CU(cudaEventCreateWithFlags(&c->route_join, cudaEventDisableTiming));
     CU(cudaEventCreateWithFlags(&c->copy_join, cudaEventDisableTiming));
     c->cls_ev.assign(c->L, nullptr);
     c->ready_ev.assign(c->L, nullptr);
@@ -457,8 +507,6 @@ ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t n
     c->layer_tokens.assign(c->L, 0);
     c->fetch_event.assign(c->L, -1);
     c->forward_event.assign(c->L, -1);
-    c->done_event.assign(c->L, -1);
-    c->job_status.assign(c->L, FT_OK);
     CU(launch_init_tables(c->tab, c->L * c->E, c->compute));
     ++c->launches;
     CU(cudaStreamSynchronize(c->compute));
@@ -492,22 +540,27 @@ ft_status ft_route_classify(ft_cache* c, int32_t layer, const float* logits, int
       return fail(FT_ERR_STATE, "layer %d (event %d) fetched but not forwarded; only one layer may run ahead", l,
                   c->fetch_event[l]);
   RouteArgs a{};
-  a.logits = logits; a.T = T; a.E = c->E; a.k = c->k; a.layer = layer; a.event = t;
-  a.pin_ts = c->pin_previous ? t - 1 : INT_MIN;
+  a.logits = logits; a.T = T; a.E = c->E; a.k = c->k; a.layer = layer;
   a.out_idx = topk_idx; a.out_w = topk_w;
   a.tab = c->tab; a.plan = c->plans[layer]; a.scr = c->scr;
-  a.mirror = c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE ? c->mirror_dev + layer : nullptr;
+  a.ring = c->ring_dev;
   a.expert_bytes = (long long)c->eb;
   a.build_rows = (long long)T * c->k <= kMaxExperts;
-  if (c->timing) c->timers[PHASE_ROUTE].begin(c->compute);
-  CU(launch_route_classify(a, c->compute));
-  if (c->timing) c->timers[PHASE_ROUTE].end(c->compute);
+  // The route stream starts after everything the caller has enqueued on the
+  // compute stream so far: the logits, and in the double-buffered schedule the
+  // FFN of event t-2 (whose slots this event may evict).
+  CU(cudaEventRecord(c->route_join, c->compute));
+  CU(cudaStreamWaitEvent(c->route, c->route_join, 0));
+  if (c->timing) c->timers[PHASE_ROUTE].begin(c->route);
+  if (c->cap_route_ev) CU(cudaEventRecordWithFlags(c->cap_route_ev[2 * layer], c->route, cudaEventRecordExternal));
+  CU(launch_route_classify(a, c->route));
+  if (c->cap_route_ev) CU(cudaEventRecordWithFlags(c->cap_route_ev[2 * layer + 1], c->route, cudaEventRecordExternal));
+  if (c->timing) c->timers[PHASE_ROUTE].end(c->route);
   ++c->launches;
-  CU(cudaEventRecord(c->cls_ev[layer], c->compute));
+  CU(cudaEventRecord(c->cls_ev[layer], c->route));
   c->layer_event[layer] = t;
   c->layer_tokens[layer] = T;
   c->next_event = t + 1;
-  c->pin_previous = true;
   return FT_OK;
 }
 
@@ -517,11 +570,7 @@ ft_status ft_fetch_misses(ft_cache* c, int32_t layer) {
   const int ev = c->layer_event[layer];
   if (ev < 0 || c->fetch_event[layer] == ev) return fail(FT_ERR_STATE, "layer %d has no classification awaiting fetch", layer);
   if (c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE) {
-    {
-      std::lock_guard<std::mutex> lk(c->mu);
-      c->jobs.emplace_back(layer, ev);
-    }
-    c->cv_job.notify_one();
+    // nothing to enqueue: the copy thread picks the event up from the ring
   } else {
     CU(cudaStreamWaitEvent(c->copy[0], c->cls_ev[layer], 0));
     PullArgs p{};
@@ -529,9 +578,11 @@ ft_status ft_fetch_misses(ft_cache* c, int32_t layer) {
     p.hdr = pl.hdr; p.miss_expert = pl.miss_expert; p.miss_slot = pl.miss_slot;
     p.layer = layer; p.E = c->E; p.bank_blobs = c->cfg.bank_blobs; p.bank = c->bank_dev;
     p.pool = c->pool; p.expert_bytes = (long long)c->eb;
-    const int ctas = c->cfg.pull_ctas > 0 ? c->cfg.pull_ctas : 32;
+    const int ctas = c->cfg.pull_ctas > 0 ? c->cfg.pull_ctas : 64;
     if (c->timing) c->timers[PHASE_FETCH].begin(c->copy[0]);
+    if (c->cap_fetch_ev) CU(cudaEventRecordWithFlags(c->cap_fetch_ev[2 * layer], c->copy[0], cudaEventRecordExternal));
     CU(launch_pull_misses(p, ctas, c->copy[0]));
+    if (c->cap_fetch_ev) CU(cudaEventRecordWithFlags(c->cap_fetch_ev[2 * layer + 1], c->copy[0], cudaEventRecordExternal));
     if (c->timing) c->timers[PHASE_FETCH].end(c->copy[0]);
     ++c->launches;
     CU(cudaEventRecord(c->ready_ev[layer], c->copy[0]));
@@ -549,37 +600,46 @@ ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, v
   if (T != c->layer_tokens[layer]) return fail(FT_ERR_INVALID_ARG, "T=%d differs from the plan's T=%d", T, c->layer_tokens[layer]);
   if (T > 0 && (!x || !y)) return fail(FT_ERR_INVALID_ARG, "null x or y");
   if (c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE) {
-    const ft_status js = wait_fetch_issued(c, layer, ev);
-    if (js != FT_OK) return fail(js, "layer %d: miss copy failed (%s)", layer, ft_status_str(js));
+    // the FFN reads the plan written by route_classify; its slots are waited
+    // for inside the kernel (ready flag set after the copies)
+    CU(cudaStreamWaitEvent(c->compute, c->cls_ev[layer], 0));
+  } else {
+    CU(cudaStreamWaitEvent(c->compute, c->ready_ev[layer], 0));
   }
-  CU(cudaStreamWaitEvent(c->compute, c->ready_ev[layer], 0));
   c->forward_event[layer] = ev;
   if (T == 0) return FT_OK;
   if (T > kDecodeMaxTokens) return fail(FT_ERR_UNSUPPORTED, "T=%d > %d needs the grouped GEMM path", T, kDecodeMaxTokens);
   const Plan& pl = c->plans[layer];
   FfnArgs f{};
   f.hdr = pl.hdr; f.unique_slot = pl.unique_slot; f.u_offset = pl.u_offset; f.rows_by_u = pl.rows_by_u;
-  f.topk_w = pl.topk_w; f.x = x; f.y = y; f.pool = static_cast<const uint8_t*>(c->pool);
+  f.topk_w = pl.topk_w; f.x = x; f.y = static_cast<float*>(y); f.pool = static_cast<const uint8_t*>(c->pool);
   f.expert_bytes = (long long)c->eb; f.H = c->H; f.I = c->I; f.k = c->k; f.T = T; f.wdtype = c->wdtype; f.h = c->h_buf;
+  f.max_unique = std::min(T * c->k, c->E);
+  f.status = c->tab.status;
+  f.gbar = c->gbar;
+  f.ready_flags = c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE ? c->ready_flags : nullptr;
+  // the two kernels are timed as one unit: an event between them would cut
+  // the programmatic dependency that lets the down kernel start early
   const bool tm = c->timing;
-  if (tm) {
-    c->timers[PHASE_FFN].begin(c->compute);
-    c->timers[PHASE_GEMV].begin(c->compute);
+  if (tm) c->timers[PHASE_FFN].begin(c->compute);
+  if (c->cap_ffn_ev) CU(cudaEventRecordWithFlags(c->cap_ffn_ev[2 * layer], c->compute, cudaEventRecordExternal));
+  cudaError_t e = c->fused_ok ? launch_decode_ffn_fused(f, c->compute) : cudaErrorNotSupported;
+  if (e == cudaSuccess) {
+    ++c->launches;
+  } else {
+    if (e != cudaErrorNotSupported) {
+      cudaGetLastError();  // clear a launch-configuration error, then take the two-kernel path from now on
+      c->fused_ok = false;
+    }
+    e = launch_decode_gateup(f, c->compute);
+    if (e != cudaSuccess) return fail(FT_ERR_CUDA, "gate/up launch: %s", cudaGetErrorString(e));
+    ++c->launches;
+    e = launch_decode_down(f, c->compute);
+    if (e != cudaSuccess) return fail(FT_ERR_CUDA, "down launch: %s", cudaGetErrorString(e));
+    ++c->launches;
   }
-  cudaError_t e = launch_decode_gateup(f, c->compute);
-  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "gate/up launch: %s", cudaGetErrorString(e));
-  ++c->launches;
-  if (tm) {
-    c->timers[PHASE_GEMV].end(c->compute);
-    c->timers[PHASE_DOWN].begin(c->compute);
-  }
-  e = launch_decode_down(f, c->compute);
-  if (e != cudaSuccess) return fail(FT_ERR_CUDA, "down launch: %s", cudaGetErrorString(e));
-  ++c->launches;
-  if (tm) {
-    c->timers[PHASE_DOWN].end(c->compute);
-    c->timers[PHASE_FFN].end(c->compute);
-  }
+  if (c->cap_ffn_ev) CU(cudaEventRecordWithFlags(c->cap_ffn_ev[2 * layer + 1], c->compute, cudaEventRecordExternal));
+  if (tm) c->timers[PHASE_FFN].end(c->compute);
   return FT_OK;
 }
 
@@ -629,9 +689,11 @@ ft_status ft_cache_resize(ft_cache* c, void* new_pool, int64_t new_num_slots) {
   }
   free_tables(c->tab, false);
   c->tab = nt;
-  c->pool = new_pool;
-  c->C = new_num_slots;
-  c->pin_previous = false;  // the safe point: nothing is in flight
+  {
+    std::lock_guard<std::mutex> lk(c->pool_mu);
+    c->pool = new_pool;
+    c->C = new_num_slots;
+  }
   for (int l = 0; l < c->L; ++l) {
     c->layer_event[l] = -1;
     c->fetch_event[l] = -1;
@@ -743,8 +805,171 @@ ft_status ft_get_timing(ft_cache* c, ft_timing* out) {
   out->route_ms = c->timers[PHASE_ROUTE].total_ms; out->route_n = c->timers[PHASE_ROUTE].n;
   out->fetch_ms = c->timers[PHASE_FETCH].total_ms; out->fetch_n = c->timers[PHASE_FETCH].n;
   out->ffn_ms = c->timers[PHASE_FFN].total_ms; out->ffn_n = c->timers[PHASE_FFN].n;
-  out->gemv_ms = c->timers[PHASE_GEMV].total_ms; out->gemv_n = c->timers[PHASE_GEMV].n;
-  out->down_ms = c->timers[PHASE_DOWN].total_ms; out->down_n = c->timers[PHASE_DOWN].n;
+  return FT_OK;
+}
+
+// ----------------------------------------------------------------- step graphs
+
+struct ft_step_graph {
+  ft_cache* c = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int L = 0;
+  long long kernels = 0;  // kernels per launch
+  std::vector<cudaEvent_t> ev;  // [0,2L) route, [2L,4L) ffn, [4L,6L) fetch begin/end; then step begin/end
+  bool timing = false;
+  bool launched = false;
+};
+
+ft_status ft_step_graph_destroy(ft_step_graph* g) {
+  if (!g) return FT_OK;
+  if (g->c) cudaSetDevice(g->c->device);
+  if (g->launched && g->c) wait_stream(g->c->compute);
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  for (auto e : g->ev) cudaEventDestroy(e);
+  delete g;
+  return FT_OK;
+}
+
+ft_status ft_step_graph_create(ft_cache* c, const float* const* logits, const void* const* x, float* const* y,
+                               int32_t T, int32_t double_buffer, int32_t timing, ft_step_graph** out) {
+  if (!c || !out || !logits || !x || !y) return fail(FT_ERR_INVALID_ARG, "null argument");
+  *out = nullptr;
+  if (T < 0 || T > c->max_tokens) return fail(FT_ERR_INVALID_ARG, "T=%d outside 0..max_tokens", T);
+  for (int l = 0; l < c->L; ++l) {
+    if (T > 0 && (!logits[l] || !x[l] || !y[l])) return fail(FT_ERR_INVALID_ARG, "null buffer for layer %d", l);
+    if (c->fetch_event[l] >= 0 && c->fetch_event[l] == c->layer_event[l] && c->forward_event[l] != c->fetch_event[l])
+      return fail(FT_ERR_STATE, "layer %d has a fetched plan whose FFN was not enqueued", l);
+  }
+  ft_status st = sync_all(c);
+  if (st != FT_OK) return st;
+  ft_step_graph* g = new ft_step_graph();
+  g->c = c;
+  g->L = c->L;
+  g->timing = timing != 0;
+  const int nev = 6 * c->L + 2;
+  g->ev.assign(nev, nullptr);
+  for (auto& e : g->ev)
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      ft_step_graph_destroy(g);
+      return fail(FT_ERR_CUDA, "cudaEventCreate failed");
+    }
+  if (!c->capture_stream && cudaStreamCreateWithFlags(&c->capture_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    ft_step_graph_destroy(g);
+    return fail(FT_ERR_CUDA, "capture stream creation failed");
+  }
+  cudaStream_t saved_compute = c->compute;
+  const bool saved_timing = c->timing;
+  const long long launches0 = c->launches.load();
+  c->compute = c->capture_stream;
+  c->timing = false;
+  if (g->timing) {
+    c->cap_route_ev = g->ev.data();
+    c->cap_ffn_ev = g->ev.data() + 2 * c->L;
+    c->cap_fetch_ev = g->ev.data() + 4 * c->L;
+  }
+  auto restore = [&]() {
+    c->compute = saved_compute;
+    c->timing = saved_timing;
+    c->cap_route_ev = nullptr;
+    c->cap_ffn_ev = nullptr;
+    c->cap_fetch_ev = nullptr;
+  };
+  cudaError_t e = cudaStreamBeginCapture(c->capture_stream, cudaStreamCaptureModeRelaxed);
+  if (e != cudaSuccess) {
+    restore();
+    ft_step_graph_destroy(g);
+    return fail(FT_ERR_CUDA, "cudaStreamBeginCapture: %s", cudaGetErrorString(e));
+  }
+  if (g->timing) cudaEventRecordWithFlags(g->ev[6 * c->L], c->capture_stream, cudaEventRecordExternal);
+  auto route = [&](int l) -> ft_status {
+    ft_status s1 = ft_route_classify(c, l, logits[l], T, nullptr, nullptr);
+    return s1 != FT_OK ? s1 : ft_fetch_misses(c, l);
+  };
+  st = FT_OK;
+  if (double_buffer) {
+    st = route(0);
+    for (int l = 0; l < c->L && st == FT_OK; ++l) {
+      if (l + 1 < c->L) st = route(l + 1);
+      if (st == FT_OK) st = ft_moe_forward(c, l, x[l], T, y[l]);
+    }
+  } else {
+    for (int l = 0; l < c->L && st == FT_OK; ++l) {
+      st = route(l);
+      if (st == FT_OK) st = ft_moe_forward(c, l, x[l], T, y[l]);
+    }
+  }
+  if (g->timing) cudaEventRecordWithFlags(g->ev[6 * c->L + 1], c->capture_stream, cudaEventRecordExternal);
+  const std::string msg = g_last_error;
+  e = cudaStreamEndCapture(c->capture_stream, &g->graph);
+  restore();
+  g->kernels = c->launches.load() - launches0;
+  c->launches = launches0;
+  if (st != FT_OK || e != cudaSuccess) {
+    ft_step_graph_destroy(g);
+    if (st != FT_OK) return fail(st, "capture: %s", msg.c_str());
+    return fail(FT_ERR_CUDA, "cudaStreamEndCapture: %s", cudaGetErrorString(e));
+  }
+  e = cudaGraphInstantiate(&g->exec, g->graph, 0);
+  if (e == cudaSuccess) e = cudaGraphUpload(g->exec, c->compute);
+  if (e != cudaSuccess) {
+    ft_step_graph_destroy(g);
+    return fail(FT_ERR_CUDA, "cudaGraphInstantiate: %s", cudaGetErrorString(e));
+  }
+  *out = g;
+  return FT_OK;
+}
+
+ft_status ft_step_graph_launch(ft_step_graph* g) {
+  if (!g || !g->exec) return fail(FT_ERR_INVALID_ARG, "null step graph");
+  CU(cudaGraphLaunch(g->exec, g->c->compute));
+  g->c->launches += g->kernels;
+  g->launched = true;
+  return FT_OK;
+}
+
+ft_status ft_step_graph_trace(ft_step_graph* g, double* t_ms) {
+  if (!g || !t_ms) return fail(FT_ERR_INVALID_ARG, "null argument");
+  if (!g->timing || !g->launched) return fail(FT_ERR_STATE, "graph was created without timing or never launched");
+  const int L = g->L;
+  CU(wait_event(g->ev[6 * L + 1]));
+  float ms = 0.0f;
+  for (int l = 0; l < L; ++l)
+    for (int j = 0; j < 6; ++j) {  // route begin/end, fetch begin/end, ffn begin/end
+      static const int base[3] = {0, 4, 2};  // event arrays: route [0, 2L), ffn [2L, 4L), fetch [4L, 6L)
+      const int idx = base[j / 2] * L + 2 * l + (j & 1);
+      CU(cudaEventElapsedTime(&ms, g->ev[6 * L], g->ev[idx]));
+      t_ms[6 * l + j] = ms;
+    }
+  return FT_OK;
+}
+
+ft_status ft_step_graph_timing(ft_step_graph* g, double* route_ms, double* fetch_ms, double* ffn_ms,
+                               double* step_ms) {
+  if (!g) return fail(FT_ERR_INVALID_ARG, "null step graph");
+  if (!g->timing || !g->launched) return fail(FT_ERR_STATE, "graph was created without timing or never launched");
+  const int L = g->L;
+  CU(wait_event(g->ev[6 * L + 1]));
+  float ms = 0.0f;
+  for (int l = 0; l < L; ++l) {
+    if (route_ms) {
+      CU(cudaEventElapsedTime(&ms, g->ev[2 * l], g->ev[2 * l + 1]));
+      route_ms[l] = ms;
+    }
+    if (ffn_ms) {
+      CU(cudaEventElapsedTime(&ms, g->ev[2 * L + 2 * l], g->ev[2 * L + 2 * l + 1]));
+      ffn_ms[l] = ms;
+    }
+    if (fetch_ms) {
+      CU(cudaEventElapsedTime(&ms, g->ev[4 * L + 2 * l], g->ev[4 * L + 2 * l + 1]));
+      fetch_ms[l] = ms;
+    }
+  }
+  if (step_ms) {
+    CU(cudaEventElapsedTime(&ms, g->ev[6 * L], g->ev[6 * L + 1]));
+    *step_ms = ms;
+  }
   return FT_OK;
 }
 

@@ -24,9 +24,12 @@ struct Tables {
   int32_t* key_to_slot;  // [L*E]  slot of key l*E+e, -1 = absent
   int32_t* slot_key;     // [C]    key held by the slot, -1 = empty
   int32_t* slot_ts;      // [C]    event of last use, -1 = never
-  int32_t* order[2];     // [C]    all slots in ascending (slot_ts, slot); ping-pong buffers
+  int2* order[2];        // [C]    (slot, key) of all slots in ascending (slot_ts, slot); ping-pong buffers
   int32_t* order_cur;    // [1]    which order buffer is current
   int32_t* status;       // [1]    sticky device status (ft_status), 0 = ok
+  int32_t* last_nu;      // [1]    |U| of the last event (its slots are the last entries of the order)
+  int32_t* event_ctr;    // [1]    event number of the next classification
+  int32_t* pin_next;     // [1]    1: the next event pins the last event's slots (0 after create / resize)
   long long* stats;      // [ST_COUNT]
   int32_t num_slots;
 };
@@ -55,24 +58,30 @@ struct RouteScratch {
   uint32_t* ticket;  // [1]              CTAs finished
 };
 
-// Miss list mirrored into mapped pinned host memory for the copy-engine mode.
-struct HostMirror {
-  int32_t event;
+// Copy-engine mode: each route_classify appends its miss list to a ring in
+// mapped pinned host memory; it fills the fields, then stamps `event` last.
+// A library host thread polls the ring, issues the blob copies, then sets
+// ready_flags[event % kRing] = event on the copy stream after them; the FFN
+// kernels wait for that flag.
+constexpr int kRing = 16;
+struct RingEntry {
+  int32_t event;  // stamp: the event number once the entry is complete
+  int32_t layer;
   int32_t n_miss;
-  int32_t pad[2];
+  int32_t pad;
   int32_t miss_expert[kMaxExperts];
   int32_t miss_slot[kMaxExperts];
 };
 
 struct RouteArgs {
   const float* logits;
-  int T, E, k, layer, event, pin_ts;
+  int T, E, k, layer;  // the event number and the pin flag live in the tables (device state)
   int32_t* out_idx;  // optional caller outputs
   float* out_w;
   Tables tab;
   Plan plan;
   RouteScratch scr;
-  HostMirror* mirror;  // device address of the layer's mirror, or null
+  RingEntry* ring;     // device address of the event ring (copy-engine mode), or null
   long long expert_bytes;
   int build_rows;      // 1: the kernel groups rows by expert (small T*k)
 };
@@ -101,16 +110,24 @@ struct FfnArgs {
   const int32_t* u_offset;
   const int32_t* rows_by_u;
   const float* topk_w;
-  const void* x;
-  void* y;
+  const void* x;   // [T][H] f32 or bf16
+  float* y;        // [T][H] f32
   const uint8_t* pool;
   long long expert_bytes;
   int H, I, k, T, wdtype;
-  float* h;  // [T*k][I] intermediate
+  int max_unique;  // upper bound of the plan's n_unique (min(T*k, E)), sizes the grid
+  float* h;        // [T*k][I] intermediate
+  int32_t* status; // sticky status word (bounded waits record FT_ERR_TIMEOUT)
+  unsigned* gbar;  // [2] grid-barrier count and generation of the fused kernel (zeroed once)
+  const int32_t* ready_flags;  // copy-engine mode: wait for ready_flags[e % kRing] == e (e = plan event); or null
 };
 // Decode path: the gate/up+SwiGLU kernel, then the down+combine kernel.
 cudaError_t launch_decode_gateup(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_decode_down(const FfnArgs& a, cudaStream_t s);
+// Both in one cooperative kernel (gate/up, grid barrier, down, with Wd
+// prefetched during gate/up); cudaErrorNotSupported when the shape does not
+// fit its shared-memory budget (the caller then uses the two kernels).
+cudaError_t launch_decode_ffn_fused(const FfnArgs& a, cudaStream_t s);
 
 struct ResizeArgs {
   Tables old_tab;

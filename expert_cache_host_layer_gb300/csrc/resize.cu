@@ -47,9 +47,9 @@ __global__ void __launch_bounds__(kThreads) resize_tables_kernel(ResizeArgs a) {
   const int tid = threadIdx.x;
   const int C = a.old_tab.num_slots, Cn = a.new_tab.num_slots;
   const int cur = *a.old_tab.order_cur;
-  const int32_t* order = a.old_tab.order[cur];
-  int32_t* keep = a.old_tab.order[cur ^ 1];  // scratch: 1 = survives
-  int32_t* free_list = a.new_tab.order[1];   // scratch: free slots below C'
+  const int2* order = a.old_tab.order[cur];
+  int32_t* keep = reinterpret_cast<int32_t*>(a.old_tab.order[cur ^ 1]);  // scratch: 1 = survives
+  int32_t* free_list = reinterpret_cast<int32_t*>(a.new_tab.order[1]);   // scratch: free slots below C'
 
   // occupied count
   int occ_local = 0;
@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kThreads) resize_tables_kernel(ResizeArgs a) {
     const int p = base + tid;
     int s = -1, occ = 0;
     if (p < C) {
-      s = order[p];
+      s = order[p].x;
       occ = a.old_tab.slot_key[s] >= 0;
     }
     int tot;
@@ -134,12 +134,15 @@ __global__ void __launch_bounds__(kThreads) resize_tables_kernel(ResizeArgs a) {
     *a.n_moves = n_moves;
     *a.new_tab.order_cur = 0;
     *a.new_tab.status = *a.old_tab.status;
+    *a.new_tab.last_nu = 0;
+    *a.new_tab.event_ctr = *a.old_tab.event_ctr;
+    *a.new_tab.pin_next = 0;  // the safe point: nothing of the last event is still being read
     for (int i = 0; i < ST_COUNT; ++i) a.new_tab.stats[i] = a.old_tab.stats[i];
     a.new_tab.stats[ST_EVICT] += n_drop;
   }
 }
 
-// order[rank(s)] = s with rank by (slot_ts, slot) ascending over the new slots.
+// order[rank(s)] = (s, key of s) with rank by (slot_ts, slot) ascending over the new slots.
 __global__ void rank_order_kernel(Tables tab) {
   __shared__ int s_ts[1024];
   const int C = tab.num_slots;
@@ -157,7 +160,7 @@ __global__ void rank_order_kernel(Tables tab) {
         rank += o < my || (o == my && base + i < s);
       }
   }
-  if (s < C) tab.order[0][rank] = s;
+  if (s < C) tab.order[0][rank] = make_int2(s, tab.slot_key[s]);
 }
 
 __global__ void move_blobs_kernel(const int32_t* moves, const int32_t* n_moves_p, const uint4* src, uint4* dst,

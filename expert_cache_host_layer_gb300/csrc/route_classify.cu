@@ -7,18 +7,22 @@
 // Phase 1 (all CTAs): one warp per token computes the top-k experts by logit
 // (descending, lower index on ties; NaN ordered as -inf) with k rounds of a
 // warp-wide arg-max, and the gates softmax(selected logits).  Each CTA ORs its
-// tokens' experts into a shared bit set and counts picks per expert, then
-// merges both into global scratch with one atomic per non-zero word/count.
+// tokens' experts into a shared bit set and counts picks per expert.  With
+// more than one CTA, the CTAs merge both into global scratch (one atomic per
+// non-zero word/count) and the last CTA to finish (atomic ticket) runs phase
+// 2; a single CTA (decode) keeps everything in shared memory.
 //
-// Phase 2 (the last CTA to finish, found with an atomic ticket): dedup (the
-// bit set in ascending order is U), hit classification against key_to_slot,
-// global-LRU victims, table updates and the plan.  The LRU order is kept as
-// an explicit list of all slots sorted by (last use, slot).  One pass of
-// block-wide prefix sums over that list finds the first |M| candidates
-// (slots that hold neither a hit of this event nor a slot used by the
-// previous event) and compacts the list without the event's slots; the
-// event's slots, which all get last use = t, are appended in slot order.
-// That keeps the list sorted without ever sorting it.
+// Phase 2 (one CTA): dedup (the bit set in ascending order is U), hit
+// classification against key_to_slot, global-LRU victims, table updates and
+// the plan.  The LRU order is an explicit list of (slot, key) for all slots,
+// sorted by (last use, slot).  The previous event's slots are the last |U|
+// entries of that list (they were appended there), which is the pin rule
+// without any last-use lookup.  One pass of block-wide prefix sums over the
+// list (each thread owns 8 consecutive entries) finds the first |M|
+// candidates - entries that hold neither a hit of this event nor a pinned
+// slot - and compacts the list without this event's slots; those slots, which
+// all get last use = t, are appended in slot order.  That keeps the list
+// sorted without ever sorting it.
 #include <cfloat>
 #include <climits>
 
@@ -27,8 +31,9 @@
 namespace ft {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kSeg = 8;  // order entries per thread per pass
 
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
@@ -72,15 +77,36 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
   __shared__ int s_mrank[kMaxExperts];  // miss rank of each unique expert, -1 for hits
   __shared__ int s_missexp[kMaxExperts];
   __shared__ int s_victim[kMaxExperts];
+  __shared__ int s_evict[kMaxExperts];
   __shared__ int s_uoff[kMaxExperts];
+  __shared__ int s_rowu[kMaxExperts];
+  __shared__ int s_k2s[kMaxExperts];  // key_to_slot of this layer's experts
   __shared__ int s_flag;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, k = a.k, T = a.T;
   const int nwords = (E + 31) >> 5;
+  const bool single = gridDim.x == 1;
 
   for (int i = tid; i < nwords; i += kThreads) s_bits[i] = 0u;
   for (int i = tid; i < E; i += kThreads) s_cnt[i] = 0;
+  // A single CTA runs phase 2 itself: start its table reads now so they
+  // overlap the top-k work (the multi-CTA tail reads them after the ticket).
+  const int layer = a.layer, C = a.tab.num_slots;
+  int cur = 0, event = 0, n_prev = 0;
+  int2 ent0[kSeg];
+  if (single) {
+    cur = *a.tab.order_cur;
+    event = *a.tab.event_ctr;
+    n_prev = *a.tab.pin_next ? *a.tab.last_nu : 0;
+    for (int e = tid; e < E; e += kThreads) s_k2s[e] = a.tab.key_to_slot[layer * E + e];
+    const int2* order = a.tab.order[cur];
+#pragma unroll
+    for (int i = 0; i < kSeg; ++i) {
+      const int p = tid * kSeg + i;
+      ent0[i] = p < C ? order[p] : make_int2(-1, -1);
+    }
+  }
   __syncthreads();
 
   // ---------------- phase 1: top-k + gates, one warp per token -------------
@@ -139,21 +165,29 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
     }
   }
   __syncthreads();
-  for (int i = tid; i < nwords; i += kThreads)
-    if (s_bits[i]) atomicOr(&a.scr.bits[i], s_bits[i]);
-  for (int i = tid; i < E; i += kThreads)
-    if (s_cnt[i]) atomicAdd(&a.scr.counts[i], s_cnt[i]);
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_flag = (atomicAdd(a.scr.ticket, 1u) == gridDim.x - 1);
-  __syncthreads();
-  if (!s_flag) return;
-  __threadfence();
+  if (!single) {  // merge into global scratch; the last CTA continues
+    for (int i = tid; i < nwords; i += kThreads)
+      if (s_bits[i]) atomicOr(&a.scr.bits[i], s_bits[i]);
+    for (int i = tid; i < E; i += kThreads)
+      if (s_cnt[i]) atomicAdd(&a.scr.counts[i], s_cnt[i]);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_flag = (atomicAdd(a.scr.ticket, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!s_flag) return;
+    __threadfence();
+    for (int i = tid; i < nwords; i += kThreads) s_bits[i] = __ldcg(&a.scr.bits[i]);
+    for (int i = tid; i < E; i += kThreads) s_cnt[i] = __ldcg(&a.scr.counts[i]);
+    __syncthreads();
+  }
 
-  // ---------------- phase 2 (last CTA): dedup, classify, victims -----------
-  const int layer = a.layer, C = a.tab.num_slots;
-  for (int i = tid; i < nwords; i += kThreads) s_bits[i] = __ldcg(&a.scr.bits[i]);
-  __syncthreads();
+  // ---------------- phase 2 (one CTA): dedup, classify, victims ------------
+  if (!single) {
+    cur = *a.tab.order_cur;
+    event = *a.tab.event_ctr;
+    n_prev = *a.tab.pin_next ? *a.tab.last_nu : 0;
+    for (int e = tid; e < E; e += kThreads) s_k2s[e] = a.tab.key_to_slot[layer * E + e];
+  }
   if (warp == 0) {
     int c = lane < nwords ? __popc(s_bits[lane]) : 0;
 #pragma unroll
@@ -184,7 +218,7 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
     const int u = base + tid;
     int is_miss = 0;
     if (u < n_u) {
-      const int s = a.tab.key_to_slot[layer * E + s_uexp[u]];
+      const int s = s_k2s[s_uexp[u]];
       s_uslot[u] = s;
       is_miss = s < 0;
     }
@@ -200,30 +234,47 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
 
   // one pass over the LRU order: victims = first n_miss candidates; kept
   // entries are compacted into the other order buffer
-  const int cur = *a.tab.order_cur;
-  const int32_t* order = a.tab.order[cur];
-  int32_t* norder = a.tab.order[cur ^ 1];
+  const int2* order = a.tab.order[cur];
+  int2* norder = a.tab.order[cur ^ 1];
+  const int pin_from = C - n_prev;  // entries at or after this position are pinned
   int carry_cand = 0, carry_hit = 0;
-  for (int base = 0; base < C; base += kThreads) {
-    const int p = base + tid;
-    int s = -1, cand = 0, hs = 0;
-    if (p < C) {
-      s = order[p];
-      const int key = a.tab.slot_key[s];
-      if (key >= 0 && key / E == layer) {
-        const int e = key - layer * E;
-        hs = (s_bits[e >> 5] >> (e & 31)) & 1u;
+  for (int base = 0; base < C; base += kThreads * kSeg) {
+    const int p0 = base + tid * kSeg;
+    int2 ent[kSeg];
+#pragma unroll
+    for (int i = 0; i < kSeg; ++i)
+      ent[i] = (single && base == 0) ? ent0[i] : (p0 + i < C ? order[p0 + i] : make_int2(-1, -1));
+    uint32_t hit_m = 0u, cand_m = 0u;
+#pragma unroll
+    for (int i = 0; i < kSeg; ++i) {
+      const int p = p0 + i;
+      if (p < C) {
+        const int key = ent[i].y;
+        bool hs = false;
+        if (key >= 0 && key / E == layer) {
+          const int e = key - layer * E;
+          hs = (s_bits[e >> 5] >> (e & 31)) & 1u;
+        }
+        if (hs) hit_m |= 1u << i;
+        else if (p < pin_from) cand_m |= 1u << i;
       }
-      cand = !hs && a.tab.slot_ts[s] != a.pin_ts;
     }
     int tot;
-    const int packed = block_excl_scan((cand << 16) | hs, s_warp, tot);
-    if (p < C) {
-      const int cand_before = carry_cand + (packed >> 16);
-      const int hit_before = carry_hit + (packed & 0xffff);
-      const bool victim = cand && cand_before < n_miss;
-      if (victim) s_victim[cand_before] = s;
-      if (!hs && !victim) norder[p - hit_before - min(cand_before, n_miss)] = s;
+    const int packed = block_excl_scan((__popc(cand_m) << 16) | __popc(hit_m), s_warp, tot);
+    int cb = carry_cand + (packed >> 16), hb = carry_hit + (packed & 0xffff);
+#pragma unroll
+    for (int i = 0; i < kSeg; ++i) {
+      const int p = p0 + i;
+      if (p >= C) break;
+      const bool hs = (hit_m >> i) & 1u, cand = (cand_m >> i) & 1u;
+      const bool victim = cand && cb < n_miss;
+      if (victim) {
+        s_victim[cb] = ent[i].x;
+        s_evict[cb] = ent[i].y;
+      }
+      if (!hs && !victim) norder[p - hb - min(cb, n_miss)] = ent[i];
+      cb += cand;
+      hb += hs;
     }
     carry_cand += tot >> 16;
     carry_hit += tot & 0xffff;
@@ -233,32 +284,39 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
   if (carry_cand < n_miss) {  // pool too small for this event: leave the tables as they are
     if (tid == 0) {
       atomicCAS(a.tab.status, 0, (int)FT_ERR_CAPACITY);
+      a.plan.hdr[PH_EVENT] = event;
       a.plan.hdr[PH_STATUS] = (int)FT_ERR_CAPACITY;
       a.plan.hdr[PH_MISS] = 0;
       a.plan.hdr[PH_UNIQUE] = 0;
-      if (a.mirror) {
-        a.mirror->n_miss = 0;
-        a.mirror->event = a.event;
+      *a.tab.last_nu = 0;
+      *a.tab.event_ctr = event + 1;
+      *a.tab.pin_next = 1;
+      if (a.ring) {
+        RingEntry* r = a.ring + (event % kRing);
+        r->layer = layer;
+        r->n_miss = 0;
       }
     }
   } else {
     // the event's slots (hits and victims) go to the end in slot order
-    for (int u = tid; u < n_u; u += kThreads) {
-      const int s = s_mrank[u] < 0 ? s_uslot[u] : s_victim[s_mrank[u]];
-      s_uslot[u] = s;
-    }
+    for (int u = tid; u < n_u; u += kThreads)
+      if (s_mrank[u] >= 0) s_uslot[u] = s_victim[s_mrank[u]];
     __syncthreads();
     for (int u = tid; u < n_u; u += kThreads) {
       const int s = s_uslot[u];
       int rank = 0;
       for (int q = 0; q < n_u; ++q) rank += s_uslot[q] < s;
-      norder[C - n_u + rank] = s;
+      norder[C - n_u + rank] = make_int2(s, layer * E + s_uexp[u]);
+      a.tab.slot_ts[s] = event;
+      a.plan.unique_expert[u] = s_uexp[u];
+      a.plan.unique_slot[u] = s;
+      a.plan.hit[u] = s_mrank[u] < 0;
     }
     // table updates: victims lose their key, misses take their victim
     int n_evict = 0;
     for (int i = tid; i < n_miss; i += kThreads) {
       const int s = s_victim[i];
-      const int old = a.tab.slot_key[s];
+      const int old = s_evict[i];
       a.plan.evicted_key[i] = old;
       if (old >= 0) {
         a.tab.key_to_slot[old] = -1;
@@ -269,23 +327,17 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
       a.tab.slot_key[s] = key;
       a.plan.miss_expert[i] = s_missexp[i];
       a.plan.miss_slot[i] = s;
-      if (a.mirror) {
-        a.mirror->miss_expert[i] = s_missexp[i];
-        a.mirror->miss_slot[i] = s;
+      if (a.ring) {
+        RingEntry* r = a.ring + (event % kRing);
+        r->miss_expert[i] = s_missexp[i];
+        r->miss_slot[i] = s;
       }
-    }
-    for (int u = tid; u < n_u; u += kThreads) {
-      const int s = s_uslot[u];
-      a.tab.slot_ts[s] = a.event;
-      a.plan.unique_expert[u] = s_uexp[u];
-      a.plan.unique_slot[u] = s;
-      a.plan.hit[u] = s_mrank[u] < 0;
     }
     // rows per unique expert and their offsets
     int off = 0;
     for (int base = 0; base < n_u; base += kThreads) {
       const int u = base + tid;
-      const int c = u < n_u ? __ldcg(&a.scr.counts[s_uexp[u]]) : 0;
+      const int c = u < n_u ? s_cnt[s_uexp[u]] : 0;
       int tot;
       const int r = block_excl_scan(c, s_warp, tot);
       if (u < n_u) {
@@ -296,23 +348,24 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
       off += tot;
     }
     if (tid == 0) a.plan.u_offset[n_u] = off;
-    __syncthreads();
     if (a.build_rows) {  // small T*k (<= kMaxExperts): rank each row among the rows of its expert
       const int rows = T * k;
-      for (int r = tid; r < rows; r += kThreads) s_cnt[r] = __ldcg(&a.plan.e2u[__ldcg(&a.plan.topk_idx[r])]);
+      for (int r = tid; r < rows; r += kThreads) {
+        const int e = single ? a.plan.topk_idx[r] : __ldcg(&a.plan.topk_idx[r]);
+        s_rowu[r] = s_wpre[e >> 5] + __popc(s_bits[e >> 5] & ((1u << (e & 31)) - 1u));
+      }
       __syncthreads();
       for (int r = tid; r < rows; r += kThreads) {
-        const int u = s_cnt[r];
+        const int u = s_rowu[r];
         int before = 0;
-        for (int q = 0; q < r; ++q) before += s_cnt[q] == u;
+        for (int q = 0; q < r; ++q) before += s_rowu[q] == u;
         a.plan.rows_by_u[s_uoff[u] + before] = r;
       }
     }
-    // evictions: reduce the per-thread counts
     int tot_evict;
     block_excl_scan(n_evict, s_warp, tot_evict);
     if (tid == 0) {
-      a.plan.hdr[PH_EVENT] = a.event;
+      a.plan.hdr[PH_EVENT] = event;
       a.plan.hdr[PH_TOKENS] = T;
       a.plan.hdr[PH_UNIQUE] = n_u;
       a.plan.hdr[PH_MISS] = n_miss;
@@ -325,18 +378,28 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
       st[ST_MISSES] += n_miss;
       st[ST_EVICT] += tot_evict;
       st[ST_BYTES] += (long long)n_miss * a.expert_bytes;
-      if (a.mirror) {
-        a.mirror->n_miss = n_miss;
-        a.mirror->event = a.event;
+      if (a.ring) {
+        RingEntry* r = a.ring + (event % kRing);
+        r->layer = layer;
+        r->n_miss = n_miss;
       }
+      *a.tab.last_nu = n_u;
+      *a.tab.event_ctr = event + 1;
+      *a.tab.pin_next = 1;
       *a.tab.order_cur = cur ^ 1;
     }
   }
-  if (a.mirror) __threadfence_system();
-  // leave the scratch zeroed for the next launch
-  for (int i = tid; i < nwords; i += kThreads) a.scr.bits[i] = 0u;
-  for (int i = tid; i < E; i += kThreads) a.scr.counts[i] = 0;
-  if (tid == 0) *a.scr.ticket = 0u;
+  if (a.ring) {  // publish the entry: every field first, then the stamp (release, system scope)
+    __threadfence_system();
+    __syncthreads();
+    if (tid == 0)
+      asm volatile("st.release.sys.global.b32 [%0], %1;" ::"l"(&a.ring[event % kRing].event), "r"(event) : "memory");
+  }
+  if (!single) {  // leave the scratch zeroed for the next launch
+    for (int i = tid; i < nwords; i += kThreads) a.scr.bits[i] = 0u;
+    for (int i = tid; i < E; i += kThreads) a.scr.counts[i] = 0;
+    if (tid == 0) *a.scr.ticket = 0u;
+  }
 }
 
 __global__ void init_tables_kernel(Tables tab, int num_keys) {
@@ -345,12 +408,15 @@ __global__ void init_tables_kernel(Tables tab, int num_keys) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < tab.num_slots; i += stride) {
     tab.slot_key[i] = -1;
     tab.slot_ts[i] = -1;
-    tab.order[0][i] = i;  // all slots empty: (ts = -1, slot) order is slot order
-    tab.order[1][i] = i;
+    tab.order[0][i] = make_int2(i, -1);  // all slots empty: (ts = -1, slot) order is slot order
+    tab.order[1][i] = make_int2(i, -1);
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     *tab.order_cur = 0;
     *tab.status = 0;
+    *tab.last_nu = 0;
+    *tab.event_ctr = 0;
+    *tab.pin_next = 0;
     for (int i = 0; i < ST_COUNT; ++i) tab.stats[i] = 0;
   }
 }

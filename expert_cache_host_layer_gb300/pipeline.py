@@ -19,7 +19,9 @@ import torch
 
 from . import (FT_FETCH_SM_PULL, FT_W_F32, ft_cache_create, ft_cache_destroy, ft_cache_resize, ft_expert_bytes,
                ft_fetch_misses, ft_get_copy_stream, ft_get_plan, ft_get_stats, ft_get_tables, ft_get_timing,
-               ft_moe_forward, ft_reset_stats, ft_route_classify, ft_synchronize, ft_timing_enable, make_config)
+               ft_moe_forward, ft_reset_stats, ft_route_classify, ft_step_graph_create, ft_step_graph_destroy,
+               ft_step_graph_launch, ft_step_graph_timing, ft_step_graph_trace, ft_synchronize, ft_timing_enable,
+               make_config)
 
 
 class ExpertCache:
@@ -129,6 +131,38 @@ class ExpertCache:
             for l in range(L):
                 route(l)
                 self.moe_forward(l, xs[l], ys[l])
+
+
+class StepGraph:
+    """One captured step over all layers (see ft_step_graph_create); the
+    logits/x/y tensors are the fixed buffers the graph reads and writes."""
+
+    def __init__(self, cache: ExpertCache, logits, xs, ys, double_buffer=True, timing=False):
+        self.cache = cache
+        self.logits, self.xs, self.ys = logits, xs, ys  # keep the buffers alive
+        T = logits[0].shape[0]
+        self.handle = ft_step_graph_create(cache.handle, [t.data_ptr() for t in logits], [t.data_ptr() for t in xs],
+                                           [t.data_ptr() for t in ys], T, double_buffer, timing)
+
+    def launch(self):
+        ft_step_graph_launch(self.handle)
+
+    def timing(self):
+        return ft_step_graph_timing(self.handle, self.cache.L)
+
+    def trace(self):
+        return ft_step_graph_trace(self.handle, self.cache.L)
+
+    def close(self):
+        if self.handle:
+            ft_step_graph_destroy(self.handle)
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def pinned_bank(nbytes: int) -> torch.Tensor:

@@ -64,8 +64,12 @@ typedef enum ft_wdtype {
 } ft_wdtype;
 
 typedef enum ft_fetch_mode {
-  FT_FETCH_COPY_ENGINE = 0, /* cudaMemcpyAsync per miss, issued by a library host thread */
-  FT_FETCH_SM_PULL = 1      /* a kernel on the copy stream loads the blobs over the host link */
+  /* cudaMemcpyAsync per miss, issued by a library host thread that reads each
+   * event's miss list from a ring the route kernel writes to mapped host
+   * memory; the FFN waits for a ready flag set after the copies.  Copy engines
+   * leave the SMs and their memory path to the kernels. */
+  FT_FETCH_COPY_ENGINE = 0,
+  FT_FETCH_SM_PULL = 1 /* a kernel on the copy stream loads the blobs over the host link */
 } ft_fetch_mode;
 
 /*
@@ -95,6 +99,7 @@ typedef struct ft_cache_config {
 } ft_cache_config;
 
 typedef struct ft_cache ft_cache; /* opaque, library-owned */
+typedef struct ft_step_graph ft_step_graph; /* opaque, library-owned */
 
 /* Counters accumulated since create (or the last ft_reset_stats). */
 typedef struct ft_stats {
@@ -114,8 +119,6 @@ typedef struct ft_timing {
   double route_ms;  int64_t route_n;   /* route_classify kernel, compute stream */
   double fetch_ms;  int64_t fetch_n;   /* miss copies, copy stream (first to last copy of a layer) */
   double ffn_ms;    int64_t ffn_n;     /* expert FFN kernels of one ft_moe_forward, compute stream */
-  double gemv_ms;   int64_t gemv_n;    /* decode gate/up kernel alone */
-  double down_ms;   int64_t down_n;    /* decode down/combine kernel alone */
 } ft_timing;
 
 /* Header of one layer's plan (see ft_get_plan). */
@@ -175,6 +178,11 @@ ft_status ft_cache_resize(ft_cache* cache, void* new_pool, int64_t new_num_slots
  * The event number t increments by one per call.  Victims are the least
  * recently used slots excluding this event's hits and the previous event's
  * slots (which the previous layer's FFN may still read).  T may be 0.
+ * The kernel runs on a library stream that first waits for all work already
+ * enqueued on the compute stream (the logits, and the FFN of two layers back
+ * in the double-buffered schedule); its outputs are ordered before this
+ * layer's ft_moe_forward on the compute stream and before ft_synchronize,
+ * not before other work the caller enqueues in between.
  * Errors: FT_ERR_INVALID_ARG (layer, T > max_tokens, null logits),
  * FT_ERR_STATE (this layer's previous plan is still being fetched and its
  * fetch failed), FT_ERR_CUDA.
@@ -271,6 +279,38 @@ ft_status ft_moe_decode_ffn_static(int32_t hidden, int32_t inter, int32_t wdtype
                                    int32_t top_k, const void* slot_pool, int64_t num_slots,
                                    const int32_t* expert_slot, const int32_t* topk_idx, const float* topk_w,
                                    const void* x, int32_t T, void* y, void* stream);
+
+/*
+ * Step graphs: one decode/prefill step of all L layers captured into a CUDA
+ * graph, so a step costs one launch instead of ~5 API calls per layer (the
+ * pages capture their whole execution layer in a CUDA graph: "FreeToken:
+ * Efficient Edge-Native MoE Serving ...", design paragraph).  The captured
+ * schedule is the one ft_route_classify / ft_fetch_misses / ft_moe_forward
+ * give when called as
+ *   double_buffer: route(0); fetch(0); for l: { route(l+1); fetch(l+1); forward(l) }
+ *   serial:        for l: { route(l); fetch(l); forward(l) }
+ * with logits[l] (device f32 [T][E]), x[l] (device [T][H]) and y[l] (device
+ * f32 [T][H]) baked in: refill those buffers before each launch.  The event
+ * counter and the pin rule advance on the device, so replays continue the
+ * cache's decision stream exactly as direct calls would.  Works in both fetch
+ * modes (in copy-engine mode the library's copy thread serves the replays'
+ * events from the ring as they are routed).  Needs no layer with a fetched,
+ * not yet forwarded plan (FT_ERR_STATE).  Create is synchronous; launch
+ * enqueues the step on the cache's compute stream.  With `timing` set the
+ * graph records events around each layer's route kernel, miss fetch and FFN
+ * kernels; ft_step_graph_timing waits for the last launch and returns them
+ * (ms; any pointer may be NULL; arrays hold L entries).
+ */
+ft_status ft_step_graph_create(ft_cache* cache, const float* const* logits, const void* const* x, float* const* y,
+                               int32_t T, int32_t double_buffer, int32_t timing, ft_step_graph** out);
+ft_status ft_step_graph_launch(ft_step_graph* graph);
+ft_status ft_step_graph_timing(ft_step_graph* graph, double* route_ms, double* fetch_ms, double* ffn_ms,
+                               double* step_ms);
+/* Timeline of the graph's last launch (waits for it): t_ms[6*l + j] = time
+ * from the step's start to the route begin/end (j = 0, 1), fetch begin/end
+ * (2, 3) and FFN begin/end (4, 5) of layer l.  Needs a timing graph. */
+ft_status ft_step_graph_trace(ft_step_graph* graph, double* t_ms);
+ft_status ft_step_graph_destroy(ft_step_graph* graph);
 
 const char* ft_status_str(ft_status s);
 /* Message of the calling thread's last error ("" if none). */

@@ -171,3 +171,53 @@ def run_parity(w: W.Workload, steps: int | None = None, fetch_mode: int = 1, dou
     finally:
         cache.close()
     return report
+
+
+def run_parity_graph(w: W.Workload, steps: int, bank_blobs: int | None = None, double_buffer: bool = True,
+                     ffn_every: int = 1, device="cuda:0", timing: bool = False, fetch_mode: int = 1):
+    """Replay one captured step graph for `steps` steps and compare every
+    layer's plan, the tables after each step, and sampled FFN outputs with the
+    oracle (the plans stay readable after the step: each layer keeps its own)."""
+    from expert_cache_host_layer_gb300.pipeline import ExpertCache, StepGraph
+    dev = torch.device(device)
+    bank, n_blobs = make_bank(w, bank_blobs)
+    logits = W.router_logits(w.replace(steps=steps))
+    cache = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots,
+                        max(w.tokens, 1), bank, n_blobs, fetch_mode=fetch_mode, device=device)
+    ref = ExpertCacheOracle(w.num_layers, w.num_experts, w.num_slots)
+    L, T, k = w.num_layers, w.tokens, w.top_k
+    lg_buf = [torch.empty((T, w.num_experts), dtype=torch.float32, device=dev) for _ in range(L)]
+    x_buf = [torch.empty((T, w.hidden), dtype=cache.act_dtype, device=dev) for _ in range(L)]
+    y_buf = [torch.empty((T, w.hidden), dtype=torch.float32, device=dev) for _ in range(L)]
+    report = {"events": 0, "ffn_checked": 0, "max_err": 0.0}
+    graph = StepGraph(cache, lg_buf, x_buf, y_buf, double_buffer, timing=timing)
+    try:
+        for s in range(steps):
+            xs_h = [W.hidden_states(w, s, l) for l in range(L)]
+            for l in range(L):
+                lg_buf[l].copy_(torch.from_numpy(np.ascontiguousarray(logits[s, l])))
+                x_buf[l].copy_(to_act(xs_h[l], w, dev))
+            graph.launch()
+            cache.synchronize()
+            for l in range(L):
+                ridx, rw = orouting.route(logits[s, l], k)
+                ev = ref.event(l, ridx)
+                plan = cache.plan(l)
+                errs = compare_event(plan, ev, ridx, ridx, None, rw)
+                assert not errs, f"graph step {s}, layer {l}: {errs[:3]}"
+                report["events"] += 1
+                if ffn_every and ev.t % ffn_every == 0:
+                    yr = oracle_ffn(w, bank, n_blobs, l, xs_h[l], ridx, rw)
+                    mx, _ = ffn_error(y_buf[l].cpu().numpy(), yr)
+                    report["max_err"] = max(report["max_err"], mx)
+                    report["ffn_checked"] += 1
+                    assert mx <= TOL[w.wdtype], f"graph step {s}, layer {l}: FFN err {mx:.3e}"
+            k2s, sk, ts = cache.tables()
+            rk2s, rsk, rts = ref.tables()
+            assert np.array_equal(k2s, rk2s) and np.array_equal(sk, rsk) and np.array_equal(ts, rts), f"step {s}"
+            if timing:
+                report["trace"] = graph.trace()
+    finally:
+        graph.close()
+        cache.close()
+    return report

@@ -61,3 +61,29 @@ def test_dsv4_fp8_with_resize():
     rep = run_parity(w, check_tables_every=97, ffn_every=197)
     assert rep["events"] == 1024 * 24 and rep["resize_moves"] > 0
     print("dsv4:", rep)
+
+
+@pytest.mark.parametrize("fetch_mode", [0, 1])
+@pytest.mark.parametrize("double_buffer", [True, False])
+def test_tiny_step_graph_replay(double_buffer, fetch_mode):
+    from tests.harness import run_parity_graph
+    rep = run_parity_graph(W.TINY, steps=64, double_buffer=double_buffer, fetch_mode=fetch_mode)
+    assert rep["events"] == 128 and rep["ffn_checked"] == 128
+
+
+@pytest.mark.parametrize("fetch_mode", [0, 1])
+def test_qwen35b_step_graph_replay(fetch_mode):
+    from tests.harness import run_parity_graph
+    rep = run_parity_graph(W.QWEN35B_DECODE, steps=40, bank_blobs=512, ffn_every=13, fetch_mode=fetch_mode)
+    assert rep["events"] == 40 * 40
+
+
+def test_qwen35b_timing_graph_keeps_dependencies():
+    """A graph with timing event nodes computes the same results, and each
+    layer's FFN starts after its fetch and its route have ended."""
+    from tests.harness import run_parity_graph
+    rep = run_parity_graph(W.QWEN35B_DECODE, steps=6, bank_blobs=512, ffn_every=3, timing=True, fetch_mode=1)
+    tr = rep["trace"]  # [L][route b/e, fetch b/e, ffn b/e]
+    print("trace (us):", (1e3 * tr[:6]).round(1).tolist())
+    for l in range(tr.shape[0]):
+        assert tr[l, 1] <= tr[l, 4] and tr[l, 3] <= tr[l, 4], l
