@@ -45,7 +45,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=16)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=W.QWEN35B_DECODE.name, choices=sorted(W.ALL))
-    p.add_argument("--fetch-mode", type=int, default=0, help="0 copy engine, 1 SM pull")
+    p.add_argument("--fetch-mode", type=int, default=1, help="0 copy engine, 1 SM pull")
     p.add_argument("--pull-ctas", type=int, default=0)
     p.add_argument("--copy-streams", type=int, default=1)
     p.add_argument("--serial", action="store_true", help="double buffering off")
@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--no-link", action="store_true")
     p.add_argument("--trace", action="store_true", help="print one step's per-layer timeline to stderr")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--timing-steps", type=int, default=64,
+                   help="steps of the second timed pass (graphs with per-phase events) for the roofline")
     return p.parse_args()
 
 
@@ -299,7 +301,7 @@ def run_ours(args, w):
     synth.expert_blobs(w.seed, w.hidden, w.inter, w.wdtype, np.arange(n_blobs), out_ptr=bank.data_ptr())
     gen_s = time.perf_counter() - t_setup
 
-    steps_total = args.warmup + args.steps
+    steps_total = args.warmup + args.steps + args.timing_steps
     wl = w.replace(steps=steps_total, seed=w.seed + rank)  # independent replicas per rank
     logits_h = W.router_logits(wl)                             # [S][L][T][E]
     x_h = np.stack([np.stack([W.hidden_states(wl, s, l) for l in range(w.num_layers)]) for s in range(steps_total)])
@@ -321,25 +323,20 @@ def run_ours(args, w):
     use_graph = True
     cache = make_cache()
     stream = cache.stream
-    graphs = []
-    if use_graph:
-        graphs = [StepGraph(cache, list(lg_buf), list(x_buf), list(y_buf), double, timing=True) for _ in range(2)]
+    # plain graphs for the timed steps; graphs with per-phase event nodes (which
+    # slow a step down) only for the second, roofline pass
+    graphs = [StepGraph(cache, list(lg_buf), list(x_buf), list(y_buf), double) for _ in range(2)]
+    tgraphs = [StepGraph(cache, list(lg_buf), list(x_buf), list(y_buf), double, timing=True) for _ in range(2)]
 
-    def step(s, i):
+    def step(s, i, gs):
         lg_buf.copy_(logits_d[s], non_blocking=True)
         x_buf.copy_(x_d[s], non_blocking=True)
-        if use_graph:
-            graphs[i % 2].launch()
-        else:
-            cache.run_step(list(lg_buf), list(x_buf), list(y_buf), double_buffer=double)
+        gs[i % 2].launch()
 
     for s in range(args.warmup):
-        step(s, s)
+        step(s, s, graphs)
     cache.synchronize()
     st0 = cache.stats()
-    if not use_graph or args.fetch_mode == 0:  # copy-engine fetches are timed by the library's copy thread
-        cache.timing_enable(True)
-    acc = {"route": 0.0, "fetch": 0.0, "ffn": 0.0, "n": 0}
     sampler = ClockSampler(local)
     sampler.start()
     barrier(world)
@@ -347,47 +344,58 @@ def run_ours(args, w):
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for i, s in enumerate(range(args.warmup, steps_total)):
-        step(s, i)
-        if use_graph and i > 0:  # the previous step's per-layer event times (it is done or nearly so)
-            r, fe, f, _ = graphs[(i - 1) % 2].timing()
-            acc["route"] += r.sum(); acc["fetch"] += fe.sum(); acc["ffn"] += f.sum(); acc["n"] += 1
+    for i, s in enumerate(range(args.warmup, args.warmup + args.steps)):
+        step(s, i, graphs)
     ev1.record(stream)
     cache.synchronize()
     torch.cuda.synchronize(dev)
     barrier(world)
     clocks = sampler.stop()
     elapsed_ms = ev0.elapsed_time(ev1)
-    if use_graph and args.trace and rank == 0:
-        tr = graphs[(args.steps - 1) % 2].trace()
+    st1 = cache.stats()
+
+    # ---- second timed pass: per-layer route / fetch / FFN event times -----
+    acc = {"route": 0.0, "fetch": 0.0, "ffn": 0.0, "n": 0, "step": 0.0}
+    if args.fetch_mode == 0:  # copy-engine fetches are timed by the library's copy thread
+        cache.timing_enable(True)
+    t_first = args.warmup + args.steps
+    for i, s in enumerate(range(t_first, t_first + args.timing_steps)):
+        step(s, i, tgraphs)
+        if i > 0:  # the previous step's events (it is done or nearly so)
+            r, fe, f, st_ms = tgraphs[(i - 1) % 2].timing()
+            acc["route"] += r.sum(); acc["fetch"] += fe.sum(); acc["ffn"] += f.sum(); acc["n"] += 1
+            acc["step"] += st_ms
+    cache.synchronize()
+    if args.timing_steps:
+        r, fe, f, st_ms = tgraphs[(args.timing_steps - 1) % 2].timing()
+        acc["route"] += r.sum(); acc["fetch"] += fe.sum(); acc["ffn"] += f.sum(); acc["n"] += 1
+        acc["step"] += st_ms
+    tm = {"route_ms": acc["route"], "fetch_ms": acc["fetch"], "ffn_ms": acc["ffn"],
+          "route_n": acc["n"] * L, "fetch_n": acc["n"] * L, "ffn_n": acc["n"] * L}
+    if args.fetch_mode == 0:
+        ct = cache.timing()
+        tm["fetch_ms"], tm["fetch_n"] = ct["fetch_ms"], ct["fetch_n"]
+        cache.timing_enable(False)
+    st2 = cache.stats()
+    if args.trace and rank == 0 and args.timing_steps:
+        tr = tgraphs[(args.timing_steps - 1) % 2].trace()
         print("layer  route_b route_e  fetch_b fetch_e  ffn_b  ffn_e  (us from step start)", file=sys.stderr)
         for l in range(L):
             print(f"{l:5d} " + " ".join(f"{1e3 * v:7.1f}" for v in tr[l]), file=sys.stderr)
-    if use_graph:
-        r, fe, f, _ = graphs[(args.steps - 1) % 2].timing()
-        acc["route"] += r.sum(); acc["fetch"] += fe.sum(); acc["ffn"] += f.sum(); acc["n"] += 1
-        tm = {"route_ms": acc["route"], "fetch_ms": acc["fetch"], "ffn_ms": acc["ffn"],
-              "route_n": acc["n"] * L, "fetch_n": acc["n"] * L, "ffn_n": acc["n"] * L}
-        if args.fetch_mode == 0:
-            ct = cache.timing()
-            tm["fetch_ms"], tm["fetch_n"] = ct["fetch_ms"], ct["fetch_n"]
-            cache.timing_enable(False)
-    else:
-        tm = cache.timing()
-        cache.timing_enable(False)
-    st1 = cache.stats()
     elapsed_ms = max_over_ranks(elapsed_ms, world)
     tokens = world * args.steps * T
     value = tokens / (elapsed_ms / 1e3)
 
-    d = {k: st1[k] - st0[k] for k in st1}
+    d = {k: st1[k] - st0[k] for k in st1}    # the timed steps
+    d2 = {k: st2[k] - st1[k] for k in st1}   # the roofline pass
     eb = w.expert_bytes
-    ffn_bytes_per_launch = d["unique_experts"] * eb / max(1, tm["ffn_n"])
+    ffn_bytes_per_launch = d2["unique_experts"] * eb / max(1, tm["ffn_n"])
     ffn_ms = tm["ffn_ms"] / max(1, tm["ffn_n"])
     peak, peak_kind = measured_peaks()
-    achieved = ffn_bytes_per_launch / (ffn_ms / 1e3) / 1e9
-    fetch_gbs = d["bytes_fetched"] / max(1e-9, tm["fetch_ms"] / 1e3) / 1e9 if tm["fetch_n"] else None
-    for g in graphs:
+    achieved = ffn_bytes_per_launch / (ffn_ms / 1e3) / 1e9 if ffn_ms > 0 else None
+    fetch_gbs = d2["bytes_fetched"] / max(1e-9, tm["fetch_ms"] / 1e3) / 1e9 if tm["fetch_ms"] > 0 else None
+    n_tsteps = max(1, acc["n"])
+    for g in graphs + tgraphs:
         g.close()
 
     # ---- end to end through the C ABI with host buffers -------------------
@@ -450,9 +458,14 @@ def run_ours(args, w):
             "expert_gemm_gbs": achieved,
             "miss_copy": {"gbs": fetch_gbs, "bytes_per_step": d["bytes_fetched"] / args.steps,
                           "mode": ["copy_engine", "sm_pull"][args.fetch_mode], "link": link},
-            "phase_ms_per_step": {k: tm[f"{k}_ms"] / args.steps for k in ("route", "fetch", "ffn")},
-            "roofline": {"kernel": "decode expert FFN: gateup_kernel + down_kernel (PDL pair), one ft_moe_forward",
-                         "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "phase_ms_per_step": dict({k: tm[f"{k}_ms"] / n_tsteps for k in ("route", "fetch", "ffn")},
+                                      step=acc["step"] / n_tsteps, steps=acc["n"],
+                                      note="sums of per-layer kernel times from a second timed pass with "
+                                           "timing graphs (event nodes around every phase)"),
+            "roofline": {"kernel": "ffn_fused_kernel: one cooperative launch per layer (gate/up, SwiGLU, down, "
+                                   "combine), timed by event nodes around it in the timing pass",
+                         "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak if achieved else None,
                          "peak_kind": peak_kind, "traffic": None, "bytes_per_launch": ffn_bytes_per_launch,
                          "launch_us": ffn_ms * 1e3},
             "cpu_baseline": cpu,

@@ -64,6 +64,9 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* bar, uint32_t n) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(n) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -184,7 +187,6 @@ __device__ __forceinline__ float scale_at(const uint8_t* blob, long long scale_o
 
 __host__ __device__ __forceinline__ int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-__device__ __forceinline__ uint4 ldg16(const uint4* p) { return __ldg(p); }
 
 // Shared-memory layouts (bytes), shared by the kernels and their launchers.
 // Plan staged in shared memory: unique_slot[n], u_offset[n+1], rows_by_u[rows].
@@ -485,47 +487,266 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(FfnArgs a) {
 }
 
 // ---------------------------------------------------------------- fused
-// One CTA per SM, all co-resident (cooperative launch), 12 warps.
-//  prologue: thread 0 bulk-copies this CTA's Wd rows (a contiguous range of
-//            output columns, one copy per expert, as many experts as fit) into
-//            shared memory; they do not depend on h, so they stream during
-//            phase 1;
-//  phase 1:  one warp per (expert, intermediate row) task: the Wg and Wu rows
-//            are read with 16-byte loads, all issued before the arithmetic;
-//            the warp writes h = silu(g) * u for each token of the expert;
+// One CTA per SM, all co-resident (cooperative launch): eight consumer warps
+// and one producer warp.
+//  producer: one thread (after the copy-engine ready flag, if any) prefetches
+//            this CTA's Wd rows of every expert into L2, then streams the
+//            CTA's work through a ring of shared-memory stages with bulk
+//            asynchronous copies (completion counted on one mbarrier per
+//            stage; consumers free a stage through a second mbarrier);
+//  phase 1:  the CTA owns a contiguous run of (expert, intermediate row)
+//            pairs; a unit is R consecutive rows of one expert: its R Wg
+//            rows then its R Wu rows, two contiguous blocks of the slot.
+//            Two groups of four warps take alternate units; warp j of a
+//            group takes row pairs j, j+4, ...: it dots the Wg row and the Wu
+//            row with every token of the expert (one pass over x for both)
+//            and writes h = silu(g) * u itself, so units need no CTA-wide
+//            synchronisation;
 //  barrier:  grid-wide (bounded), h complete everywhere;
-//  phase 2:  one warp per output column of the CTA's range: sum over experts
-//            (ascending) and their rows of w * (Wd row . h row).
-// The CTA stays small (384 threads, <= 96 registers, <= 150 KB shared
-// memory) so that a route CTA and a fetch CTA can run on the same SM.
-constexpr int kFThreads = 384;
-constexpr int kFWarps = kFThreads / 32;
+//  phase 2:  the CTA owns output columns [c0, c1), cut into pieces of at
+//            most PR rows; a unit is one piece of as many experts' Wd as fit
+//            in a stage (rows c of Wd are contiguous), pieces outer, experts
+//            inner (ascending), so at this shape the whole of a CTA's Wd is
+//            in shared memory before the grid barrier is passed.  The
+//            column c always belongs to warp (c - piece start) % 8, which
+//            keeps its sum over experts in registers and writes y once.
+//  copy:     in SM-pull mode two more warps copy the NEXT event's missed
+//            blobs from the host bank into their victim slots meanwhile (8 KB
+//            items spread over all CTAs, 8 loads in flight per thread).  The
+//            victims exclude this event's slots (pin rule) and the FFN before
+//            this one has finished, so nothing still reads them; the next FFN
+//            runs after this kernel on the same stream.  One kernel per layer
+//            thus moves the next layer's experts over the host link while
+//            this layer's experts stream from HBM.
+// Every mbarrier wait is bounded; a wait that runs out records
+// FT_ERR_TIMEOUT, sets a CTA-wide abort flag that ends all later waits at
+// once, and the producer still waits (bounded) for its copies in flight
+// before it exits.
+constexpr int kFConsumers = 8;
+constexpr int kFCopyWarps = 2;  // warps kFConsumers + 1 .. : the next event's miss fetch
+constexpr int kFThreads = (kFConsumers + 1 + kFCopyWarps) * 32;
+constexpr int kFCopyUnroll = 8;  // 16-byte loads in flight per copy thread
 constexpr int kFusedSmemBudget = 150 * 1024;
+constexpr int kFStages = 4;
+constexpr int kFStageMax = 32 * 1024;
+constexpr int kFMaxUnitRows = 32;   // R (row pairs of a phase-1 unit)
+constexpr int kFMaxPieceRows = 16;  // PR (Wd rows of a phase-2 unit): two per warp
 
 struct FusedLayout {
-  int cols_max, x_off, h_off, h_bytes, plan_off, w_off, wd_off, wd_cap, bar_off, total;
-  __host__ __device__ FusedLayout(int H, int I, int T, int wsize, int act_bytes, int max_unique, int rows,
-                                  int grid) {
-    cols_max = (H + grid - 1) / grid;  // output columns per CTA
+  int x_off, plan_off, w_off, bar_off, h_off, h_bytes, ring_off, stage_bytes, R, PR, total;
+  __host__ __device__ FusedLayout(int H, int I, int T, int wsize, int act_bytes, int max_unique, int rows) {
+    const int row_g = H * wsize, row_d = I * wsize;
     x_off = 0;
-    h_off = align_up(T * H * act_bytes, 16);
+    plan_off = align_up(T * H * act_bytes, 128);
+    w_off = plan_off + align_up(plan_bytes(max_unique, rows), 16);
+    bar_off = w_off + align_up(rows * 4, 16);
+    h_off = bar_off + align_up((2 * kFStages + 1) * 8, 128);  // full[], empty[], abort word
+    const int fixed = h_off;
     h_bytes = rows * I * 4;
-    if (h_bytes > 32 * 1024) h_bytes = 0;  // larger h is read from L2
-    plan_off = align_up(h_off + h_bytes, 16);
-    w_off = plan_off + plan_bytes(max_unique, rows);
-    wd_off = align_up(w_off + rows * 4, 128);
-    const int per_expert = align_up(cols_max * I * wsize, 128);
-    wd_cap = (kFusedSmemBudget - wd_off - 64) / per_expert;  // experts whose Wd rows fit
-    if (wd_cap < 0) wd_cap = 0;
-    if (wd_cap > max_unique) wd_cap = max_unique;
-    bar_off = wd_off + wd_cap * per_expert;
-    total = bar_off + 16;
+    // h sits in shared memory only if that leaves at least 64 KB of ring
+    if (kFusedSmemBudget - fixed - h_bytes < 64 * 1024) h_bytes = 0;
+    ring_off = align_up(h_off + h_bytes, 128);
+    int sb = (kFusedSmemBudget - ring_off) / kFStages;
+    if (sb > kFStageMax) sb = kFStageMax;
+    stage_bytes = sb / 128 * 128;
+    R = row_g > 0 ? stage_bytes / (2 * row_g) : 0;
+    if (R > kFMaxUnitRows) R = kFMaxUnitRows;
+    PR = row_d > 0 ? stage_bytes / row_d : 0;
+    if (PR > kFMaxPieceRows) PR = kFMaxPieceRows;
+    total = ring_off + kFStages * stage_bytes;
   }
+  __host__ __device__ bool ok() const { return stage_bytes > 0 && R >= 1 && PR >= 1; }
 };
 
-// NC: 16-byte chunks per lane per gate/up row (H*wsize <= 512*NC); MR: most
-// rows (tokens) of one expert, 1 for single-token decode.
-template <int WT, int NC, int MR>
+__device__ __forceinline__ uint4 ld_host16(const uint4* p) {  // streamed once: evict first
+  uint4 v;
+  asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// The copy warps' work: 16-byte words of the next event's missed blobs, in
+// items of kFCopyWarps * 32 * kFCopyUnroll words, item i on CTA i % grid.
+__device__ __forceinline__ void fused_fetch(const PullArgs& p, int ct) {
+  constexpr long long kItem16 = (long long)kFCopyWarps * 32 * kFCopyUnroll;
+  const int n_miss = __ldcg(&p.hdr[PH_MISS]);
+  const long long eb16 = p.expert_bytes >> 4;
+  const long long per_blob = (eb16 + kItem16 - 1) / kItem16;
+  const long long items = (long long)n_miss * per_blob;
+  const uint4* bank = static_cast<const uint4*>(p.bank);
+  uint4* pool = static_cast<uint4*>(p.pool);
+  for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+    const int m = (int)(it / per_blob);
+    const long long c = it - (long long)m * per_blob;
+    const int e = __ldcg(&p.miss_expert[m]);
+    const int slot = __ldcg(&p.miss_slot[m]);
+    const long long blob = ((long long)p.layer * p.E + e) % p.bank_blobs;
+    const uint4* src = bank + blob * eb16 + c * kItem16;
+    uint4* dst = pool + (long long)slot * eb16 + c * kItem16;
+    const long long n = min(kItem16, eb16 - c * kItem16);
+    uint4 v[kFCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kFCopyUnroll; ++u) {
+      const long long i = (long long)u * (kFCopyWarps * 32) + ct;
+      if (i < n) v[u] = ld_host16(src + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kFCopyUnroll; ++u) {
+      const long long i = (long long)u * (kFCopyWarps * 32) + ct;
+      if (i < n) dst[i] = v[u];
+    }
+  }
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Bounded mbarrier wait that gives up at once when the CTA has aborted, and
+// aborts the CTA when it runs out.
+__device__ __forceinline__ bool fwait(uint64_t* bar, uint32_t parity, int32_t* status, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      if (status) atomicCAS(status, 0, (int)FT_ERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// Consumer-side acquire of a ring stage: lane 0 waits, then every lane
+// observes the completed phase itself (so the async-proxy writes are visible
+// to it).
+__device__ __forceinline__ bool stage_acquire(uint64_t* full, uint32_t parity, int32_t* status,
+                                              volatile int* abort_flag) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = fwait(full, parity, status, abort_flag);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) mbar_try_wait(full, parity);
+  return ok;
+}
+
+__device__ __forceinline__ void stage_release(uint64_t* empty) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(empty);
+}
+
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 2, %0;" ::"n"(kFConsumers * 32) : "memory");
+}
+
+// MR: most rows (tokens) of one expert, 1 for single-token decode.
+// Phase 2 of the fused kernel for one CTA: y[t][c] for c in [c0, c1).
+// kHs: h was copied into shared memory; DCL: 16-byte chunks per lane of one
+// Wd row (row bytes = 512 * DCL).  Units continue the ring sequence at `unit`.
+template <int WT, int MR, int DCL, bool kHs>
+__device__ __forceinline__ void fused_phase2(const FfnArgs& a, const FusedLayout& lay, uint8_t* ring,
+                                             uint64_t* full, uint64_t* empty, volatile int* abort_flag,
+                                             const int32_t* p_slot, const int32_t* p_off, const int32_t* p_rows,
+                                             const float* p_w, const float* hbase, int n_u, int c0, int c1,
+                                             int unit) {
+  constexpr int EPC = W<WT>::kEPC, WSZ = W<WT>::kBytes;
+  const int H = a.H, I = a.I, k = a.k, T = a.T;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int SB = lay.stage_bytes;
+  const long long row_d = (long long)I * WSZ, scale_off = 3LL * H * I * WSZ;
+  const int sblk = I / 128;
+  const int sbase = 2 * (I / 128) * (H / 128);
+  for (int p0 = c0; p0 < c1; p0 += lay.PR) {
+    const int PR = min(lay.PR, c1 - p0);
+    const int EU = max(1, SB / (int)(PR * row_d));  // experts per unit (as the producer packs them)
+    float acc[2][MR];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int t = 0; t < MR; ++t) acc[m][t] = 0.0f;
+    for (int ub = 0; ub < n_u; ub += EU, ++unit) {
+      const int s = unit % kFStages;
+      const bool ok = stage_acquire(&full[s], (unit / kFStages) & 1, a.status, abort_flag);
+      const int ne = ok ? min(EU, n_u - ub) : 0;
+#pragma unroll 2
+      for (int k2 = 0; k2 < ne; ++k2) {
+        const int u = ub + k2;
+        const int row0 = p_off[u];
+        const int nrows = min(p_off[u + 1] - row0, MR);
+        int hrow[MR], tok[MR];
+        float wgt[MR];
+#pragma unroll
+        for (int t = 0; t < MR; ++t) {
+          const int row = t < nrows ? p_rows[row0 + t] : 0;
+          hrow[t] = row * I;
+          tok[t] = row / k;
+          wgt[t] = t < nrows ? p_w[row] : 0.0f;
+        }
+        const uint8_t* blob = a.pool + (long long)p_slot[u] * a.expert_bytes;
+        const uint8_t* piece = ring + (size_t)s * SB + (size_t)k2 * PR * row_d;
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const int j = warp + m * kFConsumers;
+          if (j < PR) {
+            const int cc = p0 + j;
+            const uint4* wrow = reinterpret_cast<const uint4*>(piece + j * row_d);
+            float part[MR];
+#pragma unroll
+            for (int t = 0; t < MR; ++t) part[t] = 0.0f;
+#pragma unroll
+            for (int i = 0; i < DCL; ++i) {
+              const int c = i * 32 + lane;
+              float f[EPC];
+              decode_chunk<WT>(wrow[c], f);
+              float sc = 1.0f;
+              if (WT == FT_W_FP8E4M3_B128) sc = scale_at(blob, scale_off, sbase + (cc >> 7) * sblk + ((c * EPC) >> 7));
+#pragma unroll
+              for (int t = 0; t < MR; ++t) {
+                if (t < nrows) {
+                  const float4* hp = reinterpret_cast<const float4*>(hbase + hrow[t] + c * EPC);
+                  float q0 = 0.0f, q1 = 0.0f;
+#pragma unroll
+                  for (int e4 = 0; e4 < EPC / 4; ++e4) {
+                    const float4 hv = kHs ? hp[e4] : __ldcg(hp + e4);
+                    q0 = fmaf(f[4 * e4], hv.x, q0);
+                    q1 = fmaf(f[4 * e4 + 1], hv.y, q1);
+                    q0 = fmaf(f[4 * e4 + 2], hv.z, q0);
+                    q1 = fmaf(f[4 * e4 + 3], hv.w, q1);
+                  }
+                  part[t] = fmaf(sc, q0 + q1, part[t]);
+                }
+              }
+            }
+#pragma unroll
+            for (int t = 0; t < MR; ++t)  // per-lane partial sums; reduced once per column
+              if (t < nrows)
+#pragma unroll
+                for (int tt = 0; tt < MR; ++tt)
+                  if (tt == tok[t]) acc[m][tt] = fmaf(wgt[t], part[t], acc[m][tt]);
+          }
+        }
+      }
+      stage_release(&empty[s]);
+    }
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const int j = warp + m * kFConsumers;
+      if (j < PR) {
+#pragma unroll
+        for (int t = 0; t < MR; ++t) {
+          if (t < T) {
+            const float v = warp_sum(acc[m][t]);
+            if (lane == 0) a.y[(long long)t * H + p0 + j] = v;
+          }
+        }
+      }
+    }
+  }
+}
+
+// NCL: 16-byte chunks per lane of one Wg/Wu row (row bytes <= 512 * NCL);
+// DCL: the same for one Wd row (row bytes = 512 * DCL).
+template <int WT, int MR, int NCL, int DCL>
 __global__ void __maxnreg__(96) ffn_fused_kernel(FfnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr bool kF32 = WT == FT_W_F32;
@@ -533,28 +754,36 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(FfnArgs a) {
   const int H = a.H, I = a.I, k = a.k, T = a.T;
   const int act_bytes = kF32 ? 4 : 2;
   const int rows_total = T * k;
-  const FusedLayout lay(H, I, T, WSZ, act_bytes, a.max_unique, rows_total, gridDim.x);
-  uint8_t* xs = smem + lay.x_off;
-  float* hs = reinterpret_cast<float*>(smem + lay.h_off);
+  const FusedLayout lay(H, I, T, WSZ, act_bytes, a.max_unique, rows_total);
+  const uint8_t* xs = smem + lay.x_off;
   int32_t* p_slot = reinterpret_cast<int32_t*>(smem + lay.plan_off);
   int32_t* p_off = p_slot + a.max_unique;
   int32_t* p_rows = p_off + a.max_unique + 1;
   float* p_w = reinterpret_cast<float*>(smem + lay.w_off);
-  uint8_t* wds = smem + lay.wd_off;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + lay.bar_off);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bar_off);
+  uint64_t* empty = full + kFStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kFStages);
+  float* hs = reinterpret_cast<float*>(smem + lay.h_off);
+  uint8_t* ring = smem + lay.ring_off;
+  const int SB = lay.stage_bytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_u = min(__ldg(&a.hdr[PH_UNIQUE]), a.max_unique);
-  // this CTA's output columns [c0, c1), balanced and contiguous
+  const long long row_g = (long long)H * WSZ, row_d = (long long)I * WSZ;
+  const long long wd_off = 2LL * H * I * WSZ, scale_off = 3LL * H * I * WSZ;
+  // phase-1 rows [q0, q1) of the flattened (expert, intermediate row) index
+  const long long nq = (long long)n_u * I;
+  const int q0 = (int)(nq * blockIdx.x / gridDim.x), q1 = (int)(nq * (blockIdx.x + 1) / gridDim.x);
+  // phase-2 output columns [c0, c1)
   const int c0 = (int)((long long)H * blockIdx.x / gridDim.x);
   const int c1 = (int)((long long)H * (blockIdx.x + 1) / gridDim.x);
-  const long long d_row_bytes = (long long)I * WSZ;
-  const int per_expert = align_up(lay.cols_max * I * WSZ, 128);
-  const long long wd_off = 2LL * H * I * WSZ;
-  const int n_pref = min(n_u, lay.wd_cap);  // experts whose Wd rows are in shared memory
 
+  // ---- prologue (all threads): barriers, plan and x into shared memory
   if (threadIdx.x == 0) {
-    wait_ready_flag(a);
-    mbar_init(bar, 1);
+    for (int s = 0; s < kFStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kFConsumers);
+    }
+    *abort_flag = 0;
     mbar_init_fence();
   }
   for (int i = threadIdx.x; i < n_u; i += kFThreads) p_slot[i] = __ldg(&a.unique_slot[i]);
@@ -566,90 +795,149 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(FfnArgs a) {
   {
     const int n16 = T * H * act_bytes / 16;
     const uint4* src = static_cast<const uint4*>(a.x);
-    for (int i = threadIdx.x; i < n16; i += kFThreads) reinterpret_cast<uint4*>(xs)[i] = src[i];
+    for (int i = threadIdx.x; i < n16; i += kFThreads) reinterpret_cast<uint4*>(smem + lay.x_off)[i] = src[i];
   }
   __syncthreads();
-  if (threadIdx.x == 0 && n_pref > 0 && c1 > c0) {
-    const uint32_t bytes = (uint32_t)((c1 - c0) * d_row_bytes);
-    mbar_expect_tx(bar, bytes * n_pref);
-    for (int u = 0; u < n_pref; ++u)
-      bulk_g2s(wds + (size_t)u * per_expert,
-               a.pool + (long long)p_slot[u] * a.expert_bytes + wd_off + (long long)c0 * d_row_bytes, bytes, bar);
+
+  // ---- copy warps
+  if (warp > kFConsumers) {
+    if (a.nx.hdr) fused_fetch(a.nx, threadIdx.x - (kFConsumers + 1) * 32);
+    return;
   }
 
-  // ---- phase 1: gate/up
-  const long long g_row_bytes = (long long)H * WSZ;
-  const long long scale_off = 3LL * H * I * WSZ;
-  const int nch = H / EPC;
-  {
-    const int sblk = H / 128;
-    const int gw = blockIdx.x * kFWarps + warp, nw = gridDim.x * kFWarps;
-    for (int task = gw; task < n_u * I; task += nw) {
-      const int u = task / I, r = task - u * I;
-      const uint8_t* blob = a.pool + (long long)p_slot[u] * a.expert_bytes;
-      const uint4* grow = reinterpret_cast<const uint4*>(blob + (long long)r * g_row_bytes);
-      const uint4* urow = reinterpret_cast<const uint4*>(blob + (long long)(I + r) * g_row_bytes);
-      uint4 wg[NC], wu[NC];
-#pragma unroll
-      for (int i = 0; i < NC; ++i) {
-        const int c = i * 32 + lane;
-        if (c < nch) {
-          wg[i] = ldg16(grow + c);
-          wu[i] = ldg16(urow + c);
+  // ---- producer warp
+  if (warp == kFConsumers) {
+    if (lane == 0) {
+      wait_ready_flag(a);  // copy-engine mode: the slots' bytes are in place
+      for (int u = 0; u < n_u && c1 > c0; ++u)
+        prefetch_l2(a.pool + (long long)p_slot[u] * a.expert_bytes + wd_off + c0 * row_d,
+                    (uint32_t)((c1 - c0) * row_d));
+      int i = 0;
+      bool go = true;
+      auto issue = [&](const uint8_t* s0, uint32_t b0, const uint8_t* s1, uint32_t b1) {
+        const int s = i % kFStages;
+        if (i >= kFStages && !fwait(&empty[s], ((i / kFStages) - 1) & 1, a.status, abort_flag)) {
+          go = false;
+          return;
+        }
+        mbar_expect_tx(&full[s], b0 + b1);
+        bulk_g2s(ring + (size_t)s * SB, s0, b0, &full[s]);
+        if (b1) bulk_g2s(ring + (size_t)s * SB + b0, s1, b1, &full[s]);
+        ++i;
+      };
+      for (int q = q0; q < q1 && go;) {
+        const int u = q / I, r = q - u * I;
+        const int R = min(min(lay.R, I - r), q1 - q);
+        const uint8_t* blob = a.pool + (long long)p_slot[u] * a.expert_bytes;
+        issue(blob + r * row_g, (uint32_t)(R * row_g), blob + (I + r) * row_g, (uint32_t)(R * row_g));
+        q += R;
+      }
+      for (int p0 = c0; p0 < c1 && go; p0 += lay.PR) {
+        const int PR = min(lay.PR, c1 - p0);
+        const int EU = max(1, SB / (int)(PR * row_d));  // experts per unit
+        for (int ub = 0; ub < n_u && go; ub += EU) {
+          const int s = i % kFStages;
+          if (i >= kFStages && !fwait(&empty[s], ((i / kFStages) - 1) & 1, a.status, abort_flag)) {
+            go = false;
+            break;
+          }
+          const int ne = min(EU, n_u - ub);
+          mbar_expect_tx(&full[s], (uint32_t)(ne * PR * row_d));
+          for (int k2 = 0; k2 < ne; ++k2)
+            bulk_g2s(ring + (size_t)s * SB + (size_t)k2 * PR * row_d,
+                     a.pool + (long long)p_slot[ub + k2] * a.expert_bytes + wd_off + p0 * row_d,
+                     (uint32_t)(PR * row_d), &full[s]);
+          ++i;
         }
       }
+      // no copy may still be writing this CTA's shared memory when it exits
+      // (bounded, and not cut short by an abort)
+      for (int j = i - kFStages < 0 ? 0 : i - kFStages; j < i; ++j)
+        mbar_wait(&full[j % kFStages], (j / kFStages) & 1, a.status);
+    }
+    return;
+  }
+
+  // ---- consumers, phase 1: gate/up + SwiGLU
+  const int ctid = threadIdx.x;  // 0 .. 255
+  int unit = 0;
+  {
+    const int sblk = H / 128;
+    const int nch = (int)(row_g / 16);  // 16-byte chunks per row
+    const int group = warp >> 2, gw = warp & 3;
+    for (int q = q0; q < q1; ++unit) {
+      const int u = q / I, r = q - u * I;
+      const int R = min(min(lay.R, I - r), q1 - q);
+      q += R;
+      if ((unit & 1) != group) continue;  // the other group's unit
+      const int s = unit % kFStages;
+      const bool ok = stage_acquire(&full[s], (unit / kFStages) & 1, a.status, abort_flag);
       const int row0 = p_off[u];
       const int nrows = min(p_off[u + 1] - row0, MR);
-      float ag[MR], au[MR];
+      const uint8_t* blob = a.pool + (long long)p_slot[u] * a.expert_bytes;
+      const uint8_t* xrow[MR];
 #pragma unroll
-      for (int q = 0; q < MR; ++q) ag[q] = au[q] = 0.0f;
+      for (int t = 0; t < MR; ++t)
+        xrow[t] = xs + (size_t)(t < nrows ? p_rows[row0 + t] / k : 0) * H * act_bytes;
+      for (int jp = gw; jp < R && ok; jp += 4) {
+        const uint4* grow = reinterpret_cast<const uint4*>(ring + (size_t)s * SB + jp * row_g);
+        const uint4* urow = reinterpret_cast<const uint4*>(ring + (size_t)s * SB + (R + jp) * row_g);
+        const int rr = r + jp;
+        float ag[MR], au[MR];
 #pragma unroll
-      for (int i = 0; i < NC; ++i) {
-        const int c = i * 32 + lane;
-        if (c < nch) {
-          float fg[EPC], fu[EPC];
-          decode_chunk<WT>(wg[i], fg);
-          decode_chunk<WT>(wu[i], fu);
-          float sg = 1.0f, su = 1.0f;
-          if (WT == FT_W_FP8E4M3_B128) {
-            const int cb = (c * EPC) >> 7;
-            sg = scale_at(blob, scale_off, (r >> 7) * sblk + cb);
-            su = scale_at(blob, scale_off, (I >> 7) * sblk + (r >> 7) * sblk + cb);
-          }
+        for (int t = 0; t < MR; ++t) ag[t] = au[t] = 0.0f;
 #pragma unroll
-          for (int q = 0; q < MR; ++q) {
-            if (q < nrows) {
-              float xv[EPC];
-              load_act<kF32, EPC>(xs + (size_t)(p_rows[row0 + q] / k) * H * act_bytes, c * EPC, xv);
-              float pg = 0.0f, pu = 0.0f;
+        for (int i = 0; i < NCL; ++i) {
+          const int c = i * 32 + lane;
+          if (c < nch) {
+            float fg[EPC], fu[EPC];
+            decode_chunk<WT>(grow[c], fg);
+            decode_chunk<WT>(urow[c], fu);
+            float sg = 1.0f, su = 1.0f;
+            if (WT == FT_W_FP8E4M3_B128) {
+              const int cb = (c * EPC) >> 7;
+              sg = scale_at(blob, scale_off, (rr >> 7) * sblk + cb);
+              su = scale_at(blob, scale_off, (I / 128) * sblk + (rr >> 7) * sblk + cb);
+            }
 #pragma unroll
-              for (int e = 0; e < EPC; ++e) {
-                pg = fmaf(fg[e], xv[e], pg);
-                pu = fmaf(fu[e], xv[e], pu);
+            for (int t = 0; t < MR; ++t) {
+              if (t < nrows) {
+                float xv[EPC];
+                load_act<kF32, EPC>(xrow[t], c * EPC, xv);
+                float pg0 = 0.0f, pg1 = 0.0f, pu0 = 0.0f, pu1 = 0.0f;
+#pragma unroll
+                for (int e = 0; e < EPC; e += 2) {
+                  pg0 = fmaf(fg[e], xv[e], pg0);
+                  pu0 = fmaf(fu[e], xv[e], pu0);
+                  pg1 = fmaf(fg[e + 1], xv[e + 1], pg1);
+                  pu1 = fmaf(fu[e + 1], xv[e + 1], pu1);
+                }
+                ag[t] = fmaf(sg, pg0 + pg1, ag[t]);
+                au[t] = fmaf(su, pu0 + pu1, au[t]);
               }
-              ag[q] = fmaf(sg, pg, ag[q]);
-              au[q] = fmaf(su, pu, au[q]);
             }
           }
         }
-      }
 #pragma unroll
-      for (int q = 0; q < MR; ++q) {
-        if (q < nrows) {
-          const float g = warp_sum(ag[q]);
-          const float v = warp_sum(au[q]);
-          if (lane == 0) a.h[(long long)p_rows[row0 + q] * I + r] = g / (1.0f + expf(-g)) * v;
+        for (int t = 0; t < MR; ++t) {
+          if (t < nrows) {
+            const float g = warp_sum(ag[t]);
+            const float v = warp_sum(au[t]);
+            if (lane == t) a.h[(long long)p_rows[row0 + t] * I + rr] = g / (1.0f + expf(-g)) * v;
+          }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_n(&empty[s], 2);  // four warps of a group stand for the eight
     }
   }
 
   // ---- every CTA's h is written and visible after this (bounded)
-  __syncthreads();
-  if (threadIdx.x == 0) {
+  __threadfence();
+  consumers_sync();
+  if (ctid == 0) {
     unsigned* count = a.gbar;
     unsigned* gen = a.gbar + 1;
-    __threadfence();
     const unsigned g = *reinterpret_cast<volatile unsigned*>(gen);
     if (atomicAdd(count, 1u) == gridDim.x - 1) {
       *reinterpret_cast<volatile unsigned*>(count) = 0u;
@@ -660,87 +948,50 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(FfnArgs a) {
       while (*reinterpret_cast<volatile unsigned*>(gen) == g) {
         if (global_ns() - t0 > kWaitLimitNs) {
           if (a.status) atomicCAS(a.status, 0, (int)FT_ERR_TIMEOUT);
+          *abort_flag = 1;
           break;
         }
       }
     }
     __threadfence();
   }
-  __syncthreads();
-
-  // ---- phase 2: down + combine
+  consumers_sync();
   const bool h_in_smem = lay.h_bytes > 0;
   if (h_in_smem) {
     const int n4 = rows_total * I / 4;
     const float4* src = reinterpret_cast<const float4*>(a.h);
-    for (int i = threadIdx.x; i < n4; i += kFThreads) reinterpret_cast<float4*>(hs)[i] = __ldcg(src + i);
-    __syncthreads();
+    for (int i = ctid; i < n4; i += kFConsumers * 32) reinterpret_cast<float4*>(hs)[i] = __ldcg(src + i);
+    consumers_sync();
   }
-  const float* hbase = h_in_smem ? hs : a.h;
-  bool wd_ready = true;
-  if (n_pref > 0 && c1 > c0) {  // every thread acquires the bulk copies' completion
-    if (lane == 0) wd_ready = mbar_wait(bar, 0, a.status);
-    wd_ready = __shfl_sync(0xffffffffu, wd_ready, 0);
-    if (wd_ready) mbar_try_wait(bar, 0);
-  }
-  const int dch = I / EPC;
-  const int sblk = I / 128;
-  const int sbase = 2 * (I / 128) * (H / 128);
-  for (int cc = c0 + warp; cc < c1; cc += kFWarps) {
-    float acc[MR];
-#pragma unroll
-    for (int q = 0; q < MR; ++q) acc[q] = 0.0f;
-    for (int u = 0; u < n_u; ++u) {
-      const uint8_t* blob = a.pool + (long long)p_slot[u] * a.expert_bytes;
-      const uint4* wrow = (u < n_pref && wd_ready)
-                              ? reinterpret_cast<const uint4*>(wds + (size_t)u * per_expert + (cc - c0) * d_row_bytes)
-                              : reinterpret_cast<const uint4*>(blob + wd_off + (long long)cc * d_row_bytes);
-      const int row0 = p_off[u];
-      const int nrows = min(p_off[u + 1] - row0, MR);
-      float part[MR];
-#pragma unroll
-      for (int q = 0; q < MR; ++q) part[q] = 0.0f;
-      for (int c = lane; c < dch; c += 32) {
-        float f[EPC];
-        decode_chunk<WT>(u < n_pref && wd_ready ? wrow[c] : ldg16(wrow + c), f);
-        float sc = 1.0f;
-        if (WT == FT_W_FP8E4M3_B128) sc = scale_at(blob, scale_off, sbase + (cc >> 7) * sblk + ((c * EPC) >> 7));
-#pragma unroll
-        for (int q = 0; q < MR; ++q) {
-          if (q < nrows) {
-            const float4* hp = reinterpret_cast<const float4*>(hbase + (long long)p_rows[row0 + q] * I + c * EPC);
-            float p = 0.0f;
-#pragma unroll
-            for (int e4 = 0; e4 < EPC / 4; ++e4) {
-              const float4 hv = h_in_smem ? hp[e4] : __ldcg(hp + e4);
-              p = fmaf(f[4 * e4], hv.x, p);
-              p = fmaf(f[4 * e4 + 1], hv.y, p);
-              p = fmaf(f[4 * e4 + 2], hv.z, p);
-              p = fmaf(f[4 * e4 + 3], hv.w, p);
-            }
-            part[q] = fmaf(sc, p, part[q]);
-          }
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < MR; ++q) {
-        if (q < nrows) {
-          const int row = p_rows[row0 + q];
-          const int t = row / k;
-#pragma unroll
-          for (int tt = 0; tt < MR; ++tt)
-            if (tt == t) acc[tt] = fmaf(p_w[row], part[q], acc[tt]);
-        }
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < MR; ++t) {
-      if (t < T) {
-        const float v = warp_sum(acc[t]);
-        if (lane == 0) a.y[(long long)t * H + cc] = v;
+  // ---- consumers, phase 2: down projection + gate-weighted combine
+  if (h_in_smem)
+    fused_phase2<WT, MR, DCL, true>(a, lay, ring, full, empty, abort_flag, p_slot, p_off, p_rows, p_w, hs, n_u, c0,
+                                    c1, unit);
+  else
+    fused_phase2<WT, MR, DCL, false>(a, lay, ring, full, empty, abort_flag, p_slot, p_off, p_rows, p_w, a.h, n_u,
+                                     c0, c1, unit);
+
+  // ---- copy-engine mode: the last CTA to finish tells the copy thread that
+  // this event's slots are no longer read (every bulk copy of every CTA has
+  // been consumed by now)
+  if (a.done_host) {
+    consumers_sync();
+    if (ctid == 0) {
+      __threadfence();
+      if (atomicAdd(a.gbar + 2, 1u) == gridDim.x - 1) {
+        *reinterpret_cast<volatile unsigned*>(a.gbar + 2) = 0u;
+        const int ev = __ldg(&a.hdr[PH_EVENT]);
+        __threadfence_system();
+        asm volatile("st.release.sys.global.b32 [%0], %1;" ::"l"(a.done_host + (ev % kRing)), "r"(ev) : "memory");
       }
     }
   }
+}
+
+__global__ void signal_done_kernel(const int32_t* hdr, int32_t* done_host) {
+  const int ev = *reinterpret_cast<const volatile int32_t*>(hdr + PH_EVENT);
+  __threadfence_system();
+  asm volatile("st.release.sys.global.b32 [%0], %1;" ::"l"(done_host + (ev % kRing)), "r"(ev) : "memory");
 }
 
 int num_sms() {
@@ -764,6 +1015,8 @@ int blocks_per_sm_t(K kernel, int threads, int smem, cudaError_t* err) {
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
   *err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (*err == cudaSuccess)  // same split as the route and fetch kernels, so they can share an SM
+    *err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (*err != cudaSuccess) return 0;
   int per_sm = 1;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
@@ -816,27 +1069,10 @@ cudaError_t down_typed(const FfnArgs& a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, down_kernel<WT>, a);
 }
 
-template <int WT>
-cudaError_t fused_typed(const FfnArgs& a, cudaStream_t s) {
-  constexpr int EPC = W<WT>::kEPC;
-  const int nch = a.H / EPC;
-  const int grid = num_sms();  // one CTA per SM, all co-resident
-  const FusedLayout lay(a.H, a.I, a.T, W<WT>::kBytes, WT == FT_W_F32 ? 4 : 2, a.max_unique, a.T * a.k, grid);
-  if (lay.total > kFusedSmemBudget + 1024 || !a.gbar || nch > 32 * 8) return cudaErrorNotSupported;
-  const void* fn;
+template <int WT, int MR, int NCL, int DCL>
+cudaError_t fused_launch(const FfnArgs& a, const FusedLayout& lay, int grid, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
-  int per_sm = 0;
-  if (a.T == 1) {
-    fn = nch <= 64 ? reinterpret_cast<const void*>(ffn_fused_kernel<WT, 2, 1>)
-                   : reinterpret_cast<const void*>(ffn_fused_kernel<WT, 8, 1>);
-    per_sm = nch <= 64 ? blocks_per_sm_t(ffn_fused_kernel<WT, 2, 1>, kFThreads, lay.total, &e)
-                       : blocks_per_sm_t(ffn_fused_kernel<WT, 8, 1>, kFThreads, lay.total, &e);
-  } else {
-    fn = nch <= 64 ? reinterpret_cast<const void*>(ffn_fused_kernel<WT, 2, kMaxRows>)
-                   : reinterpret_cast<const void*>(ffn_fused_kernel<WT, 8, kMaxRows>);
-    per_sm = nch <= 64 ? blocks_per_sm_t(ffn_fused_kernel<WT, 2, kMaxRows>, kFThreads, lay.total, &e)
-                       : blocks_per_sm_t(ffn_fused_kernel<WT, 8, kMaxRows>, kFThreads, lay.total, &e);
-  }
+  const int per_sm = blocks_per_sm_t(ffn_fused_kernel<WT, MR, NCL, DCL>, kFThreads, lay.total, &e);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorNotSupported;
   cudaLaunchConfig_t cfg = {};
@@ -850,10 +1086,31 @@ cudaError_t fused_typed(const FfnArgs& a, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void* args[] = {const_cast<FfnArgs*>(&a)};
-  return cudaLaunchKernelExC(&cfg, fn, args);
+  return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(ffn_fused_kernel<WT, MR, NCL, DCL>), args);
+}
+
+template <int WT>
+cudaError_t fused_typed(const FfnArgs& a, cudaStream_t s) {
+  const int grid = num_sms();  // one CTA per SM, all co-resident
+  const FusedLayout lay(a.H, a.I, a.T, W<WT>::kBytes, WT == FT_W_F32 ? 4 : 2, a.max_unique, a.T * a.k);
+  if (!lay.ok() || lay.total > kFusedSmemBudget + 1024 || !a.gbar || a.T > kMaxRows) return cudaErrorNotSupported;
+  // One row shape per weight type has an instantiation (16-byte chunks per
+  // lane of a Wg/Wu row, of a Wd row): fp32 H 256 / I 128 (1 KB, 512 B),
+  // bf16 H 2048 / I 512 (4 KB, 1 KB), fp8 H 4096 / I 2048 (4 KB, 2 KB).
+  // Other shapes take the two-kernel path.
+  constexpr int NCL = WT == FT_W_F32 ? 2 : 8;
+  constexpr int DCL = WT == FT_W_F32 ? 1 : (WT == FT_W_BF16 ? 2 : 4);
+  const int nch = a.H * W<WT>::kBytes / 16, dch = a.I * W<WT>::kBytes / 16;
+  if (nch > 32 * NCL || nch <= 32 * NCL - 64 || dch != 32 * DCL) return cudaErrorNotSupported;
+  return a.T == 1 ? fused_launch<WT, 1, NCL, DCL>(a, lay, grid, s) : fused_launch<WT, kMaxRows, NCL, DCL>(a, lay, grid, s);
 }
 
 }  // namespace
+
+cudaError_t launch_signal_done(const FfnArgs& a, cudaStream_t s) {
+  signal_done_kernel<<<1, 1, 0, s>>>(a.hdr, a.done_host);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_decode_ffn_fused(const FfnArgs& a, cudaStream_t s) {
   switch (a.wdtype) {

@@ -56,6 +56,11 @@ __global__ void __launch_bounds__(kThreads) pull_misses_kernel(PullArgs a) {
 
 }  // namespace
 
+cudaError_t prefer_max_shared_fetch() {
+  return cudaFuncSetAttribute(pull_misses_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
+
 cudaError_t launch_pull_misses(const PullArgs& a, int ctas, cudaStream_t s) {
   pull_misses_kernel<<<ctas, kThreads, 0, s>>>(a);
   return cudaGetLastError();

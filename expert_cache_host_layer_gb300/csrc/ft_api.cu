@@ -154,6 +154,8 @@ struct ft_cache {
   RingEntry* ring_dev = nullptr;
   int32_t* ready_flags = nullptr;     // device [kRing], set on the copy stream after an event's copies
   int32_t* flag_src = nullptr;        // pinned host [kRing], sources of those 4-byte copies
+  int32_t* done_host = nullptr;       // mapped pinned [kRing]: done_host[e % kRing] = e once FFN(e) is done
+  int32_t* done_dev = nullptr;        // its device address
   int32_t* counter_host = nullptr;    // pinned host word for reading the device event counter
   float* h_buf = nullptr;             // decode intermediate [max_rows][I]
   unsigned* gbar = nullptr;           // grid-barrier words of the fused FFN kernel
@@ -162,6 +164,20 @@ struct ft_cache {
   cudaStream_t compute = nullptr;
   cudaStream_t route = nullptr;        // route_classify kernels (off the FFN's critical path)
   cudaEvent_t route_join = nullptr;    // compute -> route ordering at each ft_route_classify
+  cudaEvent_t slots_free = nullptr;    // compute -> copy ordering when routing runs ahead
+  // copy-engine mode: end of each of the last two step-graph launches; a third
+  // launch first waits (polling) for the oldest, so the host never queues so
+  // much work that a launch call blocks while an FFN waits for the copy thread
+  cudaEvent_t inflight[2] = {nullptr, nullptr};
+  long long graph_launches = 0;
+  // true: routing waits for all compute-stream work (the API's rule); false
+  // inside an SM-pull step graph, where every layer's logits are ready at the
+  // step's start and only the miss fetch has to wait for the FFN of event t-2
+  bool route_follows_compute = true;
+  // SM-pull mode: the layer whose fetch was requested but not yet enqueued.
+  // The next ft_moe_forward of another layer runs it inside its fused kernel;
+  // anything else that needs it first launches it on its own (flush_fetch).
+  int pending_fetch = -1;
   cudaStream_t copy[2] = {nullptr, nullptr};
   int ncopy = 1;
   cudaEvent_t copy_join = nullptr;
@@ -181,7 +197,7 @@ struct ft_cache {
   // counters
   std::atomic<long long> launches{0}, memcpys{0};
   // timing
-  bool timing = false;
+  std::atomic<bool> timing{false};   // read by the copy thread
   PhaseTimer timers[PHASE_COUNT];
   // step-graph capture: while set, ft_route_classify / ft_moe_forward record
   // external event nodes around their kernels into these arrays
@@ -194,12 +210,14 @@ struct ft_cache {
 namespace {
 
 // Copy-engine thread.  Polls the stamp of ring entry e % kRing until it
-// reads e (the route kernel writes every field first), copies the event's
-// misses from the host bank into their victim slots on the copy stream(s),
-// then copies e into ready_flags[e % kRing] after them.  A ring entry is not
-// overwritten before it is read: event e + kRing can only be routed after the
-// FFN of event e + kRing - 2 ran, which waited for this thread's flag of that
-// event.
+// reads e (the route kernel writes every field first) and done_host until the
+// FFN of event e - 2 has finished (its slots may be this event's victims),
+// copies the event's misses from the host bank into their victim slots on the
+// copy stream(s), then copies e into ready_flags[e % kRing] after them.  A
+// ring entry is not overwritten before it is read: event e + kRing can only be
+// routed after the FFN of event e + kRing - L - 1 or later ran (routing runs
+// at most one step of L <= kRing - 2 layers ahead), which waited for this
+// thread's flag of that event.
 void helper_loop(ft_cache* c) {
   cudaSetDevice(c->device);
   long long e = 0;
@@ -207,8 +225,24 @@ void helper_loop(ft_cache* c) {
   while (!c->stop.load(std::memory_order_relaxed)) {
     RingEntry* r = c->ring_host + (e % kRing);
     const int stamp = __atomic_load_n(&r->event, __ATOMIC_ACQUIRE);
+    if (stamp > (int)e) {
+      // Overrun: the entry was rewritten by a later event, which can only
+      // happen after FFNs gave up waiting for this thread (their wait is
+      // bounded).  Those events' copies are lost; report it and resume at the
+      // oldest event still in the ring.
+      int zero = 0;
+      c->copy_status.compare_exchange_strong(zero, (int)FT_ERR_TIMEOUT);
+      e = stamp - kRing + 1 > e ? stamp - kRing + 1 : e + 1;
+      c->copied_events.store(e, std::memory_order_release);
+      continue;
+    }
     if (stamp != (int)e) {
-      if (++idle > 2000) std::this_thread::sleep_for(std::chrono::microseconds(20));
+      if (++idle > 20000) std::this_thread::sleep_for(std::chrono::microseconds(5));
+      continue;
+    }
+    // the victims of event e may be slots that the FFN of event e - 2 reads
+    if (e >= 2 && __atomic_load_n(&c->done_host[(e - 2) % kRing], __ATOMIC_ACQUIRE) != (int)(e - 2)) {
+      if (++idle > 20000) std::this_thread::sleep_for(std::chrono::microseconds(5));
       continue;
     }
     idle = 0;
@@ -270,15 +304,55 @@ cudaError_t wait_event(cudaEvent_t ev) {
   }
 }
 
+// SM pull on its own: a pull kernel on the copy stream after the layer's
+// routing (and, when routing runs ahead, after the FFNs enqueued so far).
+ft_status launch_pull(ft_cache* c, int layer) {
+  CU(cudaStreamWaitEvent(c->copy[0], c->cls_ev[layer], 0));
+  if (!c->route_follows_compute) {  // the victims' old contents may still be read by an enqueued FFN
+    CU(cudaEventRecord(c->slots_free, c->compute));
+    CU(cudaStreamWaitEvent(c->copy[0], c->slots_free, 0));
+  }
+  PullArgs p{};
+  const Plan& pl = c->plans[layer];
+  p.hdr = pl.hdr; p.miss_expert = pl.miss_expert; p.miss_slot = pl.miss_slot;
+  p.layer = layer; p.E = c->E; p.bank_blobs = c->cfg.bank_blobs; p.bank = c->bank_dev;
+  p.pool = c->pool; p.expert_bytes = (long long)c->eb;
+  const int ctas = c->cfg.pull_ctas > 0 ? c->cfg.pull_ctas : 64;
+  if (c->timing) c->timers[PHASE_FETCH].begin(c->copy[0]);
+  if (c->cap_fetch_ev) CU(cudaEventRecordWithFlags(c->cap_fetch_ev[2 * layer], c->copy[0], cudaEventRecordExternal));
+  CU(launch_pull_misses(p, ctas, c->copy[0]));
+  if (c->cap_fetch_ev) CU(cudaEventRecordWithFlags(c->cap_fetch_ev[2 * layer + 1], c->copy[0], cudaEventRecordExternal));
+  if (c->timing) c->timers[PHASE_FETCH].end(c->copy[0]);
+  ++c->launches;
+  CU(cudaEventRecord(c->ready_ev[layer], c->copy[0]));
+  return FT_OK;
+}
+
+ft_status flush_fetch(ft_cache* c) {
+  if (c->pending_fetch < 0) return FT_OK;
+  const int l = c->pending_fetch;
+  c->pending_fetch = -1;
+  return launch_pull(c, l);
+}
+
 ft_status sync_all(ft_cache* c) {
+  if (c->pending_fetch >= 0) {  // a requested fetch is part of the work to finish
+    const ft_status st = flush_fetch(c);
+    if (st != FT_OK) return st;
+  }
   CU(wait_stream(c->compute));  // FFNs (and graph replays) done
   CU(wait_stream(c->route));
   if (c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE) {  // every routed event's copies must be enqueued
     CU(cudaMemcpyAsync(c->counter_host, c->tab.event_ctr, sizeof(int32_t), cudaMemcpyDeviceToHost, c->route));
     CU(wait_stream(c->route));
     const int routed = *c->counter_host;
-    while (c->copied_events.load(std::memory_order_acquire) < routed)
+    const auto t0 = std::chrono::steady_clock::now();
+    while (c->copied_events.load(std::memory_order_acquire) < routed) {
+      if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(10))
+        return fail(FT_ERR_TIMEOUT, "copy thread did not reach event %d (at %lld) within 10 s", routed,
+                    (long long)c->copied_events.load());
       std::this_thread::sleep_for(std::chrono::microseconds(10));
+    }
   }
   for (int i = 0; i < c->ncopy; ++i) CU(wait_stream(c->copy[i]));
   CU(wait_stream(c->compute));
@@ -373,6 +447,9 @@ ft_status ft_cache_destroy(ft_cache* c) {
   if (c->capture_stream) cudaStreamDestroy(c->capture_stream);
   if (c->route) cudaStreamDestroy(c->route);
   if (c->route_join) cudaEventDestroy(c->route_join);
+  if (c->slots_free) cudaEventDestroy(c->slots_free);
+  for (auto& ev : c->inflight)
+    if (ev) cudaEventDestroy(ev);
   free_tables(c->tab, true);
   cudaFree(c->plan_mem);
   cudaFree(c->scr_mem);
@@ -380,6 +457,7 @@ ft_status ft_cache_destroy(ft_cache* c) {
   cudaFree(c->gbar);
   if (c->ring_host) cudaFreeHost(c->ring_host);
   if (c->flag_src) cudaFreeHost(c->flag_src);
+  if (c->done_host) cudaFreeHost(c->done_host);
   if (c->counter_host) cudaFreeHost(c->counter_host);
   cudaFree(c->ready_flags);
   if (c->registered_bank) cudaHostUnregister(const_cast<uint8_t*>(c->bank_host));
@@ -480,14 +558,17 @@ ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t n
     // decode intermediate
     const long long drows = (long long)std::min(g.max_tokens, kDecodeMaxTokens) * g.top_k;
     CU(cudaMalloc(&c->h_buf, sizeof(float) * drows * c->I));
-    CU(cudaMalloc(&c->gbar, 2 * sizeof(unsigned)));
-    CU(cudaMemset(c->gbar, 0, 2 * sizeof(unsigned)));
+    CU(cudaMalloc(&c->gbar, 3 * sizeof(unsigned)));
+    CU(cudaMemset(c->gbar, 0, 3 * sizeof(unsigned)));
     if (g.fetch_mode == FT_FETCH_COPY_ENGINE) {  // event ring (mapped host) and ready flags (device)
       CU(cudaHostAlloc(reinterpret_cast<void**>(&c->ring_host), sizeof(RingEntry) * kRing, cudaHostAllocMapped));
       memset(c->ring_host, 0, sizeof(RingEntry) * kRing);
       for (int i = 0; i < kRing; ++i) c->ring_host[i].event = -1;
       CU(cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->ring_dev), c->ring_host, 0));
       CU(cudaHostAlloc(reinterpret_cast<void**>(&c->flag_src), sizeof(int32_t) * kRing, cudaHostAllocDefault));
+      CU(cudaHostAlloc(reinterpret_cast<void**>(&c->done_host), sizeof(int32_t) * kRing, cudaHostAllocMapped));
+      for (int i = 0; i < kRing; ++i) c->done_host[i] = -1;
+      CU(cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->done_dev), c->done_host, 0));
       CU(cudaHostAlloc(reinterpret_cast<void**>(&c->counter_host), sizeof(int32_t), cudaHostAllocDefault));
       CU(cudaMalloc(&c->ready_flags, sizeof(int32_t) * kRing));
       CU(cudaMemset(c->ready_flags, 0xff, sizeof(int32_t) * kRing));  // -1: no event yet
@@ -495,7 +576,11 @@ ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t n
     // streams and events
     for (int i = 0; i < c->ncopy; ++i) CU(cudaStreamCreateWithFlags(&c->copy[i], cudaStreamNonBlocking));
     CU(cudaStreamCreateWithFlags(&c->route, cudaStreamNonBlocking));
+    CU(prefer_max_shared_route());
+    CU(prefer_max_shared_fetch());
     CU(cudaEventCreateWithFlags(&c->route_join, cudaEventDisableTiming));
+    CU(cudaEventCreateWithFlags(&c->slots_free, cudaEventDisableTiming));
+    for (auto& ev : c->inflight) CU(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
     CU(cudaEventCreateWithFlags(&c->copy_join, cudaEventDisableTiming));
     c->cls_ev.assign(c->L, nullptr);
     c->ready_ev.assign(c->L, nullptr);
@@ -549,8 +634,10 @@ ft_status ft_route_classify(ft_cache* c, int32_t layer, const float* logits, int
   // The route stream starts after everything the caller has enqueued on the
   // compute stream so far: the logits, and in the double-buffered schedule the
   // FFN of event t-2 (whose slots this event may evict).
-  CU(cudaEventRecord(c->route_join, c->compute));
-  CU(cudaStreamWaitEvent(c->route, c->route_join, 0));
+  if (c->route_follows_compute) {
+    CU(cudaEventRecord(c->route_join, c->compute));
+    CU(cudaStreamWaitEvent(c->route, c->route_join, 0));
+  }
   if (c->timing) c->timers[PHASE_ROUTE].begin(c->route);
   if (c->cap_route_ev) CU(cudaEventRecordWithFlags(c->cap_route_ev[2 * layer], c->route, cudaEventRecordExternal));
   CU(launch_route_classify(a, c->route));
@@ -564,6 +651,7 @@ ft_status ft_route_classify(ft_cache* c, int32_t layer, const float* logits, int
   return FT_OK;
 }
 
+
 ft_status ft_fetch_misses(ft_cache* c, int32_t layer) {
   if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
   if (layer < 0 || layer >= c->L) return fail(FT_ERR_INVALID_ARG, "layer %d out of range", layer);
@@ -572,20 +660,11 @@ ft_status ft_fetch_misses(ft_cache* c, int32_t layer) {
   if (c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE) {
     // nothing to enqueue: the copy thread picks the event up from the ring
   } else {
-    CU(cudaStreamWaitEvent(c->copy[0], c->cls_ev[layer], 0));
-    PullArgs p{};
-    const Plan& pl = c->plans[layer];
-    p.hdr = pl.hdr; p.miss_expert = pl.miss_expert; p.miss_slot = pl.miss_slot;
-    p.layer = layer; p.E = c->E; p.bank_blobs = c->cfg.bank_blobs; p.bank = c->bank_dev;
-    p.pool = c->pool; p.expert_bytes = (long long)c->eb;
-    const int ctas = c->cfg.pull_ctas > 0 ? c->cfg.pull_ctas : 64;
-    if (c->timing) c->timers[PHASE_FETCH].begin(c->copy[0]);
-    if (c->cap_fetch_ev) CU(cudaEventRecordWithFlags(c->cap_fetch_ev[2 * layer], c->copy[0], cudaEventRecordExternal));
-    CU(launch_pull_misses(p, ctas, c->copy[0]));
-    if (c->cap_fetch_ev) CU(cudaEventRecordWithFlags(c->cap_fetch_ev[2 * layer + 1], c->copy[0], cudaEventRecordExternal));
-    if (c->timing) c->timers[PHASE_FETCH].end(c->copy[0]);
-    ++c->launches;
-    CU(cudaEventRecord(c->ready_ev[layer], c->copy[0]));
+    // deferred: the next forward of another layer copies these misses inside
+    // its kernel; at most one fetch waits
+    ft_status st = flush_fetch(c);
+    if (st != FT_OK) return st;
+    c->pending_fetch = layer;
   }
   c->fetch_event[layer] = ev;
   return FT_OK;
@@ -604,10 +683,23 @@ ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, v
     // for inside the kernel (ready flag set after the copies)
     CU(cudaStreamWaitEvent(c->compute, c->cls_ev[layer], 0));
   } else {
+    if (c->pending_fetch == layer || T == 0 || T > kDecodeMaxTokens || !c->fused_ok) {
+      ft_status st = flush_fetch(c);  // this layer's own fetch, or no fused kernel to carry it
+      if (st != FT_OK) return st;
+    }
     CU(cudaStreamWaitEvent(c->compute, c->ready_ev[layer], 0));
   }
   c->forward_event[layer] = ev;
-  if (T == 0) return FT_OK;
+  if (T == 0) {
+    if (c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE) {  // no FFN kernel: the copy thread still needs the signal
+      FfnArgs f0{};
+      f0.hdr = c->plans[layer].hdr;
+      f0.done_host = c->done_dev;
+      CU(launch_signal_done(f0, c->compute));
+      ++c->launches;
+    }
+    return FT_OK;
+  }
   if (T > kDecodeMaxTokens) return fail(FT_ERR_UNSUPPORTED, "T=%d > %d needs the grouped GEMM path", T, kDecodeMaxTokens);
   const Plan& pl = c->plans[layer];
   FfnArgs f{};
@@ -618,14 +710,30 @@ ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, v
   f.status = c->tab.status;
   f.gbar = c->gbar;
   f.ready_flags = c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE ? c->ready_flags : nullptr;
+  f.done_host = c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE ? c->done_dev : nullptr;
   // the two kernels are timed as one unit: an event between them would cut
   // the programmatic dependency that lets the down kernel start early
   const bool tm = c->timing;
+  const int nx = c->pending_fetch;  // fetched inside this FFN's kernel, if it launches
+  if (nx >= 0) {
+    CU(cudaStreamWaitEvent(c->compute, c->cls_ev[nx], 0));  // its miss list
+    const Plan& pn = c->plans[nx];
+    f.nx.hdr = pn.hdr; f.nx.miss_expert = pn.miss_expert; f.nx.miss_slot = pn.miss_slot;
+    f.nx.layer = nx; f.nx.E = c->E; f.nx.bank_blobs = c->cfg.bank_blobs; f.nx.bank = c->bank_dev;
+    f.nx.pool = c->pool; f.nx.expert_bytes = (long long)c->eb;
+    if (c->cap_fetch_ev) CU(cudaEventRecordWithFlags(c->cap_fetch_ev[2 * nx], c->compute, cudaEventRecordExternal));
+  }
   if (tm) c->timers[PHASE_FFN].begin(c->compute);
   if (c->cap_ffn_ev) CU(cudaEventRecordWithFlags(c->cap_ffn_ev[2 * layer], c->compute, cudaEventRecordExternal));
   cudaError_t e = c->fused_ok ? launch_decode_ffn_fused(f, c->compute) : cudaErrorNotSupported;
   if (e == cudaSuccess) {
     ++c->launches;
+    if (nx >= 0) {
+      c->pending_fetch = -1;
+      if (c->cap_fetch_ev)
+        CU(cudaEventRecordWithFlags(c->cap_fetch_ev[2 * nx + 1], c->compute, cudaEventRecordExternal));
+      CU(cudaEventRecord(c->ready_ev[nx], c->compute));
+    }
   } else {
     if (e != cudaErrorNotSupported) {
       cudaGetLastError();  // clear a launch-configuration error, then take the two-kernel path from now on
@@ -637,9 +745,15 @@ ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, v
     e = launch_decode_down(f, c->compute);
     if (e != cudaSuccess) return fail(FT_ERR_CUDA, "down launch: %s", cudaGetErrorString(e));
     ++c->launches;
+    if (f.done_host) {
+      e = launch_signal_done(f, c->compute);
+      if (e != cudaSuccess) return fail(FT_ERR_CUDA, "done-signal launch: %s", cudaGetErrorString(e));
+      ++c->launches;
+    }
   }
   if (c->cap_ffn_ev) CU(cudaEventRecordWithFlags(c->cap_ffn_ev[2 * layer + 1], c->compute, cudaEventRecordExternal));
   if (tm) c->timers[PHASE_FFN].end(c->compute);
+  if (nx >= 0 && c->pending_fetch == nx) return flush_fetch(c);  // the two-kernel path did not carry it
   return FT_OK;
 }
 
@@ -818,6 +932,7 @@ struct ft_step_graph {
   long long kernels = 0;  // kernels per launch
   std::vector<cudaEvent_t> ev;  // [0,2L) route, [2L,4L) ffn, [4L,6L) fetch begin/end; then step begin/end
   bool timing = false;
+  bool fetch_events = false;  // false in copy-engine mode: the copy thread's copies are not graph nodes
   bool launched = false;
 };
 
@@ -868,10 +983,12 @@ ft_status ft_step_graph_create(ft_cache* c, const float* const* logits, const vo
     c->cap_route_ev = g->ev.data();
     c->cap_ffn_ev = g->ev.data() + 2 * c->L;
     c->cap_fetch_ev = g->ev.data() + 4 * c->L;
+    g->fetch_events = c->cfg.fetch_mode == FT_FETCH_SM_PULL;
   }
   auto restore = [&]() {
     c->compute = saved_compute;
     c->timing = saved_timing;
+    c->route_follows_compute = true;
     c->cap_route_ev = nullptr;
     c->cap_ffn_ev = nullptr;
     c->cap_fetch_ev = nullptr;
@@ -883,23 +1000,33 @@ ft_status ft_step_graph_create(ft_cache* c, const float* const* logits, const vo
     return fail(FT_ERR_CUDA, "cudaStreamBeginCapture: %s", cudaGetErrorString(e));
   }
   if (g->timing) cudaEventRecordWithFlags(g->ev[6 * c->L], c->capture_stream, cudaEventRecordExternal);
+  if (c->cfg.fetch_mode == FT_FETCH_SM_PULL || c->L + 2 <= kRing) {
+    // Routing runs ahead on the route stream from the step's start (the
+    // logits are inputs of the graph).  Each pull kernel waits for its routing
+    // and for the FFN enqueued before it; in copy-engine mode the copy thread
+    // waits for the FFN of event t - 2 before it copies event t's misses.
+    e = cudaEventRecord(c->route_join, c->compute);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c->route, c->route_join, 0);
+    c->route_follows_compute = false;
+  }
   auto route = [&](int l) -> ft_status {
     ft_status s1 = ft_route_classify(c, l, logits[l], T, nullptr, nullptr);
     return s1 != FT_OK ? s1 : ft_fetch_misses(c, l);
   };
-  st = FT_OK;
-  if (double_buffer) {
+  st = e == cudaSuccess ? FT_OK : fail(FT_ERR_CUDA, "route stream join: %s", cudaGetErrorString(e));
+  if (st == FT_OK && double_buffer) {
     st = route(0);
     for (int l = 0; l < c->L && st == FT_OK; ++l) {
       if (l + 1 < c->L) st = route(l + 1);
       if (st == FT_OK) st = ft_moe_forward(c, l, x[l], T, y[l]);
     }
-  } else {
+  } else if (st == FT_OK) {
     for (int l = 0; l < c->L && st == FT_OK; ++l) {
       st = route(l);
       if (st == FT_OK) st = ft_moe_forward(c, l, x[l], T, y[l]);
     }
   }
+  if (st == FT_OK && c->pending_fetch >= 0) st = flush_fetch(c);  // inside the capture
   if (g->timing) cudaEventRecordWithFlags(g->ev[6 * c->L + 1], c->capture_stream, cudaEventRecordExternal);
   const std::string msg = g_last_error;
   e = cudaStreamEndCapture(c->capture_stream, &g->graph);
@@ -923,7 +1050,13 @@ ft_status ft_step_graph_create(ft_cache* c, const float* const* logits, const vo
 
 ft_status ft_step_graph_launch(ft_step_graph* g) {
   if (!g || !g->exec) return fail(FT_ERR_INVALID_ARG, "null step graph");
-  CU(cudaGraphLaunch(g->exec, g->c->compute));
+  ft_cache* c = g->c;
+  const bool ce = c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE;
+  cudaEvent_t done = c->inflight[c->graph_launches % 2];
+  if (ce && c->graph_launches >= 2) CU(wait_event(done));
+  CU(cudaGraphLaunch(g->exec, c->compute));
+  if (ce) CU(cudaEventRecord(done, c->compute));
+  ++c->graph_launches;
   g->c->launches += g->kernels;
   g->launched = true;
   return FT_OK;
@@ -939,6 +1072,10 @@ ft_status ft_step_graph_trace(ft_step_graph* g, double* t_ms) {
     for (int j = 0; j < 6; ++j) {  // route begin/end, fetch begin/end, ffn begin/end
       static const int base[3] = {0, 4, 2};  // event arrays: route [0, 2L), ffn [2L, 4L), fetch [4L, 6L)
       const int idx = base[j / 2] * L + 2 * l + (j & 1);
+      if (j / 2 == 1 && !g->fetch_events) {
+        t_ms[6 * l + j] = -1.0;
+        continue;
+      }
       CU(cudaEventElapsedTime(&ms, g->ev[6 * L], g->ev[idx]));
       t_ms[6 * l + j] = ms;
     }
@@ -962,7 +1099,8 @@ ft_status ft_step_graph_timing(ft_step_graph* g, double* route_ms, double* fetch
       ffn_ms[l] = ms;
     }
     if (fetch_ms) {
-      CU(cudaEventElapsedTime(&ms, g->ev[4 * L + 2 * l], g->ev[4 * L + 2 * l + 1]));
+      ms = 0.0f;
+      if (g->fetch_events) CU(cudaEventElapsedTime(&ms, g->ev[4 * L + 2 * l], g->ev[4 * L + 2 * l + 1]));
       fetch_ms[l] = ms;
     }
   }

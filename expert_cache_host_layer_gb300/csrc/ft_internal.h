@@ -60,10 +60,13 @@ struct RouteScratch {
 
 // Copy-engine mode: each route_classify appends its miss list to a ring in
 // mapped pinned host memory; it fills the fields, then stamps `event` last.
-// A library host thread polls the ring, issues the blob copies, then sets
+// A library host thread polls the ring; once the FFN of event - 2 has
+// finished (the FFN's last CTA writes its event to done_host[e % kRing], also
+// mapped pinned memory) it issues the blob copies, then sets
 // ready_flags[event % kRing] = event on the copy stream after them; the FFN
-// kernels wait for that flag.
-constexpr int kRing = 16;
+// kernels wait for that flag.  kRing bounds how far routing may run ahead of
+// the copies (a step graph routes at most one step of L layers ahead).
+constexpr int kRing = 128;
 struct RingEntry {
   int32_t event;  // stamp: the event number once the entry is complete
   int32_t layer;
@@ -90,6 +93,12 @@ struct RouteArgs {
 ft_status set_error(ft_status s, const char* fmt, ...);
 
 cudaError_t launch_route_classify(const RouteArgs& a, cudaStream_t s);
+// An SM changes its L1/shared-memory split only when it is empty, so kernels
+// that run side by side (route, miss pull, FFN) all ask for the largest
+// shared-memory split; otherwise a small-split kernel keeps the FFN's CTAs
+// (about 150 KB each) off its SMs until it drains.  Called at cache creation.
+cudaError_t prefer_max_shared_route();
+cudaError_t prefer_max_shared_fetch();
 cudaError_t launch_init_tables(Tables tab, int num_keys, cudaStream_t s);
 
 struct PullArgs {
@@ -118,9 +127,16 @@ struct FfnArgs {
   int max_unique;  // upper bound of the plan's n_unique (min(T*k, E)), sizes the grid
   float* h;        // [T*k][I] intermediate
   int32_t* status; // sticky status word (bounded waits record FT_ERR_TIMEOUT)
-  unsigned* gbar;  // [2] grid-barrier count and generation of the fused kernel (zeroed once)
+  unsigned* gbar;  // [3] grid-barrier count and generation, finished-CTA count of the fused kernel (zeroed once)
   const int32_t* ready_flags;  // copy-engine mode: wait for ready_flags[e % kRing] == e (e = plan event); or null
+  int32_t* done_host;          // copy-engine mode: device address of the mapped [kRing] words where the
+                               // FFN stores e at done_host[e % kRing] once it no longer reads its slots; or null
+  PullArgs nx;                 // SM-pull mode: the next event's miss fetch, done by the fused kernel's copy
+                               // warps while it computes (nx.hdr null: none)
 };
+// Copy-engine mode, two-kernel path or T == 0: one thread stores the plan's
+// event into done_host after the work before it on the stream.
+cudaError_t launch_signal_done(const FfnArgs& a, cudaStream_t s);
 // Decode path: the gate/up+SwiGLU kernel, then the down+combine kernel.
 cudaError_t launch_decode_gateup(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_decode_down(const FfnArgs& a, cudaStream_t s);

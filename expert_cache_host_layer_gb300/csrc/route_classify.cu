@@ -423,6 +423,21 @@ __global__ void init_tables_kernel(Tables tab, int num_keys) {
 
 }  // namespace
 
+cudaError_t prefer_max_shared_route() {
+  const void* fns[] = {reinterpret_cast<const void*>(route_classify_kernel<1>),
+                       reinterpret_cast<const void*>(route_classify_kernel<2>),
+                       reinterpret_cast<const void*>(route_classify_kernel<4>),
+                       reinterpret_cast<const void*>(route_classify_kernel<8>),
+                       reinterpret_cast<const void*>(route_classify_kernel<16>),
+                       reinterpret_cast<const void*>(route_classify_kernel<32>)};
+  for (const void* f : fns) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                               cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_route_classify(const RouteArgs& a, cudaStream_t s) {
   const int warps_needed = (a.T + kWarps - 1) / kWarps;
   int grid = warps_needed < 1 ? 1 : warps_needed;

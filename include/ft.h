@@ -296,10 +296,19 @@ ft_status ft_moe_decode_ffn_static(int32_t hidden, int32_t inter, int32_t wdtype
  * modes (in copy-engine mode the library's copy thread serves the replays'
  * events from the ring as they are routed).  Needs no layer with a fetched,
  * not yet forwarded plan (FT_ERR_STATE).  Create is synchronous; launch
- * enqueues the step on the cache's compute stream.  With `timing` set the
+ * enqueues the step on the cache's compute stream.  In copy-engine mode a
+ * launch first waits (polling, no blocking runtime call) for the end of the
+ * launch two before it, so at most two steps are queued: the FFNs wait for
+ * the library's copy thread, which must never be stuck behind a host thread
+ * blocked in a full launch queue.  In SM-pull mode the routing of every layer
+ * runs ahead of the FFNs from the step's start (the logits are graph inputs)
+ * and each layer's pull kernel waits for the FFN of two events before.  With `timing` set the
  * graph records events around each layer's route kernel, miss fetch and FFN
  * kernels; ft_step_graph_timing waits for the last launch and returns them
- * (ms; any pointer may be NULL; arrays hold L entries).
+ * (ms; any pointer may be NULL; arrays hold L entries).  In copy-engine mode
+ * the misses are copied by the library's copy thread outside the graph, so
+ * the graph has no fetch events: fetch_ms is 0 there (ft_timing_enable /
+ * ft_get_timing time those copies instead).
  */
 ft_status ft_step_graph_create(ft_cache* cache, const float* const* logits, const void* const* x, float* const* y,
                                int32_t T, int32_t double_buffer, int32_t timing, ft_step_graph** out);
@@ -308,7 +317,8 @@ ft_status ft_step_graph_timing(ft_step_graph* graph, double* route_ms, double* f
                                double* step_ms);
 /* Timeline of the graph's last launch (waits for it): t_ms[6*l + j] = time
  * from the step's start to the route begin/end (j = 0, 1), fetch begin/end
- * (2, 3) and FFN begin/end (4, 5) of layer l.  Needs a timing graph. */
+ * (2, 3) and FFN begin/end (4, 5) of layer l.  Needs a timing graph.  The
+ * fetch entries are -1 in copy-engine mode (no fetch events in the graph). */
 ft_status ft_step_graph_trace(ft_step_graph* graph, double* t_ms);
 ft_status ft_step_graph_destroy(ft_step_graph* graph);
 

@@ -217,6 +217,7 @@ def run_parity_graph(w: W.Workload, steps: int, bank_blobs: int | None = None, d
             assert np.array_equal(k2s, rk2s) and np.array_equal(sk, rsk) and np.array_equal(ts, rts), f"step {s}"
             if timing:
                 report["trace"] = graph.trace()
+                report["timing"] = graph.timing()
     finally:
         graph.close()
         cache.close()
