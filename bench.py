@@ -48,6 +48,7 @@ def parse():
     p.add_argument("--fetch-mode", type=int, default=1, help="0 copy engine, 1 SM pull")
     p.add_argument("--pull-ctas", type=int, default=0)
     p.add_argument("--copy-streams", type=int, default=1)
+    p.add_argument("--fetch-warps", type=int, default=0, help="SM pull: FFN warps per SM copying the next misses")
     p.add_argument("--serial", action="store_true", help="double buffering off")
     p.add_argument("--bank-blobs", type=int, default=0, help="0 = full bank; fewer = aliased bank")
     p.add_argument("--slots", type=int, default=0, help="override the cache size")
@@ -235,6 +236,60 @@ def run_reference(args, w):
 
 # --------------------------------------------------------------------- our arm
 
+# dram__bytes_read.sum + dram__bytes_write.sum of one ffn_fused_kernel launch
+# (35B-shaped bf16 decode layer, 8 unique experts), mean of the two launches
+# of the ncu --set full capture summarised under profiles/.  It belongs to the
+# kernel as captured: set it to None whenever that kernel changes.
+FFN_TRAFFIC_PER_LAUNCH = {}
+
+
+def ffn_only(w, dev, peak):
+    """The fused FFN kernel alone, through the public API: a one-layer cache of
+    16*k slots whose routing rotates through 16 disjoint sets of k experts, so
+    after 16 warm-up events every event hits (no fetch rides along) and each
+    FFN streams k experts that the previous 15 events did not touch (16*k
+    experts > L2).  Times the kernel with the step graph's event nodes."""
+    import torch
+
+    from expert_cache_host_layer_gb300.pipeline import ExpertCache, StepGraph, pinned_bank
+    k, E = w.top_k, w.num_experts
+    nsets = 16
+    n_blobs = nsets * k
+    if n_blobs > E:
+        return None
+    bank = pinned_bank(n_blobs * w.expert_bytes)
+    synth.expert_blobs(w.seed, w.hidden, w.inter, w.wdtype, np.arange(n_blobs), out_ptr=bank.data_ptr())
+    act = torch.float32 if w.wdtype == synth.W_F32 else torch.bfloat16
+    c = ExpertCache(1, E, k, w.hidden, w.inter, w.wdtype, n_blobs, 1, bank, n_blobs, fetch_mode=1, device=dev)
+    lg = torch.full((1, E), -1.0, dtype=torch.float32, device=dev)
+    x = torch.from_numpy(W.hidden_states(w, 0, 0)[:1]).to(dev, act)
+    y = torch.empty((1, w.hidden), dtype=torch.float32, device=dev)
+    g = StepGraph(c, [lg], [x], [y], True, timing=True)
+    try:
+        def launch(j):
+            lg.fill_(-1.0)
+            lg[0, (j % nsets) * k:(j % nsets + 1) * k] = torch.arange(k, 0, -1, device=dev, dtype=torch.float32)
+            g.launch()
+        for j in range(2 * nsets):  # fill the slots, then one all-hit round
+            launch(j)
+        c.synchronize()
+        st0 = c.stats()
+        ffn_ms = []
+        for j in range(64):
+            launch(j)
+            ffn_ms.append(float(g.timing()[2][0]))
+        st1 = c.stats()
+    finally:
+        g.close()
+        c.close()
+    us = 1e3 * float(np.mean(ffn_ms))
+    moved = k * w.expert_bytes
+    return {"kernel": "ffn_fused_kernel with no fetch (all hits)", "launches": len(ffn_ms), "launch_us": us,
+            "bytes_per_launch": moved, "achieved": moved / (us / 1e6) / 1e9, "peak": peak,
+            "frac": moved / (us / 1e6) / 1e9 / peak, "unit": "GB/s",
+            "misses": st1["misses"] - st0["misses"]}
+
+
 def link_ceilings(cache, w, dev, bank):
     """Host-link ceilings measured on this machine, outside the timed region:
     the copy engine (one cudaMemcpyAsync per blob, as the copy-engine fetch
@@ -261,8 +316,11 @@ def link_ceilings(cache, w, dev, bank):
     c = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, 1024, 32, bank,
                     cache.bank_blobs, fetch_mode=1, device=dev)
     best_pull = 0.0
+    spread = []  # the same over layers spread across the bank (its far pages)
     try:
-        for l in range(4):
+        for l in list(range(4)) + [9, 19, 29, 39]:
+            if l >= w.num_layers:
+                continue
             lg = torch.from_numpy(S.router_iid(7, 0, l, 32, w.num_experts)).to(dev)
             st0 = c.stats()
             c.route_classify(l, lg)
@@ -273,16 +331,20 @@ def link_ceilings(cache, w, dev, bank):
             tm = c.timing()
             st1 = c.stats()
             c.timing_enable(False)
-            if l > 0:
-                best_pull = max(best_pull, (st1["bytes_fetched"] - st0["bytes_fetched"]) / (tm["fetch_ms"] / 1e3) / 1e9)
+            gbs = (st1["bytes_fetched"] - st0["bytes_fetched"]) / (tm["fetch_ms"] / 1e3) / 1e9
+            if 0 < l < 4:
+                best_pull = max(best_pull, gbs)
+            elif l >= 4:
+                spread.append(gbs)
             c.close()
             c = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, 1024, 32, bank,
                             cache.bank_blobs, fetch_mode=1, device=dev)
     finally:
         c.close()
     return {"copy_engine_gbs": best_ce, "sm_pull_gbs": best_pull,
+            "sm_pull_spread_gbs": float(np.mean(spread)) if spread else None,
             "how": "best of a few isolated runs: 32 x one-blob cudaMemcpyAsync H2D from pinned memory; "
-                   "pull_misses_kernel on a cold cache"}
+                   "pull_misses_kernel on a cold cache (first layers' blobs; spread: layers across the bank)"}
 
 
 def run_ours(args, w):
@@ -318,7 +380,7 @@ def run_ours(args, w):
     def make_cache():
         return ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots, T, bank,
                            n_blobs, fetch_mode=args.fetch_mode, pull_ctas=args.pull_ctas,
-                           copy_streams=args.copy_streams, device=dev)
+                           copy_streams=args.copy_streams, fetch_warps=args.fetch_warps, device=dev)
 
     use_graph = True
     cache = make_cache()
@@ -434,6 +496,9 @@ def run_ours(args, w):
             link = link_ceilings(cache, w, dev, bank)
         except Exception as ex:
             link = {"error": str(ex)[:200]}
+    ffn_alone = None
+    if rank == 0 and T <= 8:
+        ffn_alone = ffn_only(w, dev, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -466,8 +531,9 @@ def run_ours(args, w):
                                    "combine), timed by event nodes around it in the timing pass",
                          "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak if achieved else None,
-                         "peak_kind": peak_kind, "traffic": None, "bytes_per_launch": ffn_bytes_per_launch,
-                         "launch_us": ffn_ms * 1e3},
+                         "peak_kind": peak_kind, "traffic": FFN_TRAFFIC_PER_LAUNCH.get(w.name),
+                         "bytes_per_launch": ffn_bytes_per_launch,
+                         "launch_us": ffn_ms * 1e3, "ffn_only": ffn_alone},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": d["kernel_launches"],

@@ -33,7 +33,7 @@ class ft_cache_config(ctypes.Structure):
                 ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("wdtype", ctypes.c_int32),
                 ("host_bank", ctypes.c_void_p), ("host_bank_bytes", ctypes.c_uint64),
                 ("bank_blobs", ctypes.c_int64), ("max_tokens", ctypes.c_int32), ("fetch_mode", ctypes.c_int32),
-                ("pull_ctas", ctypes.c_int32), ("copy_streams", ctypes.c_int32)]
+                ("pull_ctas", ctypes.c_int32), ("copy_streams", ctypes.c_int32), ("fetch_warps", ctypes.c_int32)]
 
 
 class ft_stats(ctypes.Structure):
@@ -215,9 +215,10 @@ def ft_get_timing(cache: int) -> dict:
 
 
 def make_config(num_layers, num_experts, top_k, hidden, inter, wdtype, host_bank_ptr, host_bank_bytes, bank_blobs,
-                max_tokens, fetch_mode=FT_FETCH_SM_PULL, pull_ctas=0, copy_streams=1) -> ft_cache_config:
+                max_tokens, fetch_mode=FT_FETCH_SM_PULL, pull_ctas=0, copy_streams=1,
+                fetch_warps=0) -> ft_cache_config:
     return ft_cache_config(num_layers, num_experts, top_k, hidden, inter, wdtype, host_bank_ptr, host_bank_bytes,
-                           bank_blobs, max_tokens, fetch_mode, pull_ctas, copy_streams)
+                           bank_blobs, max_tokens, fetch_mode, pull_ctas, copy_streams, fetch_warps)
 
 
 def ft_step_graph_create(cache: int, logits_ptrs, x_ptrs, y_ptrs, T: int, double_buffer: bool = True,

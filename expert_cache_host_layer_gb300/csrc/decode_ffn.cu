@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(FfnArgs a) {
 //            in shared memory before the grid barrier is passed.  The
 //            column c always belongs to warp (c - piece start) % 8, which
 //            keeps its sum over experts in registers and writes y once.
-//  copy:     in SM-pull mode two more warps copy the NEXT event's missed
+//  copy:     in SM-pull mode up to four more warps copy the NEXT event's missed
 //            blobs from the host bank into their victim slots meanwhile (8 KB
 //            items spread over all CTAs, 8 loads in flight per thread).  The
 //            victims exclude this event's slots (pin rule) and the FFN before
@@ -523,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(FfnArgs a) {
 // once, and the producer still waits (bounded) for its copies in flight
 // before it exits.
 constexpr int kFConsumers = 8;
-constexpr int kFCopyWarps = 2;  // warps kFConsumers + 1 .. : the next event's miss fetch
+constexpr int kFCopyWarps = kMaxFetchWarps;  // warps kFConsumers + 1 .. : the next event's miss fetch
 constexpr int kFThreads = (kFConsumers + 1 + kFCopyWarps) * 32;
 constexpr int kFCopyUnroll = 8;  // 16-byte loads in flight per copy thread
 constexpr int kFusedSmemBudget = 150 * 1024;
@@ -565,9 +565,10 @@ __device__ __forceinline__ uint4 ld_host16(const uint4* p) {  // streamed once: 
 }
 
 // The copy warps' work: 16-byte words of the next event's missed blobs, in
-// items of kFCopyWarps * 32 * kFCopyUnroll words, item i on CTA i % grid.
-__device__ __forceinline__ void fused_fetch(const PullArgs& p, int ct) {
-  constexpr long long kItem16 = (long long)kFCopyWarps * 32 * kFCopyUnroll;
+// items of nw * 32 * kFCopyUnroll words (nw copy warps take part), item i on
+// CTA i % grid.
+__device__ __forceinline__ void fused_fetch(const PullArgs& p, int ct, int nw) {
+  const long long kItem16 = (long long)nw * 32 * kFCopyUnroll;
   const int n_miss = __ldcg(&p.hdr[PH_MISS]);
   const long long eb16 = p.expert_bytes >> 4;
   const long long per_blob = (eb16 + kItem16 - 1) / kItem16;
@@ -586,12 +587,12 @@ __device__ __forceinline__ void fused_fetch(const PullArgs& p, int ct) {
     uint4 v[kFCopyUnroll];
 #pragma unroll
     for (int u = 0; u < kFCopyUnroll; ++u) {
-      const long long i = (long long)u * (kFCopyWarps * 32) + ct;
+      const long long i = (long long)u * (nw * 32) + ct;
       if (i < n) v[u] = ld_host16(src + i);
     }
 #pragma unroll
     for (int u = 0; u < kFCopyUnroll; ++u) {
-      const long long i = (long long)u * (kFCopyWarps * 32) + ct;
+      const long long i = (long long)u * (nw * 32) + ct;
       if (i < n) dst[i] = v[u];
     }
   }
@@ -801,7 +802,8 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(FfnArgs a) {
 
   // ---- copy warps
   if (warp > kFConsumers) {
-    if (a.nx.hdr) fused_fetch(a.nx, threadIdx.x - (kFConsumers + 1) * 32);
+    const int nw = min(max(a.fetch_warps, 1), kFCopyWarps);
+    if (a.nx.hdr && warp - (kFConsumers + 1) < nw) fused_fetch(a.nx, threadIdx.x - (kFConsumers + 1) * 32, nw);
     return;
   }
 

@@ -24,6 +24,7 @@
 #include <cstdio>
 #include <cstring>
 #include <chrono>
+#include <map>
 #include <mutex>
 #include <string>
 #include <thread>
@@ -208,6 +209,11 @@ struct ft_cache {
 };
 
 namespace {
+
+// Host banks that ft_cache_create registered, with the number of live caches
+// using each.
+std::mutex g_bank_mu;
+std::map<const void*, int> g_bank_refs;
 
 // Copy-engine thread.  Polls the stamp of ring entry e % kRing until it
 // reads e (the route kernel writes every field first) and done_host until the
@@ -460,7 +466,14 @@ ft_status ft_cache_destroy(ft_cache* c) {
   if (c->done_host) cudaFreeHost(c->done_host);
   if (c->counter_host) cudaFreeHost(c->counter_host);
   cudaFree(c->ready_flags);
-  if (c->registered_bank) cudaHostUnregister(const_cast<uint8_t*>(c->bank_host));
+  if (c->registered_bank) {
+    std::lock_guard<std::mutex> lk(g_bank_mu);
+    auto it = g_bank_refs.find(c->bank_host);
+    if (it != g_bank_refs.end() && --it->second == 0) {
+      cudaHostUnregister(const_cast<uint8_t*>(c->bank_host));
+      g_bank_refs.erase(it);
+    }
+  }
   delete c;
   return FT_OK;
 }
@@ -484,6 +497,8 @@ ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t n
   if (g.fetch_mode != FT_FETCH_COPY_ENGINE && g.fetch_mode != FT_FETCH_SM_PULL)
     return fail(FT_ERR_INVALID_ARG, "unknown fetch_mode %d", g.fetch_mode);
   if (g.copy_streams < 0 || g.copy_streams > 2) return fail(FT_ERR_INVALID_ARG, "copy_streams must be 0, 1 or 2");
+  if (g.fetch_warps < 0 || g.fetch_warps > kMaxFetchWarps)
+    return fail(FT_ERR_INVALID_ARG, "fetch_warps must be 0..%d", kMaxFetchWarps);
   if (!g.host_bank || g.bank_blobs < 1 || g.bank_blobs > (int64_t)g.num_layers * g.num_experts)
     return fail(FT_ERR_INVALID_ARG, "host_bank null or bank_blobs outside 1..L*E");
   if (g.host_bank_bytes < (uint64_t)g.bank_blobs * eb)
@@ -515,9 +530,18 @@ ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t n
     CU(cudaPointerGetAttributes(&ha, g.host_bank));
     if (ha.type == cudaMemoryTypeDevice || ha.type == cudaMemoryTypeManaged)
       return fail(FT_ERR_INVALID_ARG, "host_bank must be host memory");
-    if (ha.type != cudaMemoryTypeHost) {
-      CU(cudaHostRegister(const_cast<void*>(g.host_bank), g.host_bank_bytes, cudaHostRegisterMapped));
-      c->registered_bank = true;
+    {
+      // A bank the library registered stays registered while any cache uses it.
+      std::lock_guard<std::mutex> lk(g_bank_mu);
+      auto it = g_bank_refs.find(g.host_bank);
+      if (it != g_bank_refs.end()) {
+        ++it->second;
+        c->registered_bank = true;
+      } else if (ha.type != cudaMemoryTypeHost) {
+        CU(cudaHostRegister(const_cast<void*>(g.host_bank), g.host_bank_bytes, cudaHostRegisterMapped));
+        g_bank_refs[g.host_bank] = 1;
+        c->registered_bank = true;
+      }
     }
     void* dptr = nullptr;
     CU(cudaHostGetDevicePointer(&dptr, const_cast<void*>(g.host_bank), 0));
@@ -721,6 +745,7 @@ ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, v
     f.nx.hdr = pn.hdr; f.nx.miss_expert = pn.miss_expert; f.nx.miss_slot = pn.miss_slot;
     f.nx.layer = nx; f.nx.E = c->E; f.nx.bank_blobs = c->cfg.bank_blobs; f.nx.bank = c->bank_dev;
     f.nx.pool = c->pool; f.nx.expert_bytes = (long long)c->eb;
+    f.fetch_warps = c->cfg.fetch_warps > 0 ? c->cfg.fetch_warps : kDefaultFetchWarps;
     if (c->cap_fetch_ev) CU(cudaEventRecordWithFlags(c->cap_fetch_ev[2 * nx], c->compute, cudaEventRecordExternal));
   }
   if (tm) c->timers[PHASE_FFN].begin(c->compute);

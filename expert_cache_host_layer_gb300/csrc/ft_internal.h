@@ -11,7 +11,9 @@ namespace ft {
 
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
-constexpr int kDecodeMaxTokens = 8;  // T above this takes the grouped-GEMM path
+constexpr int kDecodeMaxTokens = 8;
+constexpr int kMaxFetchWarps = 4;      // copy warps of the fused decode FFN kernel
+constexpr int kDefaultFetchWarps = 2;  // of which take part by default  // T above this takes the grouped-GEMM path
 
 // Stats slots in the device counter array.
 enum { ST_EVENTS = 0, ST_UNIQUE, ST_HITS, ST_MISSES, ST_EVICT, ST_BYTES, ST_COUNT };
@@ -133,6 +135,7 @@ struct FfnArgs {
                                // FFN stores e at done_host[e % kRing] once it no longer reads its slots; or null
   PullArgs nx;                 // SM-pull mode: the next event's miss fetch, done by the fused kernel's copy
                                // warps while it computes (nx.hdr null: none)
+  int fetch_warps;             // how many of the kernel's copy warps take part (1..kMaxFetchWarps)
 };
 // Copy-engine mode, two-kernel path or T == 0: one thread stores the plan's
 // event into done_host after the work before it on the stream.

@@ -29,6 +29,7 @@ class ExpertCache:
 
     def __init__(self, num_layers, num_experts, top_k, hidden, inter, wdtype, num_slots, max_tokens, bank,
                  bank_blobs=None, fetch_mode=FT_FETCH_SM_PULL, pull_ctas=0, copy_streams=1, device="cuda:0",
+                 fetch_warps=0,
                  stream: torch.cuda.Stream | None = None):
         self.L, self.E, self.k, self.H, self.I = num_layers, num_experts, top_k, hidden, inter
         self.wdtype = wdtype
@@ -45,7 +46,7 @@ class ExpertCache:
         self.num_slots = num_slots
         cfg = make_config(num_layers, num_experts, top_k, hidden, inter, wdtype, bank.data_ptr(),
                           bank.numel() * bank.element_size(), self.bank_blobs, max_tokens, fetch_mode, pull_ctas,
-                          copy_streams)
+                          copy_streams, fetch_warps)
         self.handle = ft_cache_create(cfg, self.pool.data_ptr(), num_slots, self.stream.cuda_stream)
         self.copy_stream = torch.cuda.ExternalStream(ft_get_copy_stream(self.handle), device=self.device)
 
@@ -166,5 +167,8 @@ class StepGraph:
 
 
 def pinned_bank(nbytes: int) -> torch.Tensor:
-    """A pinned host byte buffer for the expert bank."""
+    """A pinned host byte buffer for the expert bank (cudaHostAlloc through
+    torch).  Measured on GB300: the GPU reads such a bank over the host link
+    several times faster than a huge-page mapping page-locked afterwards with
+    cudaHostRegister, at the bank's scattered blob offsets."""
     return torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)

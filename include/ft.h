@@ -88,7 +88,11 @@ typedef struct ft_cache_config {
   int32_t hidden;      /* H: multiple of 128 (of 8 for FT_W_F32) */
   int32_t inter;       /* I: multiple of 128 (of 8 for FT_W_F32) */
   int32_t wdtype;      /* ft_wdtype */
-  const void* host_bank;     /* host: [bank_blobs][expert_bytes]; pinned, or registered by create */
+  const void* host_bank;     /* host: [bank_blobs][expert_bytes].  Best allocated with cudaHostAlloc: on
+                                GB300 the GPU reads that several times faster over the host link than
+                                memory page-locked later.  Memory that is not pinned yet is registered
+                                (cudaHostRegister, mapped) by create and stays registered while any
+                                cache of this process uses it. */
   uint64_t host_bank_bytes;  /* >= bank_blobs * expert_bytes */
   int64_t bank_blobs;        /* physical blobs; key (l, e) reads blob (l*E + e) mod bank_blobs.
                                 L*E for a full bank; fewer aliases blobs to save host RAM */
@@ -96,6 +100,8 @@ typedef struct ft_cache_config {
   int32_t fetch_mode;        /* ft_fetch_mode */
   int32_t pull_ctas;         /* CTAs of the SM-pull fetch kernel; 0 = library default */
   int32_t copy_streams;      /* copy-engine mode: 1 or 2 streams the misses alternate over; 0 = 1 */
+  int32_t fetch_warps;       /* SM-pull mode: warps per SM of each FFN kernel that copy the next layer's
+                                misses over the host link (1..4); 0 = library default (2) */
 } ft_cache_config;
 
 typedef struct ft_cache ft_cache; /* opaque, library-owned */
