@@ -205,10 +205,21 @@ def cpu_baseline_subprocess(w: W.Workload, seconds: float):
                       f"fp64 SwiGLU FFN), {dt:.1f} s on 1 host thread"}
 
 
+def workload_config(w: W.Workload, world: int, n_blobs: int) -> dict:
+    """The `config` block both arms print for the same workload."""
+    return {"workload": w.name, "global_batch": world * w.tokens, "layers": w.num_layers,
+            "experts": w.num_experts, "top_k": w.top_k, "hidden": w.hidden, "inter": w.inter,
+            "slots": w.num_slots, "bank_blobs": n_blobs, "bank_gb": round(n_blobs * w.expert_bytes / 1e9, 2),
+            "parallelism": f"replicas{world}",
+            "l2": "inputs larger than L2 (each step reads ~2 GB of expert slots)"}
+
+
 def run_reference(args, w):
     rank, _, world = dist_setup(args.gpus)
     if rank != 0:
         return
+    if args.slots:
+        w = w.replace(num_slots=args.slots)
     # each step: the oracle over a bounded sample of steps of the same workload
     per = []
     total_steps = 0
@@ -224,8 +235,7 @@ def run_reference(args, w):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "global_batch": w.tokens, "layers": w.num_layers,
-                       "experts": w.num_experts, "top_k": w.top_k, "slots": w.num_slots},
+            "config": workload_config(w, args.gpus, args.bank_blobs or w.blobs),
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": f"{total_steps} decode steps (cold cache start) of {w.name}, "
@@ -513,12 +523,9 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.wdtype == synth.W_BF16 else
             ("f32" if w.wdtype == synth.W_F32 else "fp8e4m3"), "data": "synthetic",
-            "config": {"workload": w.name, "global_batch": world * T, "layers": L, "experts": w.num_experts,
-                       "top_k": w.top_k, "hidden": w.hidden, "inter": w.inter, "slots": w.num_slots,
-                       "bank_blobs": n_blobs, "bank_gb": round(n_blobs * eb / 1e9, 2),
-                       "fetch_mode": ["copy_engine", "sm_pull"][args.fetch_mode],
-                       "double_buffer": double, "step_graph": use_graph, "parallelism": f"replicas{world}",
-                       "l2": "inputs larger than L2 (each step reads ~2 GB of expert slots)"},
+            "config": dict(workload_config(w, world, n_blobs),
+                           fetch_mode=["copy_engine", "sm_pull"][args.fetch_mode], double_buffer=double,
+                           step_graph=use_graph),
             "miss_rate": d["misses"] / max(1, d["unique_experts"]),
             "expert_gemm_gbs": achieved,
             "miss_copy": {"gbs": fetch_gbs, "bytes_per_step": d["bytes_fetched"] / args.steps,
