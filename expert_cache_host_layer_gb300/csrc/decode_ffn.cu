@@ -1006,20 +1006,28 @@ int num_sms() {
   return n;
 }
 
-// CTAs per SM of `kernel` at `smem` bytes of dynamic shared memory; sets the
-// kernel's shared-memory limit the first time a size is seen (cached).
+// CTAs per SM of `kernel` at `smem` bytes of dynamic shared memory (cached
+// per size).  The kernel's shared-memory limit only ever grows, to the
+// largest size seen: lowering it for a smaller launch would make a later,
+// larger launch of the same kernel fail.
 template <typename K>
 int blocks_per_sm_t(K kernel, int threads, int smem, cudaError_t* err) {
   static std::mutex mu;
   static std::map<std::pair<const void*, int>, int> cache;
+  static std::map<const void*, int> limit;
   std::lock_guard<std::mutex> lk(mu);
   const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), smem * 4096 + threads);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
-  *err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (*err == cudaSuccess)  // same split as the route and fetch kernels, so they can share an SM
-    *err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-  if (*err != cudaSuccess) return 0;
+  int& lim = limit[reinterpret_cast<const void*>(kernel)];
+  if (smem > lim) {
+    *err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (*err == cudaSuccess)  // same split as the route and fetch kernels, so they can share an SM
+      *err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared);
+    if (*err != cudaSuccess) return 0;
+    lim = smem;
+  }
   int per_sm = 1;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
   if (per_sm < 0) per_sm = 0;
