@@ -159,6 +159,11 @@ struct ft_cache {
   int32_t* done_dev = nullptr;        // its device address
   int32_t* counter_host = nullptr;    // pinned host word for reading the device event counter
   float* h_buf = nullptr;             // decode intermediate [max_rows][I]
+  // prefill (T > kDecodeMaxTokens): bf16 h [rows][I], fp32 per-row outputs
+  // [rows][H], grouped place of each row; allocated only when max_tokens > 8
+  void* pf_h = nullptr;
+  float* pf_yp = nullptr;
+  int32_t* pf_pos = nullptr;
   unsigned* gbar = nullptr;           // grid-barrier words of the fused FFN kernel
   bool fused_ok = true;               // false once the fused FFN kernel reported it cannot run
   // streams and events
@@ -460,6 +465,9 @@ ft_status ft_cache_destroy(ft_cache* c) {
   cudaFree(c->plan_mem);
   cudaFree(c->scr_mem);
   cudaFree(c->h_buf);
+  cudaFree(c->pf_h);
+  cudaFree(c->pf_yp);
+  cudaFree(c->pf_pos);
   cudaFree(c->gbar);
   if (c->ring_host) cudaFreeHost(c->ring_host);
   if (c->flag_src) cudaFreeHost(c->flag_src);
@@ -582,6 +590,12 @@ ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t n
     // decode intermediate
     const long long drows = (long long)std::min(g.max_tokens, kDecodeMaxTokens) * g.top_k;
     CU(cudaMalloc(&c->h_buf, sizeof(float) * drows * c->I));
+    if (g.max_tokens > kDecodeMaxTokens && prefill_supported(c->H, c->I, c->wdtype, c->E)) {
+      const long long prows = (long long)g.max_tokens * g.top_k;
+      CU(cudaMalloc(&c->pf_h, sizeof(uint16_t) * prows * c->I));
+      CU(cudaMalloc(&c->pf_yp, sizeof(float) * prows * c->H));
+      CU(cudaMalloc(&c->pf_pos, sizeof(int32_t) * prows));
+    }
     CU(cudaMalloc(&c->gbar, 3 * sizeof(unsigned)));
     CU(cudaMemset(c->gbar, 0, 3 * sizeof(unsigned)));
     if (g.fetch_mode == FT_FETCH_COPY_ENGINE) {  // event ring (mapped host) and ready flags (device)
@@ -724,8 +738,28 @@ ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, v
     }
     return FT_OK;
   }
-  if (T > kDecodeMaxTokens) return fail(FT_ERR_UNSUPPORTED, "T=%d > %d needs the grouped GEMM path", T, kDecodeMaxTokens);
   const Plan& pl = c->plans[layer];
+  if (T > kDecodeMaxTokens) {  // prefill: grouped GEMMs
+    if (!c->pf_yp)
+      return fail(FT_ERR_UNSUPPORTED, "T=%d > %d: the prefill path needs bf16 weights (H %% 128, I %% 64)", T,
+                  kDecodeMaxTokens);
+    PrefillArgs p{};
+    p.hdr = pl.hdr; p.unique_expert = pl.unique_expert; p.unique_slot = pl.unique_slot; p.u_offset = pl.u_offset;
+    p.topk_idx = pl.topk_idx; p.topk_w = pl.topk_w; p.rows_by_u = pl.rows_by_u; p.pos = c->pf_pos;
+    p.x = x; p.h = c->pf_h; p.yp = c->pf_yp; p.y = static_cast<float*>(y);
+    p.pool = static_cast<const uint8_t*>(c->pool); p.expert_bytes = (long long)c->eb;
+    p.H = c->H; p.I = c->I; p.k = c->k; p.T = T; p.E = c->E;
+    const bool tm = c->timing;
+    if (tm) c->timers[PHASE_FFN].begin(c->compute);
+    if (c->cap_ffn_ev) CU(cudaEventRecordWithFlags(c->cap_ffn_ev[2 * layer], c->compute, cudaEventRecordExternal));
+    int n = 0;
+    const cudaError_t e = launch_prefill_ffn(p, c->compute, &n);
+    if (e != cudaSuccess) return fail(FT_ERR_CUDA, "prefill FFN launch: %s", cudaGetErrorString(e));
+    c->launches += n;
+    if (c->cap_ffn_ev) CU(cudaEventRecordWithFlags(c->cap_ffn_ev[2 * layer + 1], c->compute, cudaEventRecordExternal));
+    if (tm) c->timers[PHASE_FFN].end(c->compute);
+    return FT_OK;
+  }
   FfnArgs f{};
   f.hdr = pl.hdr; f.unique_slot = pl.unique_slot; f.u_offset = pl.u_offset; f.rows_by_u = pl.rows_by_u;
   f.topk_w = pl.topk_w; f.x = x; f.y = static_cast<float*>(y); f.pool = static_cast<const uint8_t*>(c->pool);

@@ -140,6 +140,28 @@ struct FfnArgs {
 // Copy-engine mode, two-kernel path or T == 0: one thread stores the plan's
 // event into done_host after the work before it on the stream.
 cudaError_t launch_signal_done(const FfnArgs& a, cudaStream_t s);
+// Prefill path (T > kDecodeMaxTokens, bf16 weights): grouped rows, the
+// gate/up + SwiGLU grouped GEMM, the down grouped GEMM, the combine.
+struct PrefillArgs {
+  const int32_t* hdr;
+  const int32_t* unique_expert;
+  const int32_t* unique_slot;
+  const int32_t* u_offset;
+  const int32_t* topk_idx;   // [T*k]
+  const float* topk_w;       // [T*k]
+  int32_t* rows_by_u;        // [T*k] out: rows grouped by unique expert
+  int32_t* pos;              // [T*k] out: grouped place of each row
+  const void* x;             // [T][H] bf16
+  void* h;                   // [T*k][I] bf16 scratch
+  float* yp;                 // [T*k][H] fp32 scratch
+  float* y;                  // [T][H] fp32 out
+  const uint8_t* pool;
+  long long expert_bytes;
+  int H, I, k, T, E;
+};
+bool prefill_supported(int H, int I, int wdtype, int E);
+cudaError_t launch_prefill_ffn(const PrefillArgs& a, cudaStream_t s, int* launches);
+
 // Decode path: the gate/up+SwiGLU kernel, then the down+combine kernel.
 cudaError_t launch_decode_gateup(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_decode_down(const FfnArgs& a, cudaStream_t s);
