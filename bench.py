@@ -55,6 +55,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-link", action="store_true")
+    p.add_argument("--prefill", action="store_true",
+                   help="also measure the 16,384-token prefill chunk (40 layers) and report it under 'prefill'")
     p.add_argument("--trace", action="store_true", help="print one step's per-layer timeline to stderr")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--timing-steps", type=int, default=64,
@@ -251,6 +253,60 @@ def run_reference(args, w):
 # of the ncu --set full capture summarised under profiles/.  It belongs to the
 # kernel as captured: set it to None whenever that kernel changes.
 FFN_TRAFFIC_PER_LAUNCH = {}
+
+
+def prefill_measure(dev, steps=2):
+    """The 35B-shaped prefill chunk (16,384 tokens per layer, 40 layers, 3072
+    slots): 40 x ~214 unique experts per step thrash the 3072-slot LRU, so
+    every step fetches nearly all its experts over the host link.  One step's
+    routing and hidden states are replayed `steps` times through a captured
+    step graph (the first as warm-up); the bank is aliased to 1024 blobs
+    (same transfer sizes).  Returns per-layer phase times and throughput."""
+    import torch
+
+    from expert_cache_host_layer_gb300.pipeline import ExpertCache, StepGraph
+    w = W.QWEN35B_PREFILL
+    L, T = w.num_layers, w.tokens
+    n_blobs = 1024
+    from expert_cache_host_layer_gb300.pipeline import pinned_bank
+    bank = pinned_bank(n_blobs * w.expert_bytes)
+    synth.expert_blobs(w.seed, w.hidden, w.inter, w.wdtype, np.arange(n_blobs), out_ptr=bank.data_ptr())
+    lg = [torch.from_numpy(synth.router_iid(w.seed, 0, l, T, w.num_experts, 1.1)).to(dev) for l in range(L)]
+    xs = [torch.from_numpy(W.hidden_states(w, 0, l)).to(dev, torch.bfloat16) for l in range(L)]
+    ys = [torch.empty((T, w.hidden), dtype=torch.float32, device=dev) for _ in range(L)]
+    c = ExpertCache(L, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots, T, bank, n_blobs,
+                    fetch_mode=1, device=dev)
+    out = {}
+    try:
+        for double in (True, False):
+            g = StepGraph(c, lg, xs, ys, double, timing=True)
+            try:
+                g.launch()  # warm-up step
+                c.synchronize()
+                st0 = c.stats()
+                tot = {"route": 0.0, "fetch": 0.0, "ffn": 0.0, "step": 0.0}
+                for _ in range(steps - 1):
+                    g.launch()
+                    r, fe, f, step_ms = g.timing()
+                    tot["route"] += r.sum(); tot["fetch"] += fe.sum(); tot["ffn"] += f.sum(); tot["step"] += step_ms
+                st1 = c.stats()
+            finally:
+                g.close()
+            n = max(1, steps - 1)
+            rows = T * w.top_k
+            flop = 2.0 * rows * (2 * w.inter * w.hidden + w.hidden * w.inter)  # per layer
+            ffn_ms = tot["ffn"] / n / L
+            out["double_buffer" if double else "serial"] = {
+                "tokens_per_s": T / (tot["step"] / n / 1e3), "ms_per_step": tot["step"] / n,
+                "per_layer_ms": {k: tot[k] / n / L for k in ("route", "fetch", "ffn")},
+                "ffn_tflops": flop / (ffn_ms / 1e3) / 1e12,
+                "fetched_gb_per_step": (st1["bytes_fetched"] - st0["bytes_fetched"]) / n / 1e9,
+                "miss_rate": (st1["misses"] - st0["misses"]) / max(1, st1["unique_experts"] - st0["unique_experts"])}
+    finally:
+        c.close()
+    out["note"] = ("step graph with timing event nodes, 40 layers, one 16,384-token chunk each; FFN = grouped "
+                   "mma.sync bf16 GEMMs (gate/up + SwiGLU, down) + combine; times from the event nodes")
+    return out
 
 
 def ffn_only(w, dev, peak):
@@ -509,6 +565,9 @@ def run_ours(args, w):
     ffn_alone = None
     if rank == 0 and T <= 8:
         ffn_alone = ffn_only(w, dev, peak)
+    prefill = None
+    if rank == 0 and args.prefill:
+        prefill = prefill_measure(dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -542,6 +601,7 @@ def run_ours(args, w):
                          "bytes_per_launch": ffn_bytes_per_launch,
                          "launch_us": ffn_ms * 1e3, "ffn_only": ffn_alone},
             "cpu_baseline": cpu,
+            "prefill": prefill,
             "e2e": e2e,
             "gpu_launches": d["kernel_launches"],
             "clocks": clocks,
