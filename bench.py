@@ -119,6 +119,16 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None, "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def measured_bf16_tflops() -> float:
+    """Burst bf16 dense TFLOP/s from MEASURED_PEAKS.json (the recipe's fallback
+    1900 if absent): the denominator of the prefill GEMMs' tensor fraction."""
+    try:
+        with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return 1900.0
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -255,7 +265,7 @@ def run_reference(args, w):
 FFN_TRAFFIC_PER_LAUNCH = {"qwen35b-a3b-shape-decode-b1": ((50.404352 + 0.292096) + (50.404608 + 0.148224)) / 2 * 1e6}
 
 
-def prefill_measure(dev, steps=2):
+def prefill_measure(dev, peak_tflops, steps=2):
     """The 35B-shaped prefill chunk (16,384 tokens per layer, 40 layers, 3072
     slots): 40 x ~214 unique experts per step thrash the 3072-slot LRU, so
     every step fetches nearly all its experts over the host link.  One step's
@@ -300,6 +310,7 @@ def prefill_measure(dev, steps=2):
                 "tokens_per_s": T / (tot["step"] / n / 1e3), "ms_per_step": tot["step"] / n,
                 "per_layer_ms": {k: tot[k] / n / L for k in ("route", "fetch", "ffn")},
                 "ffn_tflops": flop / (ffn_ms / 1e3) / 1e12,
+                "tensor_frac": flop / (ffn_ms / 1e3) / 1e12 / peak_tflops,
                 "fetched_gb_per_step": (st1["bytes_fetched"] - st0["bytes_fetched"]) / n / 1e9,
                 "miss_rate": (st1["misses"] - st0["misses"]) / max(1, st1["unique_experts"] - st0["unique_experts"])}
     finally:
@@ -567,7 +578,7 @@ def run_ours(args, w):
         ffn_alone = ffn_only(w, dev, peak)
     prefill = None
     if rank == 0 and args.prefill:
-        prefill = prefill_measure(dev)
+        prefill = prefill_measure(dev, measured_bf16_tflops())
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -586,6 +597,8 @@ def run_ours(args, w):
                            fetch_mode=["copy_engine", "sm_pull"][args.fetch_mode], double_buffer=double,
                            step_graph=use_graph),
             "miss_rate": d["misses"] / max(1, d["unique_experts"]),
+            "exposed_copy_ms_per_step": (elapsed_ms / args.steps - L * ffn_alone["launch_us"] / 1e3)
+            if ffn_alone else None,
             "expert_gemm_gbs": achieved,
             "miss_copy": {"gbs": fetch_gbs, "bytes_per_step": d["bytes_fetched"] / args.steps,
                           "mode": ["copy_engine", "sm_pull"][args.fetch_mode], "link": link},

@@ -1,0 +1,92 @@
+"""Cache policies the method is compared with, simulated on the same routing
+traces (oracle; test infrastructure, like the rest of this package).
+
+The pages contrast the global (layer, expert) LRU cache with static
+placements:
+- layer-based offload, which keeps whole layers on the GPU and reads the rest
+  from host memory ("FreeToken: az VRAM ile büyük MoE modelleri", the engine
+  comparison);
+- static expert placement that cannot follow routing which changes from token
+  to token ("FreeToken: Efficient Edge-Native MoE Serving ...", motivation
+  paragraph);
+- keeping a fixed share of experts resident (the --offload-ratio flag of the
+  FreeToken MoE inference guide).
+
+Readings:
+- Every policy gets the same C slots.
+- A miss is a unique (layer, expert) of a layer event that is not resident.
+- Static policies are preloaded and never evict; their misses are streamed
+  and not kept.
+- The static split gives each layer floor(C/L) slots (the first C mod L
+  layers one more) and runs an LRU inside each layer.  There is no pin:
+  layers do not share slots.
+"""
+from __future__ import annotations
+
+from collections import OrderedDict
+
+import numpy as np
+
+
+def unique_events(topk_trace):
+    """[(layer, sorted unique experts)] in event order, from top-k indices
+    shaped [steps][L][T][k]."""
+    steps, L = topk_trace.shape[0], topk_trace.shape[1]
+    return [(l, np.unique(topk_trace[s, l])) for s in range(steps) for l in range(L)]
+
+
+def static_split_lru(events, num_layers: int, num_slots: int):
+    """Per-layer LRU caches of floor(C/L) (+1 for the first C mod L layers)
+    slots.  Returns (misses, unique)."""
+    cap = [num_slots // num_layers + (1 if l < num_slots % num_layers else 0) for l in range(num_layers)]
+    caches = [OrderedDict() for _ in range(num_layers)]
+    misses = unique = 0
+    for l, experts in events:
+        c = caches[l]
+        for e in experts:
+            unique += 1
+            if e in c:
+                c.move_to_end(e)
+                continue
+            misses += 1
+            if cap[l] == 0:
+                continue
+            if len(c) >= cap[l]:
+                # evict the least recently used expert that this event does not use
+                victim = next((k for k in c if k not in set(experts.tolist())), None)
+                if victim is None:
+                    continue
+                del c[victim]
+            c[e] = True
+    return misses, unique
+
+
+def static_layers(events, num_layers: int, num_experts: int, num_slots: int):
+    """Whole layers resident, the first floor(C/E) of them (layer-based
+    offload).  Returns (misses, unique)."""
+    resident = num_slots // num_experts
+    misses = unique = 0
+    for l, experts in events:
+        unique += len(experts)
+        if l >= resident:
+            misses += len(experts)
+    return misses, unique
+
+
+def static_profile(events, num_experts: int, num_slots: int, profile_events: int):
+    """The num_slots (layer, expert) keys used most often in the first
+    `profile_events` events stay resident (ties: lower key first); measured on
+    the events after the profile.  Returns (misses, unique)."""
+    counts = {}
+    for l, experts in events[:profile_events]:
+        for e in experts:
+            key = l * num_experts + int(e)
+            counts[key] = counts.get(key, 0) + 1
+    ranked = sorted(counts.items(), key=lambda kv: (-kv[1], kv[0]))
+    resident = {key for key, _ in ranked[:num_slots]}
+    misses = unique = 0
+    for l, experts in events[profile_events:]:
+        for e in experts:
+            unique += 1
+            misses += (l * num_experts + int(e)) not in resident
+    return misses, unique

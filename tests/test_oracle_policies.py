@@ -1,0 +1,94 @@
+"""Comparison cache policies (oracle/policies.py) against brute force and
+closed forms, then all of them against the method's global LRU on the
+35B-A3B-shaped decode trace (the miss rates DESIGN records)."""
+import numpy as np
+import pytest
+
+from oracle import policies, routing
+from oracle.cache import ExpertCacheOracle
+from synth import workloads as W
+
+
+def _random_events(rng, L, E, k, steps):
+    trace = np.stack([np.stack([rng.choice(E, size=(1, k), replace=False) for _ in range(L)])
+                      for _ in range(steps)])
+    return trace, policies.unique_events(trace)
+
+
+def _textbook_lru_misses(events, cap):
+    """One LRU list with explicit last-use stamps (no shared code with the policy)."""
+    last = {}
+    misses = 0
+    for t, (_, experts) in enumerate(events):
+        for e in experts:
+            if e not in last:
+                misses += 1
+                if len(last) >= cap:
+                    victim = min((s, x) for x, s in last.items() if x not in set(experts.tolist()))[1]
+                    del last[victim]
+            last[e] = t
+    return misses
+
+
+def test_static_split_with_one_layer_is_textbook_lru():
+    rng = np.random.default_rng(3)
+    _, events = _random_events(rng, 1, 12, 3, 200)
+    for cap in (3, 5, 8, 12):
+        m, u = policies.static_split_lru(events, 1, cap)
+        assert u == 600 and m == _textbook_lru_misses(events, cap), cap
+
+
+def test_static_split_shares_slots_as_stated():
+    rng = np.random.default_rng(4)
+    trace, events = _random_events(rng, 3, 10, 2, 50)
+    # 3 layers, 7 slots: layers get 3, 2, 2; each layer alone is a textbook LRU of its share
+    m, u = policies.static_split_lru(events, 3, 7)
+    want = sum(_textbook_lru_misses([ev for ev in events if ev[0] == l], cap) for l, cap in enumerate((3, 2, 2)))
+    assert m == want and u == 300
+
+
+def test_static_layers_closed_form():
+    rng = np.random.default_rng(5)
+    trace, events = _random_events(rng, 4, 16, 2, 30)
+    total = sum(len(x) for _, x in events)
+    assert policies.static_layers(events, 4, 16, 0) == (total, total)
+    assert policies.static_layers(events, 4, 16, 64) == (0, total)
+    later = sum(len(x) for l, x in events if l >= 2)  # two whole layers resident
+    assert policies.static_layers(events, 4, 16, 2 * 16 + 15) == (later, total)
+
+
+def test_static_profile_bounds_and_monotone():
+    rng = np.random.default_rng(6)
+    trace, events = _random_events(rng, 2, 20, 3, 60)
+    half = len(events) // 2
+    after = sum(len(x) for _, x in events[half:])
+    assert policies.static_profile(events, 20, 0, half) == (after, after)
+    m_all, _ = policies.static_profile(events, 20, 40, half)  # every key of the profile fits
+    seen = {l * 20 + int(e) for l, x in events[:half] for e in x}
+    assert m_all == sum(1 for l, x in events[half:] for e in x if l * 20 + int(e) not in seen)
+    ms = [policies.static_profile(events, 20, c, half)[0] for c in range(0, 41, 5)]
+    assert all(a >= b for a, b in zip(ms, ms[1:]))
+
+
+@pytest.mark.parametrize("steps", [512])
+def test_policies_on_the_35b_decode_trace(steps):
+    """Global (layer, expert) LRU against static placements with the same 3072
+    slots on the 35B-A3B-shaped decode routing (512 steps, batch 1)."""
+    w = W.QWEN35B_DECODE
+    logits = W.router_logits(w.replace(steps=steps))
+    trace = np.stack([np.stack([routing.route(logits[s, l], w.top_k)[0] for l in range(w.num_layers)])
+                      for s in range(steps)])
+    events = policies.unique_events(trace)
+    cache = ExpertCacheOracle(w.num_layers, w.num_experts, w.num_slots)
+    for l, experts in ((l, trace[s, l]) for s in range(steps) for l in range(w.num_layers)):
+        cache.event(l, experts)
+    rates = {"global_lru": cache.n_miss / cache.n_unique}
+    m, u = policies.static_split_lru(events, w.num_layers, w.num_slots)
+    rates["static_split_lru"] = m / u
+    m, u = policies.static_layers(events, w.num_layers, w.num_experts, w.num_slots)
+    rates["static_layers"] = m / u
+    m, u = policies.static_profile(events, w.num_experts, w.num_slots, 64 * w.num_layers)
+    rates["static_profile_64_steps"] = m / u
+    print("miss rates (35B decode, 3072 slots, 512 steps):", {k: round(v, 4) for k, v in rates.items()})
+    # the method's cache beats placing whole layers (the offload the pages compare against)
+    assert rates["global_lru"] < rates["static_layers"]
