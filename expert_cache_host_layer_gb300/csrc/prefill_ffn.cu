@@ -24,6 +24,9 @@
 // Efficient Edge-Native MoE Serving ...", ablation paragraph).
 #include <cuda_bf16.h>
 
+#include <mutex>
+#include <set>
+
 #include "ft_internal.h"
 
 namespace ft {
@@ -396,8 +399,13 @@ bool prefill_supported(int H, int I, int wdtype, int E) {
 }
 
 cudaError_t launch_prefill_ffn(const PrefillArgs& a, cudaStream_t s, int* launches) {
-  static bool attrs = false;
-  if (!attrs) {
+  static std::mutex mu;
+  static std::set<int> ready;  // devices whose kernel attributes are set
+  int dev = 0;
+  cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess) return ge;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ready.count(dev)) {
     cudaError_t e = cudaFuncSetAttribute(gateup_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(down_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
     if (e == cudaSuccess)
@@ -407,7 +415,7 @@ cudaError_t launch_prefill_ffn(const PrefillArgs& a, cudaStream_t s, int* launch
       e = cudaFuncSetAttribute(down_gemm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    attrs = true;
+    ready.insert(dev);
   }
   const int grid = 2 * prefill_sms();
   group_rows_kernel<<<a.E, kPThreads, 0, s>>>(a);
