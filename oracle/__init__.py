@@ -15,7 +15,11 @@ fp64 where floating point is involved:
                  table updates, and the safe-point resize;
 * ``fp8``      - OCP FP8 E4M3 decoding;
 * ``ffn``      - expert-blob dequantisation and the SwiGLU expert FFN with the
-                 gate-weighted combine.
+                 gate-weighted combine;
+* ``stream``   - the decision stream of a whole workload (events in step,
+                 then layer order, with the safe-point resize);
+* ``policies`` - the static placements the pages compare the cache with,
+                 simulated on the same routing (miss rates only).
 
 Sources (the pages' titles):
 * "FreeToken: Efficient Edge-Native MoE Serving with Bandwidth-Adaptive

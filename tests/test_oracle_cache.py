@@ -224,3 +224,47 @@ def test_exhaustive_tiny_traces_match_brute_force():
                 _, _, chosen, evicted, slots = b.event(0, idx)
                 assert ev.miss_slot.tolist() == chosen and ev.unique_slot.tolist() == slots
                 assert ev.evicted_key.tolist() == evicted
+
+
+def test_tables_are_consistent_with_the_event_records():
+    """tables() (what the GPU tables are compared with) against the events:
+    key_to_slot and slot_key are inverse maps over the resident keys, no more
+    than C keys are resident, and each slot's last use is the last event that
+    put its key there or hit it (recomputed from the event records)."""
+    import numpy as _np
+    from oracle.cache import ExpertCacheOracle as _C
+    rng = _np.random.default_rng(11)
+    L, E, k, C = 3, 12, 3, 12  # C = 2 * min(T*k, E): the capacity bound
+    cache = _C(L, E, C)
+    last_use = {}
+    for t in range(120):
+        l = t % L
+        ev = cache.event(l, rng.choice(E, size=(2, k), replace=True))
+        for u, e in enumerate(ev.unique.tolist()):
+            last_use[int(ev.unique_slot[u])] = (l * E + e, ev.t)
+        k2s, sk, ts = cache.tables()
+        resident = _np.flatnonzero(k2s >= 0)
+        assert len(resident) <= C
+        assert all(sk[k2s[key]] == key for key in resident)
+        assert all(k2s[sk[s]] == s for s in range(C) if sk[s] >= 0)
+        for s, (key, when) in last_use.items():
+            if sk[s] == key:
+                assert ts[s] == when, (t, s)
+
+
+def test_run_decisions_closed_forms():
+    """The decision stream of a workload: with every key fitting, each key
+    misses exactly once (its first use); a resize to the same size changes
+    no decision."""
+    import numpy as _np
+    from oracle.stream import run_decisions
+    rng = _np.random.default_rng(12)
+    steps, L, T, E, k = 9, 2, 3, 16, 2
+    logits = rng.standard_normal((steps, L, T, E)).astype(_np.float32)
+    cache, recs = run_decisions(L, E, k, L * E, logits)
+    keys = {l * E + int(e) for _, l, idx, _, _ in recs for e in idx.ravel()}
+    assert len(recs) == steps * L and cache.n_miss == len(keys) and cache.n_evict == 0
+    a, ra = run_decisions(L, E, k, 12, logits)
+    b, rb = run_decisions(L, E, k, 12, logits, resize_step=4, resize_slots=12)
+    assert (a.n_miss, a.n_hit, a.n_evict) == (b.n_miss, b.n_hit, b.n_evict)
+    assert all(_np.array_equal(x[4].miss_expert, y[4].miss_expert) for x, y in zip(ra, rb))
