@@ -60,3 +60,44 @@ def test_host_only_calls(lib_path):
     assert b"num_layers" in lib.ft_last_error()
     assert lib.ft_route_classify(None, 0, None, 0, None, None) == ft.FT_ERR_INVALID_ARG
     assert lib.ft_cache_destroy(None) == ft.FT_OK
+
+
+@pytest.mark.parametrize("field,value,message", [
+    ("num_experts", 0, b"num_experts"),
+    ("num_experts", 2048, b"num_experts"),
+    ("top_k", 0, b"top_k"),
+    ("top_k", 40, b"top_k"),
+    ("hidden", 102, b"unsupported hidden/inter/wdtype"),  # fp32 rows need multiples of 4
+    ("max_tokens", 0, b"max_tokens"),
+    ("fetch_mode", 7, b"fetch_mode"),
+    ("copy_streams", 3, b"copy_streams"),
+    ("fetch_warps", 5, b"fetch_warps"),
+    ("bank_blobs", 0, b"bank_blobs"),
+    ("host_bank_bytes", 1, b"host_bank_bytes"),
+])
+def test_create_rejects_bad_configs_before_any_gpu_work(lib_path, field, value, message):
+    """ft_cache_create validates its arguments on the host first: each bad
+    field gives FT_ERR_INVALID_ARG and a message naming it, with no GPU."""
+    import expert_cache_host_layer_gb300 as ft
+    lib = ft.library()
+    bank = ctypes.create_string_buffer(64)  # never read: validation comes first
+    cfg = ft.make_config(2, 16, 2, 256, 128, ft.FT_W_F32, ctypes.addressof(bank), 10 ** 9, 16, 1)
+    setattr(cfg, field, value)
+    out = ctypes.c_void_p()
+    st = lib.ft_cache_create(ctypes.byref(cfg), ctypes.c_void_p(1 << 20), 12, None, ctypes.byref(out))
+    assert st == ft.FT_ERR_INVALID_ARG and message in lib.ft_last_error(), (st, lib.ft_last_error())
+    assert not out.value
+
+
+def test_create_rejects_unaligned_pool_and_bad_slot_counts(lib_path):
+    import expert_cache_host_layer_gb300 as ft
+    lib = ft.library()
+    bank = ctypes.create_string_buffer(64)
+    cfg = ft.make_config(2, 16, 2, 256, 128, ft.FT_W_F32, ctypes.addressof(bank), 10 ** 9, 16, 1)
+    out = ctypes.c_void_p()
+    assert lib.ft_cache_create(ctypes.byref(cfg), ctypes.c_void_p((1 << 20) + 8), 12, None,
+                               ctypes.byref(out)) == ft.FT_ERR_INVALID_ARG
+    assert b"256-byte aligned" in lib.ft_last_error()
+    assert lib.ft_cache_create(ctypes.byref(cfg), ctypes.c_void_p(1 << 20), 0, None,
+                               ctypes.byref(out)) == ft.FT_ERR_INVALID_ARG
+    assert b"num_slots" in lib.ft_last_error()
