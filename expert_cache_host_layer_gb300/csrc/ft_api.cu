@@ -652,6 +652,8 @@ ft_status ft_route_classify(ft_cache* c, int32_t layer, const float* logits, int
   if (layer < 0 || layer >= c->L) return fail(FT_ERR_INVALID_ARG, "layer %d out of range", layer);
   if (T < 0 || T > c->max_tokens) return fail(FT_ERR_INVALID_ARG, "T=%d outside 0..max_tokens=%d", T, c->max_tokens);
   if (T > 0 && !logits) return fail(FT_ERR_INVALID_ARG, "null logits");
+  if (T > kDecodeMaxTokens && c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE)  // its kernels do not wait for the copy thread
+    return fail(FT_ERR_UNSUPPORTED, "T=%d > %d (prefill) needs the SM-pull fetch mode", T, kDecodeMaxTokens);
   const int t = c->next_event;
   // a fetched plan must be consumed by its FFN before the layer is re-planned
   if (c->fetch_event[layer] >= 0 && c->fetch_event[layer] == c->layer_event[layer] &&

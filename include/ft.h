@@ -174,8 +174,8 @@ ft_status ft_cache_destroy(ft_cache* cache);
 ft_status ft_cache_resize(ft_cache* cache, void* new_pool, int64_t new_num_slots);
 
 /*
- * Route one layer's token batch and update the cache, in one kernel on the
- * compute stream: top-k + gates per token, dedup of the batch's experts,
+ * Route one layer's token batch and update the cache, in one kernel: top-k
+ * + gates per token, dedup of the batch's experts,
  * hit/miss classification, global-LRU victims for the misses, table update.
  *   logits   device, float32 [T][E], row-major
  *   topk_idx device, int32 [T][k] or NULL: experts per token in selection
@@ -191,16 +191,24 @@ ft_status ft_cache_resize(ft_cache* cache, void* new_pool, int64_t new_num_slots
  * not before other work the caller enqueues in between.
  * Errors: FT_ERR_INVALID_ARG (layer, T > max_tokens, null logits),
  * FT_ERR_STATE (this layer's previous plan is still being fetched and its
- * fetch failed), FT_ERR_CUDA.
+ * fetch failed), FT_ERR_UNSUPPORTED (T > 8 in copy-engine mode: the prefill
+ * kernels read the slots without waiting for the copy thread), FT_ERR_CUDA.
  */
 ft_status ft_route_classify(ft_cache* cache, int32_t layer, const float* logits, int32_t T, int32_t* topk_idx,
                             float* topk_w);
 
 /*
  * Copy the layer's misses (from its last ft_route_classify) from the host
- * bank into their victim slots, on the copy stream, after the classification
- * completes.  Asynchronous; the compute stream does not wait here (so the
- * next layer's misses can stream while this layer computes).
+ * bank into their victim slots, after the classification completes and
+ * after the FFN of two events before (whose slots may be the victims).
+ * Asynchronous; the compute stream does not wait here, so the next layer's
+ * misses stream while this layer computes.  SM-pull mode: the copy is
+ * deferred and done by the copy warps of the next ft_moe_forward of another
+ * layer (one kernel per layer moves the next layer's experts over the host
+ * link while this layer's stream from HBM); a forward of the layer itself,
+ * a prefill forward or any synchronising call runs it as a pull kernel on the
+ * copy stream instead.  Copy-engine mode: the library's copy thread issues one
+ * cudaMemcpyAsync per miss on the copy stream.
  * Errors: FT_ERR_INVALID_ARG, FT_ERR_STATE (no classification pending for
  * this layer), FT_ERR_CUDA.
  */
@@ -212,10 +220,15 @@ ft_status ft_fetch_misses(ft_cache* cache, int32_t layer);
  *   x  device [T][H]: float32 for FT_W_F32, bf16 otherwise
  *   y  device [T][H]: float32; fully overwritten
  * T must equal the T of the layer's last ft_route_classify.  The compute
- * stream first waits for the layer's fetch.  T <= 8 runs the decode GEMV
- * kernels; larger T the grouped tensor-core GEMM path.
+ * stream first waits for the layer's fetch.  T <= 8 (decode) runs one fused
+ * kernel per layer (gate/up, SwiGLU, down, combine; in SM-pull mode it also
+ * copies the next requested layer's misses).  Larger T (prefill, bf16
+ * weights only, hidden % 128 and inter % 64) groups the rows by expert and
+ * runs the gate/up + SwiGLU and down projections as grouped tensor-core GEMMs,
+ * then combines each token's picks in pick order.
  * Errors: FT_ERR_INVALID_ARG, FT_ERR_STATE (no fetch issued for the layer's
- * current plan), FT_ERR_UNSUPPORTED, FT_ERR_CUDA.
+ * current plan), FT_ERR_UNSUPPORTED (a prefill T with other weight types or
+ * shapes, or a cache created with max_tokens <= 8), FT_ERR_CUDA.
  */
 ft_status ft_moe_forward(ft_cache* cache, int32_t layer, const void* x, int32_t T, void* y);
 
