@@ -1,6 +1,6 @@
 """Comparison cache policies (oracle/policies.py) against brute force and
 closed forms, then all of them against the method's global LRU on the
-35B-A3B-shaped decode trace (the miss rates DESIGN records)."""
+35B-A3B-shaped decode traces (the test prints the miss rates)."""
 import numpy as np
 import pytest
 
@@ -70,11 +70,13 @@ def test_static_profile_bounds_and_monotone():
     assert all(a >= b for a, b in zip(ms, ms[1:]))
 
 
-@pytest.mark.parametrize("steps", [512])
-def test_policies_on_the_35b_decode_trace(steps):
-    """Global (layer, expert) LRU against static placements with the same 3072
-    slots on the 35B-A3B-shaped decode routing (512 steps, batch 1)."""
-    w = W.QWEN35B_DECODE
+@pytest.mark.parametrize("w", [W.QWEN35B_DECODE, W.QWEN35B_DECODE_B4, W.QWEN35B_DECODE_B8],
+                         ids=["b1-3072-slots", "b4-1740-slots", "b8-1740-slots"])
+def test_policies_on_the_35b_decode_trace(w):
+    """Global (layer, expert) LRU against static placements with the same
+    slots on the 35B-A3B-shaped decode routing (512 steps; batch 1 with 3072
+    slots, 4 and 8 streams with 1740)."""
+    steps = w.steps
     logits = W.router_logits(w.replace(steps=steps))
     trace = np.stack([np.stack([routing.route(logits[s, l], w.top_k)[0] for l in range(w.num_layers)])
                       for s in range(steps)])
@@ -89,6 +91,6 @@ def test_policies_on_the_35b_decode_trace(steps):
     rates["static_layers"] = m / u
     m, u = policies.static_profile(events, w.num_experts, w.num_slots, 64 * w.num_layers)
     rates["static_profile_64_steps"] = m / u
-    print("miss rates (35B decode, 3072 slots, 512 steps):", {k: round(v, 4) for k, v in rates.items()})
+    print(f"miss rates ({w.name}, {w.num_slots} slots, {steps} steps):", {k: round(v, 4) for k, v in rates.items()})
     # the method's cache beats placing whole layers (the offload the pages compare against)
     assert rates["global_lru"] < rates["static_layers"]
