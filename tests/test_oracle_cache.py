@@ -205,6 +205,78 @@ def test_resize_keeps_most_recent_and_compacts(new_C):
     assert int(ev.hit.sum()) + len(ev.miss_expert) == len(ev.unique)
 
 
+@pytest.mark.parametrize("L,E,C,new_C,seed", [(2, 8, 9, 4, 41), (3, 8, 12, 5, 42), (4, 16, 20, 7, 43),
+                                               (2, 16, 6, 10, 44), (1, 4, 3, 2, 45)])
+def test_resize_k1_matches_textbook_lru_at_the_new_capacity(L, E, C, new_C, seed):
+    """k = 1: one key per event, so every resident key has its own last-use
+    time and LRU order is total.  After resize(C') the resident keys must be
+    exactly the C' most recently used keys of a textbook OrderedDict LRU, and
+    the next 100 events must hit, miss and evict exactly as that LRU does at
+    capacity C' (no slot arithmetic involved)."""
+    trace = random_trace(seed, L, E, 1, 1, 160)
+    c = ExpertCacheOracle(L, E, C)
+    lru = collections.OrderedDict()
+
+    def access(key, cap):
+        if key in lru:
+            lru.move_to_end(key)
+            return True, -1
+        ev = lru.popitem(last=False)[0] if len(lru) == cap else -1
+        lru[key] = True
+        return False, ev
+
+    for s in range(60):
+        for l in range(L):
+            c.event(l, trace[s][l])
+            access(l * E + int(trace[s][l][0, 0]), C)
+    c.resize(new_C)
+    while len(lru) > new_C:
+        lru.popitem(last=False)
+    assert set(np.flatnonzero(c.key_to_slot >= 0).tolist()) == set(lru)
+    n = 0
+    for s in range(60, 160):
+        for l in range(L):
+            key = l * E + int(trace[s][l][0, 0])
+            ev = c.event(l, trace[s][l])
+            hit, evicted = access(key, new_C)
+            assert ev.hit.tolist() == [int(hit)], (s, l)
+            assert ev.evicted_key.tolist() == ([] if hit else [evicted]), (s, l)
+            n += 1
+            if n == 100:
+                assert set(np.flatnonzero(c.key_to_slot >= 0).tolist()) == set(lru)
+                return
+
+
+@pytest.mark.parametrize("new_C", [4, 7, 10])
+def test_resize_drops_the_keys_the_next_misses_would_evict(new_C):
+    """Ties in last use (k = 3 picks per event share one time): shrinking
+    drops exactly the keys that the victim rule of an event would evict
+    first.  The same cache state is shrunk in one copy and, in another,
+    served one event of never-seen experts on a layer whose misses need
+    exactly that many victims with no pin (the first event after a resize
+    pins nothing, so a same-size resize clears the pin first).  Flipping the
+    tie order of either rule (slot descending among equal last use) changes
+    the dropped set and fails here."""
+    import copy
+    L, E, k, C = 3, 32, 3, 12
+    trace = random_trace(51, L, E, k, 1, 30, ties=True)
+    base = ExpertCacheOracle(L + 1, E, C)
+    for s in range(30):
+        for l in range(L):
+            base.event(l, trace[s][l])
+    occupied = int(np.count_nonzero(base.slot_key >= 0))
+    n_drop = occupied - new_C
+    assert n_drop > 0
+    shrunk = copy.deepcopy(base)
+    before = {int(k_) for k_ in shrunk.slot_key if k_ >= 0}
+    shrunk.resize(new_C)
+    dropped = before - {int(k_) for k_ in shrunk.slot_key if k_ >= 0}
+    evictor = copy.deepcopy(base)
+    evictor.resize(C)                                       # same size: only clears the pin
+    ev = evictor.event(L, np.arange(n_drop, dtype=np.int32)[None, :])   # layer L: all misses
+    assert set(ev.evicted_key.tolist()) == dropped and len(dropped) == n_drop
+
+
 def test_miss_rate_counts_unique_experts_per_event():
     c = ExpertCacheOracle(1, 8, 8)
     c.event(0, np.array([[1, 2], [2, 3]]))   # U = {1,2,3}: 3 misses

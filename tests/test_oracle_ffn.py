@@ -104,6 +104,34 @@ def test_fp8_block_scales_applied_per_block():
     assert np.all(d[:128, :] == 0.5) and np.all(d[128:, :] == 0.25)
 
 
+def test_fp8_scale_grid_is_row_block_major_on_a_non_square_grid():
+    """H = 384, I = 256: Wg and Wu have 2 x 3 grids of 128 x 128 blocks, Wd a
+    3 x 2 grid; every block gets its own scale and every weight its own code.
+    Each weight must equal its code's E4M3 value times the scale of block
+    (r // 128, c // 128) taken from the matrix's grid in row-block-major order,
+    the format the blob layout states.  A transposed (column-block-major) grid
+    puts other scales on 4 of the 6 blocks of each matrix, so it fails here."""
+    H, I = 384, 256
+    n = H * I
+    codes = np.empty(3 * n, dtype=np.uint8)
+    # finite codes only (0x00..0x7e, then the same with the sign bit), varied per element
+    codes[:] = (np.arange(3 * n) * 37) % 0x7F
+    codes[1::5] |= 0x80
+    grid_g = (I // 128) * (H // 128)                 # 6 blocks each for Wg, Wu, Wd
+    scales = np.array([2.0 ** (j - 9) for j in range(3 * grid_g)], dtype=np.float32)  # all distinct, exact in bf16
+    blob = np.concatenate([codes, synth.bf16_bits(scales).view(np.uint8)])
+    assert blob.size == ffn.expert_bytes(H, I, ffn.W_FP8)
+    g, u, d = ffn.dequant_blob(blob, H, I, ffn.W_FP8)
+    mats = ((g, I, H, 0), (u, I, H, grid_g), (d, H, I, 2 * grid_g))
+    for m, (mat, rows, cols, s0) in enumerate(mats):
+        col_blocks = cols // 128
+        for r in range(rows):
+            for c in range(0, cols, 7):          # every 7th column of every row: all blocks, many codes
+                code = int(codes[m * n + r * cols + c])
+                want = fp8.decode(code) * float(scales[s0 + (r // 128) * col_blocks + c // 128])
+                assert mat[r, c] == want, (m, r, c)
+
+
 @pytest.mark.parametrize("wdtype,H,I", [(ffn.W_F32, 64, 32), (ffn.W_BF16, 128, 64), (ffn.W_FP8, 256, 128)])
 def test_dense_identity_all_experts_zero_gates(wdtype, H, I):
     E, k, T = 8, 2, 6
