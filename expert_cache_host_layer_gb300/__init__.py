@@ -91,6 +91,7 @@ def _load():
         "ft_step_graph_trace": (st, [P, P]),
         "ft_step_graph_destroy": (st, [P]),
         "ft_moe_decode_ffn_static": (st, [I32, I32, I32, I32, I32, P, I64, P, P, P, P, I32, P, P]),
+        "ft_moe_decode_ffn_static_status": (st, [P]),
         "ft_status_str": (ctypes.c_char_p, [st]),
         "ft_last_error": (ctypes.c_char_p, []),
     }
@@ -266,6 +267,11 @@ def ft_moe_decode_ffn_static(hidden: int, inter: int, wdtype: int, num_experts: 
     _check(_lib.ft_moe_decode_ffn_static(hidden, inter, wdtype, num_experts, top_k, slot_pool or None, num_slots,
                                          expert_slot or None, topk_idx or None, topk_w or None, x or None, T,
                                          y or None, stream or None), "ft_moe_decode_ffn_static")
+
+
+def ft_moe_decode_ffn_static_status(stream: int = 0):
+    """Raise FtError if an earlier static-scratch FFN call hit a bounded-wait timeout (clears it)."""
+    _check(_lib.ft_moe_decode_ffn_static_status(stream or None), "ft_moe_decode_ffn_static_status")
 
 
 def ft_status_str(status: int) -> str:

@@ -8,31 +8,63 @@
 // a cache handle, and ft_cache_create allocates its tables and buffers; this
 // entry point needs neither.  Its working memory (the per-call expert
 // grouping and the fp32 intermediate h) lives in one file-scope __device__
-// array that the CUDA runtime reserves on every GPU that loads the library,
-// and keeps until the process exits.
+// array.  With lazy module loading (the CUDA default) the array is reserved
+// on a GPU when the library's module is first loaded there - at the first
+// call on that device - and kept until the process exits; with
+// CUDA_MODULE_LOADING=EAGER it is reserved when the library loads.
 //
 // The array is shared by all calls on a device and keeps whatever the last
-// call left in it.  Each call first rewrites every word it later reads, so
-// nothing has to start at zero; but two calls whose kernels overlap on the
-// GPU (different streams, or different host threads) race on it and produce
-// garbage.  Serialise them on one stream.
+// call left in it.  Each call first rewrites every plan word it later reads,
+// so nothing there has to start at zero; the status word is the exception: it
+// starts at zero (static storage), a bounded wait that runs out sets it, and
+// only ft_moe_decode_ffn_static_status reads and clears it.  Two calls whose
+// kernels overlap on the GPU (different streams, or different host threads)
+// race on the array and produce garbage.  Serialise them on one stream.
 #include <algorithm>
 #include <mutex>
 #include <string>
 
+#include "driver_api.h"
 #include "ft_internal.h"
 
 namespace ft {
 namespace {
 
 constexpr size_t kScratchBytes = size_t(1) << 20;   // 1 MiB
-constexpr int kPlanWords = 4096;                      // header, unique_slot, u_offset, rows_by_u
+constexpr int kStatusWords = 16;                      // word 0: sticky status of the kernels' bounded waits
+constexpr int kPlanWords = 4096;                      // status, header, unique_slot, u_offset, rows_by_u
 constexpr size_t kHBytes = kScratchBytes - kPlanWords * sizeof(int32_t);
 
 static __device__ __align__(256) unsigned char g_ffn_scratch[kScratchBytes];
 
+// Device address of g_ffn_scratch per device ordinal, with the context it was
+// looked up in: a different current context (after cudaDeviceReset, or a
+// context the caller created) gets the address looked up again.
+struct ScratchAddr {
+  CUcontext ctx = nullptr;
+  void* addr = nullptr;
+};
 std::mutex g_mu;
-void* g_scratch_addr[64] = {};  // device address of g_ffn_scratch, per device ordinal
+ScratchAddr g_scratch_addr[64];
+
+ft_status scratch_base(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return set_error(FT_ERR_CUDA, "cudaGetDevice failed or device ordinal >= 64");
+  const CUcontext ctx = current_context();
+  std::lock_guard<std::mutex> lk(g_mu);
+  ScratchAddr& a = g_scratch_addr[dev];
+  if (!a.addr || a.ctx != ctx) {  // first call on this device (or in this context): look the address up
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_ffn_scratch);
+    if (e != cudaSuccess || !p)
+      return set_error(FT_ERR_CUDA, "cudaGetSymbolAddress of the static scratch: %s", cudaGetErrorString(e));
+    a.addr = p;
+    a.ctx = ctx;
+  }
+  *out = a.addr;
+  return FT_OK;
+}
 
 // Groups the T*k (token, pick) rows by expert: the plan the decode FFN kernels read.
 __global__ void static_plan_kernel(const int32_t* topk_idx, int T, int k, int E, const int32_t* expert_slot,
@@ -112,6 +144,8 @@ extern "C" ft_status ft_moe_decode_ffn_static(int32_t hidden, int32_t inter, int
   const size_t eb = ft_expert_bytes(hidden, inter, wdtype);
   if (eb == 0 || (wdtype != FT_W_F32 && (hidden % 128 || inter % 128)))
     return set_error(FT_ERR_INVALID_ARG, "unsupported hidden/inter/wdtype (%d, %d, %d)", hidden, inter, wdtype);
+  if (hidden % 8)  // the down kernel gives each of its 8 consumer warps one output column per block of 8
+    return set_error(FT_ERR_INVALID_ARG, "hidden=%d is not a multiple of 8", hidden);
   if (num_experts < 1 || num_experts > kMaxExperts || top_k < 1 || top_k > kMaxTopK || top_k > num_experts)
     return set_error(FT_ERR_INVALID_ARG, "num_experts must be 1..%d and top_k 1..min(num_experts, %d)", kMaxExperts,
                      kMaxTopK);
@@ -120,33 +154,23 @@ extern "C" ft_status ft_moe_decode_ffn_static(int32_t hidden, int32_t inter, int
   if (T == 0) return FT_OK;
   if (!slot_pool || num_slots < 1 || !expert_slot || !topk_idx || !topk_w || !x || !y)
     return set_error(FT_ERR_INVALID_ARG, "null pointer or num_slots < 1");
-  // the scratch limit: header + unique_slot[E] + u_offset[E+1] + rows in the plan area, T*k*I floats for h
+  // the scratch limit: status + header + unique_slot[E] + u_offset[E+1] + rows in the plan area, T*k*I floats for h
   const long long rows = (long long)T * top_k;
-  if (PH_WORDS + 2LL * num_experts + 1 + rows > kPlanWords)
+  const long long plan_words = kStatusWords + PH_WORDS + 2LL * num_experts + 1 + rows;
+  if (plan_words > kPlanWords)
     return set_error(FT_ERR_INVALID_ARG, "plan of %lld words exceeds the static scratch plan area of %d words",
-                     PH_WORDS + 2LL * num_experts + 1 + rows, kPlanWords);
+                     plan_words, kPlanWords);
   if ((size_t)rows * inter * sizeof(float) > kHBytes)
     return set_error(FT_ERR_INVALID_ARG,
                      "T*top_k*inter*4 = %lld bytes exceeds the %zu-byte static scratch for the intermediate h",
                      rows * inter * 4LL, kHBytes);
 
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
-    return set_error(FT_ERR_CUDA, "cudaGetDevice failed or device ordinal >= 64");
   void* base = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_addr[dev]) {  // first call on this device: look up the array's device address once
-      void* p = nullptr;
-      const cudaError_t e = cudaGetSymbolAddress(&p, g_ffn_scratch);
-      if (e != cudaSuccess || !p)
-        return set_error(FT_ERR_CUDA, "cudaGetSymbolAddress of the static scratch: %s", cudaGetErrorString(e));
-      g_scratch_addr[dev] = p;
-    }
-    base = g_scratch_addr[dev];
-  }
+  const ft_status st = scratch_base(&base);
+  if (st != FT_OK) return st;
   int32_t* w = static_cast<int32_t*>(base);
-  int32_t* hdr = w;
+  int32_t* status = w;
+  int32_t* hdr = w + kStatusWords;
   int32_t* unique_slot = hdr + PH_WORDS;
   int32_t* u_offset = unique_slot + num_experts;
   int32_t* rows_by_u = u_offset + num_experts + 1;
@@ -163,10 +187,27 @@ extern "C" ft_status ft_moe_decode_ffn_static(int32_t hidden, int32_t inter, int
   f.expert_bytes = (long long)eb;
   f.H = hidden; f.I = inter; f.k = top_k; f.T = T; f.wdtype = wdtype; f.h = h;
   f.max_unique = (int)std::min<long long>(rows, num_experts);
-  f.status = hdr + PH_STATUS;
+  f.status = status;
   if ((e = launch_decode_gateup(f, s)) != cudaSuccess)
     return set_error(FT_ERR_CUDA, "gate/up launch: %s", cudaGetErrorString(e));
   if ((e = launch_decode_down(f, s)) != cudaSuccess)
     return set_error(FT_ERR_CUDA, "down launch: %s", cudaGetErrorString(e));
   return FT_OK;
+}
+
+extern "C" ft_status ft_moe_decode_ffn_static_status(void* stream) {
+  void* base = nullptr;
+  ft_status st = scratch_base(&base);
+  if (st != FT_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return set_error(FT_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  int32_t word = 0;
+  e = cudaMemcpy(&word, base, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return set_error(FT_ERR_CUDA, "reading the static status word: %s", cudaGetErrorString(e));
+  if (word == FT_OK) return FT_OK;
+  const int32_t zero = 0;
+  e = cudaMemcpy(base, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return set_error(FT_ERR_CUDA, "clearing the static status word: %s", cudaGetErrorString(e));
+  return set_error((ft_status)word, "a static-scratch FFN call raised %s", ft_status_str((ft_status)word));
 }

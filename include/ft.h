@@ -287,17 +287,31 @@ ft_status ft_get_timing(ft_cache* cache, ft_timing* out);
  *   y            device [T][hidden] float32
  *   stream       cudaStream_t (void*), NULL = legacy default stream
  * Asynchronous on `stream`.  Working memory is one static 1 MiB device array
- * per GPU, reserved when the library loads and kept until the process exits;
- * the first call on a device looks up its address (make that first call
- * before any stream capture).  Limits: T <= 8, and T*top_k*inter*4 bytes of
- * intermediate within 1,032,192 bytes (T*top_k <= 64 at inter 4096); larger
- * sizes return FT_ERR_INVALID_ARG with a message.  All calls share the array:
- * calls whose kernels overlap on the GPU (other streams or threads) race.
+ * per GPU.  With lazy module loading (the CUDA default) it is reserved on a
+ * GPU at the first call there, where a failure to reserve it is reported, and
+ * kept until the process exits (with CUDA_MODULE_LOADING=EAGER it is reserved
+ * when the library loads).  A caller whose memory planner then takes all
+ * device memory should make one warm-up call first.  That first call on a
+ * device (and the first after the current context changes) also looks up the
+ * array's address: make it before any stream capture.  Limits: T <= 8,
+ * hidden % 8 == 0, and T*top_k*inter*4 bytes of intermediate within 1,032,192
+ * bytes (T*top_k <= 64 at inter 4096); other sizes return FT_ERR_INVALID_ARG
+ * with a message, before any GPU work.  All calls share the array: calls whose
+ * kernels overlap on the GPU (other streams or threads) race.  A bounded wait
+ * that runs out inside the kernels leaves y incomplete and sets a sticky
+ * status word in the array; read it with ft_moe_decode_ffn_static_status.
  */
 ft_status ft_moe_decode_ffn_static(int32_t hidden, int32_t inter, int32_t wdtype, int32_t num_experts,
                                    int32_t top_k, const void* slot_pool, int64_t num_slots,
                                    const int32_t* expert_slot, const int32_t* topk_idx, const float* topk_w,
                                    const void* x, int32_t T, void* y, void* stream);
+
+/* Status of the static-scratch FFN calls on the current device: waits for
+ * `stream` (cudaStream_t as void*, NULL = legacy default stream), then returns
+ * FT_ERR_TIMEOUT if a kernel of an earlier ft_moe_decode_ffn_static call gave
+ * up a bounded wait (its y is incomplete), else FT_OK.  Reading clears the
+ * word.  Allocates nothing.  Synchronous. */
+ft_status ft_moe_decode_ffn_static_status(void* stream);
 
 /*
  * Step graphs: one decode/prefill step of all L layers captured into a CUDA
