@@ -47,7 +47,9 @@ class ft_stats(ctypes.Structure):
 class ft_timing(ctypes.Structure):
     _fields_ = [("route_ms", ctypes.c_double), ("route_n", ctypes.c_int64),
                 ("fetch_ms", ctypes.c_double), ("fetch_n", ctypes.c_int64),
-                ("ffn_ms", ctypes.c_double), ("ffn_n", ctypes.c_int64)]
+                ("ffn_ms", ctypes.c_double), ("ffn_n", ctypes.c_int64),
+                ("gemm1_ms", ctypes.c_double), ("gemm1_n", ctypes.c_int64),
+                ("gemm2_ms", ctypes.c_double), ("gemm2_n", ctypes.c_int64)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -112,6 +112,15 @@ struct PhaseTimer {
     cudaEventRecord(ev[2 * used + 1], s);
     ++used;
   }
+  // The next pair, for a caller that records both events itself.
+  bool reserve(cudaEvent_t* b, cudaEvent_t* e) {
+    if (!ensure()) return false;
+    if (used == kPairs) fold(kPairs / 2);
+    *b = ev[2 * used];
+    *e = ev[2 * used + 1];
+    ++used;
+    return true;
+  }
   void collect() { fold(used); }
   void reset() {
     collect();
@@ -120,7 +129,7 @@ struct PhaseTimer {
   }
 };
 
-enum { PHASE_ROUTE = 0, PHASE_FETCH, PHASE_FFN, PHASE_COUNT };
+enum { PHASE_ROUTE = 0, PHASE_FETCH, PHASE_FFN, PHASE_GEMM1, PHASE_GEMM2, PHASE_COUNT };
 
 }  // namespace
 
@@ -743,19 +752,22 @@ ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, v
   const Plan& pl = c->plans[layer];
   if (T > kDecodeMaxTokens) {  // prefill: grouped GEMMs
     if (!c->pf_yp)
-      return fail(FT_ERR_UNSUPPORTED, "T=%d > %d: the prefill path needs bf16 weights (H %% 128, I %% 64)", T,
+      return fail(FT_ERR_UNSUPPORTED, "T=%d > %d: the prefill path needs bf16 weights (H %% 128, I %% 128)", T,
                   kDecodeMaxTokens);
     PrefillArgs p{};
     p.hdr = pl.hdr; p.unique_expert = pl.unique_expert; p.unique_slot = pl.unique_slot; p.u_offset = pl.u_offset;
     p.topk_idx = pl.topk_idx; p.topk_w = pl.topk_w; p.rows_by_u = pl.rows_by_u; p.pos = c->pf_pos;
     p.x = x; p.h = c->pf_h; p.yp = c->pf_yp; p.y = static_cast<float*>(y);
     p.pool = static_cast<const uint8_t*>(c->pool); p.expert_bytes = (long long)c->eb;
-    p.H = c->H; p.I = c->I; p.k = c->k; p.T = T; p.E = c->E;
+    p.H = c->H; p.I = c->I; p.k = c->k; p.T = T; p.E = c->E; p.status = c->tab.status;
     const bool tm = c->timing;
     if (tm) c->timers[PHASE_FFN].begin(c->compute);
     if (c->cap_ffn_ev) CU(cudaEventRecordWithFlags(c->cap_ffn_ev[2 * layer], c->compute, cudaEventRecordExternal));
     int n = 0;
-    const cudaError_t e = launch_prefill_ffn(p, c->compute, &n);
+    cudaEvent_t marks[4] = {};
+    const bool gm = tm && c->timers[PHASE_GEMM1].reserve(&marks[0], &marks[1]) &&
+                    c->timers[PHASE_GEMM2].reserve(&marks[2], &marks[3]);
+    const cudaError_t e = launch_prefill_ffn(p, (int)c->C, c->compute, &n, gm ? marks : nullptr);
     if (e != cudaSuccess) return fail(FT_ERR_CUDA, "prefill FFN launch: %s", cudaGetErrorString(e));
     c->launches += n;
     if (c->cap_ffn_ev) CU(cudaEventRecordWithFlags(c->cap_ffn_ev[2 * layer + 1], c->compute, cudaEventRecordExternal));
@@ -980,6 +992,8 @@ ft_status ft_get_timing(ft_cache* c, ft_timing* out) {
   out->route_ms = c->timers[PHASE_ROUTE].total_ms; out->route_n = c->timers[PHASE_ROUTE].n;
   out->fetch_ms = c->timers[PHASE_FETCH].total_ms; out->fetch_n = c->timers[PHASE_FETCH].n;
   out->ffn_ms = c->timers[PHASE_FFN].total_ms; out->ffn_n = c->timers[PHASE_FFN].n;
+  out->gemm1_ms = c->timers[PHASE_GEMM1].total_ms; out->gemm1_n = c->timers[PHASE_GEMM1].n;
+  out->gemm2_ms = c->timers[PHASE_GEMM2].total_ms; out->gemm2_n = c->timers[PHASE_GEMM2].n;
   return FT_OK;
 }
 

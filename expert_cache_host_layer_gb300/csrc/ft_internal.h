@@ -157,10 +157,17 @@ struct PrefillArgs {
   float* y;                  // [T][H] fp32 out
   const uint8_t* pool;
   long long expert_bytes;
+  int32_t* status;           // sticky status word (bounded waits record FT_ERR_TIMEOUT)
   int H, I, k, T, E;
 };
 bool prefill_supported(int H, int I, int wdtype, int E);
-cudaError_t launch_prefill_ffn(const PrefillArgs& a, cudaStream_t s, int* launches);
+// marks (optional): events recorded before and after the gate/up GEMM, then
+// before and after the down GEMM.
+cudaError_t launch_prefill_ffn(const PrefillArgs& a, int num_slots, cudaStream_t s, int* launches,
+                               const cudaEvent_t* marks);
+// The two grouped GEMMs of the prefill path on tcgen05 (prefill_tc.cu).
+bool prefill_tc_supported(int H, int I);
+cudaError_t launch_prefill_gemms(const PrefillArgs& a, int num_slots, cudaStream_t s, const cudaEvent_t* marks);
 
 // Decode path: the gate/up+SwiGLU kernel, then the down+combine kernel.
 cudaError_t launch_decode_gateup(const FfnArgs& a, cudaStream_t s);

@@ -1,0 +1,551 @@
+// Prefill-path grouped expert GEMMs on the 5th-generation tensor cores
+// (tcgen05, sm_103a): the gate/up + SwiGLU GEMM and the down GEMM of the
+// routed SwiGLU experts, reading the weights straight from their cache slots.
+//
+//   gate/up:  h[p][i]  = silu(Wg[i] . x_t) * (Wu[i] . x_t)   bf16 h, p = grouped row of (t, j)
+//   down:     yp[p][c] = w_tj * (Wd[c] . h[p])               fp32
+//
+// A tile is 128 grouped rows of one expert (M) by a block of output columns
+// (N); a persistent grid walks the tiles in (m-tile, n-tile) order, m-tiles
+// expert by expert.  Every CTA runs three roles:
+//   warp 0      TMA producer: the A rows and the B rows of each 64-wide K
+//               block into a 4-stage shared-memory ring, 128-byte swizzled.
+//               Gate/up gathers its A rows (the x rows of the tile's tokens)
+//               with tile::gather4 copies, four rows per lane; the down GEMM
+//               reads its A rows (h, already grouped) as one 2D box.  The B
+//               rows come from the slot pool viewed as one 2D tensor whose
+//               rows are weight rows: Wg/Wu rows for gate/up, Wd rows for down.
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
+//               and one thread issues tcgen05.mma (M 128, N 256, K 16, bf16 in,
+//               fp32 accumulate), four per K block; tcgen05.commit frees each
+//               ring stage, and marks an accumulator full after its last block.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32 (w % 4) ..), SwiGLU or the gate weight, global stores;
+//               then the accumulator is handed back, so the epilogue of one
+//               tile overlaps the MMAs of the next.
+// The gate/up B tile is 128 Wg rows followed by the same 128 Wu rows, so the
+// accumulator's columns [0, 128) are gate and [128, 256) up for the same 128 h
+// columns and SwiGLU needs no data exchange.
+//
+// Every mbarrier wait is bounded (one second of %globaltimer).  A wait that
+// runs out records FT_ERR_TIMEOUT and sets a CTA-wide abort flag that ends
+// every later wait at once; the producer still waits (bounded) for the copies
+// it issued, the MMA thread for its MMAs, and TMEM is freed before the CTA
+// exits.
+//
+// The grouped SwiGLU expert and its gate-weighted combine follow the routed
+// experts of the MoE layers the pages serve ("FreeToken vs vLLM on one RTX
+// 3090", "Why the performance differs"; the 16k-token prefill chunk of
+// "FreeToken: Efficient Edge-Native MoE Serving ...", ablation paragraph).
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+#include <set>
+
+#include "driver_api.h"
+#include "ft_internal.h"
+
+namespace ft {
+namespace {
+
+constexpr int kTcThreads = 192;          // 6 warps: producer, MMA, 4 x epilogue
+constexpr int kBM = 128;                 // grouped rows per tile (UMMA M)
+constexpr int kBK = 64;                  // K per ring stage: one 128-byte swizzle row of bf16
+constexpr int kStages = 4;
+constexpr int kN1 = 256;                 // gate/up UMMA N: 128 gate + 128 up columns
+constexpr int kH1 = kN1 / 2;             // h columns per gate/up tile
+constexpr int kAccCols = 256;            // TMEM columns per accumulator
+constexpr int kTmemCols = 512;           // two accumulators
+constexpr int kABytes = kBM * kBK * 2;   // 16 KB
+constexpr int kBBytesMax = 256 * kBK * 2;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytesMax;
+constexpr int kTableInts = 3 * (kMaxExperts + 1);
+constexpr unsigned long long kWaitNs = 1000000000ull;
+
+// Dynamic shared memory: [ring (1024-aligned)][tile table][barriers].
+constexpr int kRingBytes = kStages * kStageBytes;
+constexpr int kTableOff = kRingBytes;
+constexpr int kBarOff = (kTableOff + kTableInts * 4 + 15) / 16 * 16;
+constexpr int kBarWords = 2 * kStages + 2 * 2 + 1;  // full, empty, tfull, tempty, drain
+constexpr int kTcSmem = kBarOff + kBarWords * 8 + 16 + 1024;  // + tmem holder, abort flag, alignment slack
+
+struct TcArgs {
+  const int32_t* hdr;
+  const int32_t* u_offset;     // [n_u + 1]
+  const int32_t* unique_slot;  // [n_u]
+  const int32_t* rows_by_u;    // [R] row ids t*k + j in grouped order
+  const float* topk_w;         // [R]
+  __nv_bfloat16* h;            // [R][I]
+  float* yp;                   // [R][H]
+  int32_t* status;
+  int H, I, k, R;
+  int n_tile;                  // UMMA N of this GEMM (gate/up 256; down 256 or 128)
+  long long slot_rows;         // rows of one slot in the B tensor map (3I for gate/up, 3H for down)
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t sa(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ unsigned long long now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(sa(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(b)) : "memory");
+}
+// Bounded wait; gives up at once when the CTA has aborted (unless `drain`),
+// and aborts the CTA when the limit runs out.
+__device__ __forceinline__ bool bwait(uint64_t* b, uint32_t parity, int32_t* status, volatile int* abort_flag,
+                                      bool drain = false) {
+  if (bar_try(b, parity)) return true;
+  const unsigned long long t0 = now_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (bar_try(b, parity)) return true;
+    if (!drain && *abort_flag) return false;
+    if (now_ns() - t0 > kWaitNs) {
+      if (status) atomicCAS(status, 0, (int)FT_ERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(sa(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(sa(bar))
+      : "memory");
+}
+// Four rows r0..r3 of a 2D tensor (box one row high), columns [c0, c0 + box).
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int c0, int r0, int r1, int r2, int r3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(sa(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(sa(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(sa(bar))
+               : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, both K-major, described by 64-bit
+// shared-memory matrix descriptors; `idesc` holds the shapes and types.
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile whose rows are
+// 128 bytes, written by TMA with the 128-byte swizzle: 8-row groups 1024 bytes
+// apart (stride byte offset), descriptor version 1, swizzle mode 128B.  The
+// leading byte offset is not used by this layout.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;              // leading byte offset (16 B; unused here)
+  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
+  d |= (uint64_t)1 << 46;              // version
+  d |= (uint64_t)2 << 61;              // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+struct Smem {
+  uint8_t* ring;
+  int* s_off;
+  int* s_pre;
+  int* s_slot;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* tfull;
+  uint64_t* tempty;
+  uint64_t* drain;
+  uint32_t* tmem_holder;
+  volatile int* abort_flag;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t* raw) {
+  Smem s;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  s.ring = base;
+  s.s_off = reinterpret_cast<int*>(base + kTableOff);
+  s.s_pre = s.s_off + (kMaxExperts + 1);
+  s.s_slot = s.s_pre + (kMaxExperts + 1);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kBarOff);
+  s.full = bars;
+  s.empty = bars + kStages;
+  s.tfull = bars + 2 * kStages;
+  s.tempty = bars + 2 * kStages + 2;
+  s.drain = bars + 2 * kStages + 4;
+  s.tmem_holder = reinterpret_cast<uint32_t*>(bars + kBarWords);
+  s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_holder + 1);
+  return s;
+}
+
+// Tile table: s_off = u_offset, s_pre[u] = m-tiles of the experts before u,
+// s_slot = slot of each unique expert; warp 0 scans.  Returns the m-tile total.
+__device__ int build_table(const TcArgs& a, int n_u, const Smem& s) {
+  for (int u = threadIdx.x; u <= n_u; u += blockDim.x) s.s_off[u] = __ldg(&a.u_offset[u]);
+  for (int u = threadIdx.x; u < n_u; u += blockDim.x) s.s_slot[u] = __ldg(&a.unique_slot[u]);
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (n_u + 31) / 32;
+    const int u0 = min(n_u, lane * per), u1 = min(n_u, u0 + per);
+    int local = 0;
+    for (int u = u0; u < u1; ++u) local += (s.s_off[u + 1] - s.s_off[u] + kBM - 1) / kBM;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int acc = incl - local;
+    for (int u = u0; u < u1; ++u) {
+      s.s_pre[u] = acc;
+      acc += (s.s_off[u + 1] - s.s_off[u] + kBM - 1) / kBM;
+    }
+    if (lane == 31) s.s_pre[n_u] = incl;
+  }
+  __syncthreads();
+  return s.s_pre[n_u];
+}
+
+__device__ __forceinline__ int tile_expert(const int* s_pre, int n_u, int mt) {
+  int lo = 0, hi = n_u - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_pre[mid] <= mt) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct TileInfo {
+  int u, p0, pend, n0, slot;
+};
+__device__ __forceinline__ TileInfo tile_info(const Smem& s, int n_u, int ntiles, int tile, int n_cols) {
+  TileInfo t;
+  const int mt = tile / ntiles, nt = tile - mt * ntiles;
+  t.u = tile_expert(s.s_pre, n_u, mt);
+  t.p0 = s.s_off[t.u] + (mt - s.s_pre[t.u]) * kBM;
+  t.pend = s.s_off[t.u + 1];
+  t.n0 = nt * n_cols;
+  t.slot = s.s_slot[t.u];
+  return t;
+}
+
+// kGateUp: the gate/up + SwiGLU GEMM (A = gathered x rows via map_a with a
+// one-row box, B = Wg/Wu rows); else the down GEMM (A = h rows via map_a with
+// a 128-row box, B = Wd rows).
+template <bool kGateUp>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const Smem s = carve(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_u = min(__ldg(&a.hdr[PH_UNIQUE]), kMaxExperts);
+  const int N = kGateUp ? kN1 : a.n_tile;           // UMMA N
+  const int n_cols = kGateUp ? kH1 : a.n_tile;      // output columns per tile
+  const int ntiles = (kGateUp ? a.I : a.H) / n_cols;
+  const int KT = (kGateUp ? a.H : a.I) / kBK;
+  const uint32_t b_bytes = (uint32_t)N * kBK * 2;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      bar_init(&s.full[i], 1);
+      bar_init(&s.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      bar_init(&s.tfull[i], 1);
+      bar_init(&s.tempty[i], 4);
+    }
+    bar_init(s.drain, 1);
+    *s.abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {  // the whole warp allocates the two accumulators
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sa(s.tmem_holder)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  const int mtiles = build_table(a, n_u, s);  // contains __syncthreads: barriers and TMEM base are visible after it
+  tc_fence_after();
+  const uint32_t tmem = *s.tmem_holder;
+  const int total = mtiles * ntiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_b)) : "memory");
+    }
+    int it = 0;
+    bool go = true;
+    for (int tile = blockIdx.x; tile < total && go; tile += gridDim.x) {
+      const TileInfo t = tile_info(s, n_u, ntiles, tile, n_cols);
+      int tok[4];
+      if (kGateUp) {  // the x rows of this lane's four grouped rows (a valid row past the expert's last)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int p = t.p0 + 4 * lane + i;
+          tok[i] = p < t.pend ? __ldg(&a.rows_by_u[p]) / a.k : 0;
+        }
+      }
+      const long long brow = (long long)t.slot * a.slot_rows + (kGateUp ? t.n0 : 2LL * a.H + t.n0);
+      for (int kt = 0; kt < KT; ++kt, ++it) {
+        const int st = it % kStages;
+        bool ok = true;
+        if (lane == 0) ok = bwait(&s.empty[st], ((it / kStages) & 1) ^ 1, a.status, s.abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          go = false;
+          break;
+        }
+        bar_try(&s.empty[st], ((it / kStages) & 1) ^ 1);  // every lane observes the freed stage itself
+        uint8_t* A = s.ring + st * kStageBytes;
+        uint8_t* B = A + kABytes;
+        if (lane == 0) bar_expect_tx(&s.full[st], kABytes + b_bytes);
+        __syncwarp();
+        const int c0 = kt * kBK;
+        if (kGateUp) {
+          tma_gather4(A + lane * 4 * 128, &map_a, c0, tok[0], tok[1], tok[2], tok[3], &s.full[st]);
+          if (lane == 0) {
+            tma_2d(B, &map_b, c0, (int)brow, &s.full[st]);                         // 128 Wg rows
+            tma_2d(B + kBM * 128, &map_b, c0, (int)(brow + a.I), &s.full[st]);    // the same 128 Wu rows
+          }
+        } else if (lane == 0) {
+          tma_2d(A, &map_a, c0, t.p0, &s.full[st]);                              // 128 h rows
+          tma_2d(B, &map_b, c0, (int)brow, &s.full[st]);                         // N Wd rows
+        }
+      }
+    }
+    // no copy may still be writing this CTA's shared memory when it exits
+    if (lane == 0)
+      for (int j = it - kStages < 0 ? 0 : it - kStages; j < it; ++j)
+        bwait(&s.full[j % kStages], (j / kStages) & 1, a.status, s.abort_flag, true);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kBM, N);
+      int it = 0, j = 0;
+      bool go = true;
+      for (int tile = blockIdx.x; tile < total && go; tile += gridDim.x, ++j) {
+        const int acc = j & 1;
+        if (!bwait(&s.tempty[acc], ((j >> 1) & 1) ^ 1, a.status, s.abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * kAccCols;
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          const int st = it % kStages;
+          if (!bwait(&s.full[st], (it / kStages) & 1, a.status, s.abort_flag)) {
+            go = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t A = sa(s.ring + st * kStageBytes), B = A + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)  // K 16 per MMA: 32 bytes along the swizzled row
+            tc_mma(d, sw128_desc(A + kk * 32), sw128_desc(B + kk * 32), idesc, (kt | kk) != 0);
+          tc_commit(&s.empty[st]);  // the stage is free once these MMAs have read it
+        }
+        if (go) tc_commit(&s.tfull[acc]);
+      }
+      // every MMA this thread issued has completed before TMEM is freed
+      tc_commit(s.drain);
+      bwait(s.drain, 0, a.status, s.abort_flag, true);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;            // TMEM lanes 32q .. 32q + 31
+    const int row = q * 32 + lane;     // tile row of this thread
+    int j = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++j) {
+      const int acc = j & 1;
+      bool ok = true;
+      if (lane == 0) ok = bwait(&s.tfull[acc], (j >> 1) & 1, a.status, s.abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      bar_try(&s.tfull[acc], (j >> 1) & 1);  // every lane observes the completed phase itself
+      tc_fence_after();
+      const TileInfo t = tile_info(s, n_u, ntiles, tile, n_cols);
+      const int p = t.p0 + row;
+      const bool live = p < t.pend;
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
+      if (kGateUp) {
+        __nv_bfloat16* hrow = a.h + (long long)(live ? p : 0) * a.I + t.n0;
+        for (int c = 0; c < kH1; c += 32) {
+          float g[32], u[32];
+          tc_ld32(tbase + c, g);
+          tc_ld32(tbase + kH1 + c, u);
+          if (live) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float h0 = g[2 * i] / (1.0f + expf(-g[2 * i])) * u[2 * i];
+              const float h1 = g[2 * i + 1] / (1.0f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+              const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
+              packed[i] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(hrow + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          }
+        }
+      } else {
+        const float wt = live ? __ldg(&a.topk_w[__ldg(&a.rows_by_u[p])]) : 0.0f;
+        float* yrow = a.yp + (long long)(live ? p : 0) * a.H + t.n0;
+        for (int c = 0; c < n_cols; c += 32) {
+          float v[32];
+          tc_ld32(tbase + c, v);
+          if (live) {
+            float4* dst = reinterpret_cast<float4*>(yrow + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(wt * v[4 * i], wt * v[4 * i + 1], wt * v[4 * i + 2], wt * v[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) bar_arrive(&s.tempty[acc]);  // this warp's quarter of the accumulator is read
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// A 2D bf16 tensor map, `cols` x `rows` (cols innermost, row pitch `pitch`
+// bytes), box `box_cols` x `box_rows`, 128-byte swizzle, zero fill outside.
+cudaError_t bf16_map(CUtensorMap* m, const void* base, unsigned long long cols, unsigned long long rows,
+                     unsigned long long pitch, uint32_t box_cols, uint32_t box_rows) {
+  static EncodeTiled enc = nullptr;
+  if (!enc) enc = reinterpret_cast<EncodeTiled>(driver_fn("cuTensorMapEncodeTiled"));
+  if (!enc) return cudaErrorNotSupported;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (pitch & 15)) return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {pitch};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int tc_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+  }
+  return n;
+}
+
+}  // namespace
+
+bool prefill_tc_supported(int H, int I) {
+  return H % 128 == 0 && I % kH1 == 0 && H % kBK == 0 && I % kBK == 0;
+}
+
+cudaError_t launch_prefill_gemms(const PrefillArgs& p, int num_slots, cudaStream_t st, const cudaEvent_t* marks) {
+  static std::mutex mu;
+  static std::set<int> ready;  // devices whose kernel attributes are set
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ready.count(dev)) {
+      e = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+      if (e != cudaSuccess) return e;
+      ready.insert(dev);
+    }
+  }
+  const int H = p.H, I = p.I, R = p.T * p.k;
+  TcArgs a{};
+  a.hdr = p.hdr; a.u_offset = p.u_offset; a.unique_slot = p.unique_slot; a.rows_by_u = p.rows_by_u;
+  a.topk_w = p.topk_w; a.h = static_cast<__nv_bfloat16*>(p.h); a.yp = p.yp; a.status = p.status;
+  a.H = H; a.I = I; a.k = p.k; a.R = R;
+  CUtensorMap mx, mw1, mh, mwd;
+  // x [T][H]: one-row boxes for the gathered A rows
+  if ((e = bf16_map(&mx, p.x, H, p.T, 2ull * H, kBK, 1)) != cudaSuccess) return e;
+  // the pool as rows of H: Wg rows [s*3I, s*3I + I), Wu rows [s*3I + I, s*3I + 2I)
+  if ((e = bf16_map(&mw1, p.pool, H, 3ull * I * num_slots, 2ull * H, kBK, kBM)) != cudaSuccess) return e;
+  // h [R][I]
+  if ((e = bf16_map(&mh, p.h, I, R, 2ull * I, kBK, kBM)) != cudaSuccess) return e;
+  // the pool as rows of I: Wd rows [s*3H + 2H, s*3H + 3H)
+  const int n2 = H % 256 == 0 ? 256 : 128;
+  if ((e = bf16_map(&mwd, p.pool, I, 3ull * H * num_slots, 2ull * I, kBK, n2)) != cudaSuccess) return e;
+  const int grid = tc_sms();
+  a.n_tile = kN1;
+  a.slot_rows = 3LL * I;
+  if (marks && (e = cudaEventRecord(marks[0], st)) != cudaSuccess) return e;
+  tc_gemm_kernel<true><<<grid, kTcThreads, kTcSmem, st>>>(mx, mw1, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (marks && (e = cudaEventRecord(marks[1], st)) != cudaSuccess) return e;
+  a.n_tile = n2;
+  a.slot_rows = 3LL * H;
+  if (marks && (e = cudaEventRecord(marks[2], st)) != cudaSuccess) return e;
+  tc_gemm_kernel<false><<<grid, kTcThreads, kTcSmem, st>>>(mh, mwd, a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (marks && (e = cudaEventRecord(marks[3], st)) != cudaSuccess) return e;
+  return cudaSuccess;
+}
+
+}  // namespace ft

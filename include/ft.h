@@ -125,6 +125,8 @@ typedef struct ft_timing {
   double route_ms;  int64_t route_n;   /* route_classify kernel, compute stream */
   double fetch_ms;  int64_t fetch_n;   /* miss copies, copy stream (first to last copy of a layer) */
   double ffn_ms;    int64_t ffn_n;     /* expert FFN kernels of one ft_moe_forward, compute stream */
+  double gemm1_ms;  int64_t gemm1_n;   /* prefill forwards: the gate/up + SwiGLU tensor-core GEMM alone */
+  double gemm2_ms;  int64_t gemm2_n;   /* prefill forwards: the down tensor-core GEMM alone */
 } ft_timing;
 
 /* Header of one layer's plan (see ft_get_plan). */

@@ -87,9 +87,9 @@ def run_parity(w: W.Workload, steps: int | None = None, fetch_mode: int = 1, dou
                ffn_tokens=None):
     """Run `steps` steps of workload w through libft and the oracle.
 
-    ffn_tokens: compare the FFN output on these token rows only (the oracle FFN
-    of a 16,384-token chunk would take too long); decisions are always
-    compared in full.  Returns a report dict; raises AssertionError on the
+    ffn_tokens: compare the FFN output on these token rows only; a callable
+    ffn_tokens(layer, topk_idx) returns the rows for that layer event (None:
+    every row).  Decisions are always compared in full.  Returns a report dict; raises AssertionError on the
     first mismatch.
     """
     from expert_cache_host_layer_gb300.pipeline import ExpertCache
@@ -149,7 +149,8 @@ def run_parity(w: W.Workload, steps: int | None = None, fetch_mode: int = 1, dou
                 t = refs[l][2].t
                 if ffn_every and t % ffn_every == 0:
                     ridx, rw, ev = refs[l]
-                    tok = np.arange(T) if ffn_tokens is None else np.asarray(ffn_tokens)
+                    sel = ffn_tokens(l, ridx) if callable(ffn_tokens) else ffn_tokens
+                    tok = np.arange(T) if sel is None else np.asarray(sel)
                     yr = oracle_ffn(w, bank, n_blobs, l, xs_h[l][tok], ridx[tok], rw[tok])
                     yg = ys[l].float().cpu().numpy()[tok]
                     mx, rm = ffn_error(yg, yr)

@@ -1,12 +1,15 @@
 """Prefill layer events (T > 8 tokens) through libft against the oracle.
 
 The prefill path groups the chunk's T*k (token, pick) rows by expert and runs
-the gate/up + SwiGLU and down projections as grouped tensor-core GEMMs that
-read the weights from the cache slots, then combines each token's picks.  The
-routing, dedup, hit/miss and LRU decisions of the chunk are compared in full;
-the FFN output on every token of a 200-token chunk (ragged against the
-128-row tiles; T*k above what the route kernel groups itself) and on sampled
-tokens of the full 16,384-token chunk.  Both with the next layer's fetch
+the gate/up + SwiGLU and down projections as grouped tcgen05 GEMMs that read
+the weights from the cache slots, then combines each token's picks.  The
+routing, dedup, hit/miss and LRU decisions of the chunk are compared in full.
+The FFN output is compared on every token of a 200-token chunk (ragged
+against the 128-row tiles; T*k above what the route kernel groups itself),
+and on the full 16,384-token chunk: every row of its first layer, and on the
+second layer 512 seeded tokens plus every token that picked the layer's
+rarest expert (the expert with the fewest rows, whose single ragged tile is
+the likeliest to be mishandled).  Both with the next layer's fetch
 double-buffered and without.
 """
 import numpy as np
@@ -26,13 +29,24 @@ def test_prefill_chunk_full_parity(double_buffer):
     print("prefill 200:", {k: rep[k] for k in ("max_err", "miss_rate")})
 
 
+def sampled_tokens(layer, idx, T=W.QWEN35B_PREFILL.tokens):
+    """Layer 0: every token.  Other layers: 512 seeded tokens plus every token
+    whose top-k holds the rarest unique expert."""
+    if layer == 0:
+        return None
+    experts, counts = np.unique(idx, return_counts=True)
+    rare = experts[np.argmin(counts)]
+    rng = np.random.default_rng(20261202 + layer)
+    tok = rng.choice(T, 512, replace=False)
+    tok = np.union1d(tok, np.flatnonzero((idx == rare).any(axis=1)))
+    return np.union1d(tok, [0, T - 1])
+
+
 @pytest.mark.parametrize("double_buffer", [True, False], ids=["double-buffered", "serial"])
 def test_prefill_16k_chunk(double_buffer):
     from tests.harness import run_parity
     w = W.QWEN35B_PREFILL.replace(num_layers=2)
-    rng = np.random.default_rng(20261202)
-    tok = np.unique(np.concatenate([[0, w.tokens - 1], rng.choice(w.tokens, 10, replace=False)]))
-    rep = run_parity(w, steps=1, bank_blobs=512, double_buffer=double_buffer, ffn_tokens=tok)
+    rep = run_parity(w, steps=1, bank_blobs=512, double_buffer=double_buffer, ffn_tokens=sampled_tokens)
     assert rep["events"] == 2 and rep["ffn_checked"] == 2
     assert rep["stats"]["unique_experts"] > 300  # nearly all 256 experts per layer
-    print("prefill 16k:", {k: rep[k] for k in ("max_err", "miss_rate")})
+    print("prefill 16k:", {k: rep[k] for k in ("max_err", "max_rms_err", "miss_rate")})
