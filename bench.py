@@ -58,6 +58,8 @@ def parse():
     p.add_argument("--prefill", action="store_true",
                    help="also measure the 16,384-token prefill chunk (40 layers) and report it under 'prefill'")
     p.add_argument("--trace", action="store_true", help="print one step's per-layer timeline to stderr")
+    p.add_argument("--prefill-gemm-only", action="store_true",
+                   help="only time the prefill chunk's two tensor-core GEMMs (all hits, no fetch) and print them")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--timing-steps", type=int, default=64,
                    help="steps of the second timed pass (graphs with per-phase events) for the roofline")
@@ -685,6 +687,10 @@ def run_ours(args, w):
 def main():
     args = parse()
     w = W.ALL[args.workload]
+    if args.prefill_gemm_only:
+        import torch
+        print(json.dumps(prefill_gemm_only(torch.device("cuda", 0), measured_bf16_tflops())), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args, w)
     else:

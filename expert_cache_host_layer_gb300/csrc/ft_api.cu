@@ -171,6 +171,7 @@ struct ft_cache {
   // prefill (T > kDecodeMaxTokens): bf16 h [rows][I], fp32 per-row outputs
   // [rows][H], grouped place of each row; allocated only when max_tokens > 8
   void* pf_h = nullptr;
+  void* pf_xp = nullptr;              // bf16 x rows in grouped order [rows][H]
   float* pf_yp = nullptr;
   int32_t* pf_pos = nullptr;
   unsigned* gbar = nullptr;           // grid-barrier words of the fused FFN kernel
@@ -475,6 +476,7 @@ ft_status ft_cache_destroy(ft_cache* c) {
   cudaFree(c->scr_mem);
   cudaFree(c->h_buf);
   cudaFree(c->pf_h);
+  cudaFree(c->pf_xp);
   cudaFree(c->pf_yp);
   cudaFree(c->pf_pos);
   cudaFree(c->gbar);
@@ -602,6 +604,7 @@ ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t n
     if (g.max_tokens > kDecodeMaxTokens && prefill_supported(c->H, c->I, c->wdtype, c->E)) {
       const long long prows = (long long)g.max_tokens * g.top_k;
       CU(cudaMalloc(&c->pf_h, sizeof(uint16_t) * prows * c->I));
+      CU(cudaMalloc(&c->pf_xp, sizeof(uint16_t) * prows * c->H));
       CU(cudaMalloc(&c->pf_yp, sizeof(float) * prows * c->H));
       CU(cudaMalloc(&c->pf_pos, sizeof(int32_t) * prows));
     }
@@ -757,7 +760,7 @@ ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, v
     PrefillArgs p{};
     p.hdr = pl.hdr; p.unique_expert = pl.unique_expert; p.unique_slot = pl.unique_slot; p.u_offset = pl.u_offset;
     p.topk_idx = pl.topk_idx; p.topk_w = pl.topk_w; p.rows_by_u = pl.rows_by_u; p.pos = c->pf_pos;
-    p.x = x; p.h = c->pf_h; p.yp = c->pf_yp; p.y = static_cast<float*>(y);
+    p.x = x; p.xp = c->pf_xp; p.h = c->pf_h; p.yp = c->pf_yp; p.y = static_cast<float*>(y);
     p.pool = static_cast<const uint8_t*>(c->pool); p.expert_bytes = (long long)c->eb;
     p.H = c->H; p.I = c->I; p.k = c->k; p.T = T; p.E = c->E; p.status = c->tab.status;
     const bool tm = c->timing;

@@ -152,6 +152,7 @@ struct PrefillArgs {
   int32_t* rows_by_u;        // [T*k] out: rows grouped by unique expert
   int32_t* pos;              // [T*k] out: grouped place of each row
   const void* x;             // [T][H] bf16
+  void* xp;                  // [T*k][H] bf16 scratch: the x row of each grouped row
   void* h;                   // [T*k][I] bf16 scratch
   float* yp;                 // [T*k][H] fp32 scratch
   float* y;                  // [T][H] fp32 out

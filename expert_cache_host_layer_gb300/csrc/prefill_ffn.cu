@@ -5,6 +5,8 @@
 //
 //   group_rows:  the T*k (token, pick) rows sorted by unique expert (ascending
 //                row within an expert): rows_by_u, and pos[row] = its place
+//   permute:     xp[p] = x[t] for the grouped row p of (t, j), so each GEMM
+//                tile's A rows are one contiguous block
 //   gate/up:     h[p][i] = silu(Wg[i] . x_t) * (Wu[i] . x_t)  (bf16 h; p the
 //                grouped place of row (t, j))
 //   down:        yp[p][c] = w_tj * (Wd[c] . h[p])              (fp32)
@@ -75,6 +77,21 @@ __global__ void __launch_bounds__(kPThreads) group_rows_kernel(PrefillArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- permute
+// One warp per grouped row: xp[p] = x[rows_by_u[p] / k], 16-byte chunks.
+__global__ void __launch_bounds__(kPThreads) permute_rows_kernel(PrefillArgs a) {
+  const int R = a.T * a.k, n16 = a.H / 8;
+  const int lane = threadIdx.x & 31;
+  const uint4* x = static_cast<const uint4*>(a.x);
+  uint4* xp = static_cast<uint4*>(a.xp);
+  for (int p = (blockIdx.x * kPThreads + threadIdx.x) >> 5; p < R; p += (gridDim.x * kPThreads) >> 5) {
+    const int t = __ldg(&a.rows_by_u[p]) / a.k;
+    const uint4* src = x + (long long)t * n16;
+    uint4* dst = xp + (long long)p * n16;
+    for (int i = lane; i < n16; i += 32) dst[i] = __ldg(src + i);
+  }
+}
+
 // ---------------------------------------------------------------- combine
 // y[t][c] = sum_{j<k} yp[pos[t*k+j]][c], four columns per thread.
 __global__ void __launch_bounds__(kPThreads) combine_kernel(PrefillArgs a) {
@@ -113,9 +130,11 @@ cudaError_t launch_prefill_ffn(const PrefillArgs& a, int num_slots, cudaStream_t
   group_rows_kernel<<<a.E, kPThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  permute_rows_kernel<<<8 * prefill_sms(), kPThreads, 0, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = launch_prefill_gemms(a, num_slots, s, marks)) != cudaSuccess) return e;
   combine_kernel<<<4 * prefill_sms(), kPThreads, 0, s>>>(a);
-  *launches = 4;
+  *launches = 5;
   return cudaGetLastError();
 }
 

@@ -9,19 +9,19 @@
 // (N); a persistent grid walks the tiles in (m-tile, n-tile) order, m-tiles
 // expert by expert.  Every CTA runs three roles:
 //   warp 0      TMA producer: the A rows and the B rows of each 64-wide K
-//               block into a 4-stage shared-memory ring, 128-byte swizzled.
-//               Gate/up gathers its A rows (the x rows of the tile's tokens)
-//               with tile::gather4 copies, four rows per lane; the down GEMM
-//               reads its A rows (h, already grouped) as one 2D box.  The B
+//               block into a 3-stage shared-memory ring, 128-byte swizzled.
+//               The A rows are one 2D box of 128 grouped rows: x rows already
+//               permuted into grouped order (gate/up) or h (down).  The B
 //               rows come from the slot pool viewed as one 2D tensor whose
 //               rows are weight rows: Wg/Wu rows for gate/up, Wd rows for down.
 //   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
 //               and one thread issues tcgen05.mma (M 128, N 256, K 16, bf16 in,
 //               fp32 accumulate), four per K block; tcgen05.commit frees each
 //               ring stage, and marks an accumulator full after its last block.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//               lanes 32 (w % 4) ..), SwiGLU or the gate weight, global stores;
-//               then the accumulator is handed back, so the epilogue of one
+//   warps 2-9   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32 (w % 4) .. and half of the columns), SwiGLU or the
+//               gate weight, then TMA stores of 32-row boxes staged in shared
+//               memory; the accumulator is handed back, so the epilogue of one
 //               tile overlaps the MMAs of the next.
 // The gate/up B tile is 128 Wg rows followed by the same 128 Wu rows, so the
 // accumulator's columns [0, 128) are gate and [128, 256) up for the same 128 h
@@ -49,10 +49,11 @@
 namespace ft {
 namespace {
 
-constexpr int kTcThreads = 192;          // 6 warps: producer, MMA, 4 x epilogue
+constexpr int kEpiWarps = 8;             // two per TMEM lane quarter, each taking half the columns
+constexpr int kTcThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue
 constexpr int kBM = 128;                 // grouped rows per tile (UMMA M)
 constexpr int kBK = 64;                  // K per ring stage: one 128-byte swizzle row of bf16
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kN1 = 256;                 // gate/up UMMA N: 128 gate + 128 up columns
 constexpr int kH1 = kN1 / 2;             // h columns per gate/up tile
 constexpr int kAccCols = 256;            // TMEM columns per accumulator
@@ -63,9 +64,13 @@ constexpr int kStageBytes = kABytes + kBBytesMax;
 constexpr int kTableInts = 3 * (kMaxExperts + 1);
 constexpr unsigned long long kWaitNs = 1000000000ull;
 
-// Dynamic shared memory: [ring (1024-aligned)][tile table][barriers].
+// Dynamic shared memory: [ring (1024-aligned)][output staging][tile table][barriers].
+// Each epilogue warp owns two 4 KB staging boxes (32 rows x 128 bytes, the
+// layout of a 128-byte-swizzled TMA store box), used alternately.
 constexpr int kRingBytes = kStages * kStageBytes;
-constexpr int kTableOff = kRingBytes;
+constexpr int kBoxBytes = 32 * 128;
+constexpr int kStageOutOff = kRingBytes;
+constexpr int kTableOff = kStageOutOff + kEpiWarps * 2 * kBoxBytes;
 constexpr int kBarOff = (kTableOff + kTableInts * 4 + 15) / 16 * 16;
 constexpr int kBarWords = 2 * kStages + 2 * 2 + 1;  // full, empty, tfull, tempty, drain
 constexpr int kTcSmem = kBarOff + kBarWords * 8 + 16 + 1024;  // + tmem holder, abort flag, alignment slack
@@ -133,15 +138,6 @@ __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int c0
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(sa(bar))
       : "memory");
 }
-// Four rows r0..r3 of a 2D tensor (box one row high), columns [c0, c0 + box).
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int c0, int r0, int r1, int r2, int r3,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-      "%4, %5, %6}], [%7];" ::"r"(sa(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(sa(bar))
-      : "memory");
-}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
@@ -173,6 +169,28 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 2D TMA store of a shared-memory box to global coordinates (c0, c1), in the
+// calling thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int c1, const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(sa(src))
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N of the thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Row `row` of a 32 x 128-byte staging box in the 128-byte swizzle layout:
+// 16-byte chunk i of the row sits at chunk position i ^ (row % 8).
+__device__ __forceinline__ void box_put16(uint8_t* box, int row, int i, uint4 v) {
+  *reinterpret_cast<uint4*>(box + row * 128 + ((i ^ (row & 7)) << 4)) = v;
+}
+
 // Shared-memory matrix descriptor of a K-major operand tile whose rows are
 // 128 bytes, written by TMA with the 128-byte swizzle: 8-row groups 1024 bytes
 // apart (stride byte offset), descriptor version 1, swizzle mode 128B.  The
@@ -193,6 +211,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 
 struct Smem {
   uint8_t* ring;
+  uint8_t* out;   // [kEpiWarps][2][kBoxBytes]
   int* s_off;
   int* s_pre;
   int* s_slot;
@@ -209,6 +228,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   Smem s;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   s.ring = base;
+  s.out = base + kStageOutOff;
   s.s_off = reinterpret_cast<int*>(base + kTableOff);
   s.s_pre = s.s_off + (kMaxExperts + 1);
   s.s_slot = s.s_pre + (kMaxExperts + 1);
@@ -276,12 +296,14 @@ __device__ __forceinline__ TileInfo tile_info(const Smem& s, int n_u, int ntiles
   return t;
 }
 
-// kGateUp: the gate/up + SwiGLU GEMM (A = gathered x rows via map_a with a
-// one-row box, B = Wg/Wu rows); else the down GEMM (A = h rows via map_a with
-// a 128-row box, B = Wd rows).
+// kGateUp: the gate/up + SwiGLU GEMM (A = grouped x rows, B = Wg/Wu rows);
+// else the down GEMM (A = h rows, B = Wd rows).  map_a and map_b load boxes of
+// 64 columns x 128 rows (x, h, Wg/Wu) or N rows (Wd); map_out stores 32-row
+// output boxes.
 template <bool kGateUp>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, TcArgs a) {
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   const __grid_constant__ CUtensorMap map_out, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const Smem s = carve(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -299,7 +321,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       bar_init(&s.tfull[i], 1);
-      bar_init(&s.tempty[i], 4);
+      bar_init(&s.tempty[i], kEpiWarps);
     }
     bar_init(s.drain, 1);
     *s.abort_flag = 0;
@@ -327,14 +349,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool go = true;
     for (int tile = blockIdx.x; tile < total && go; tile += gridDim.x) {
       const TileInfo t = tile_info(s, n_u, ntiles, tile, n_cols);
-      int tok[4];
-      if (kGateUp) {  // the x rows of this lane's four grouped rows (a valid row past the expert's last)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int p = t.p0 + 4 * lane + i;
-          tok[i] = p < t.pend ? __ldg(&a.rows_by_u[p]) / a.k : 0;
-        }
-      }
       const long long brow = (long long)t.slot * a.slot_rows + (kGateUp ? t.n0 : 2LL * a.H + t.n0);
       for (int kt = 0; kt < KT; ++kt, ++it) {
         const int st = it % kStages;
@@ -351,15 +365,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) bar_expect_tx(&s.full[st], kABytes + b_bytes);
         __syncwarp();
         const int c0 = kt * kBK;
-        if (kGateUp) {
-          tma_gather4(A + lane * 4 * 128, &map_a, c0, tok[0], tok[1], tok[2], tok[3], &s.full[st]);
-          if (lane == 0) {
-            tma_2d(B, &map_b, c0, (int)brow, &s.full[st]);                         // 128 Wg rows
-            tma_2d(B + kBM * 128, &map_b, c0, (int)(brow + a.I), &s.full[st]);    // the same 128 Wu rows
-          }
-        } else if (lane == 0) {
-          tma_2d(A, &map_a, c0, t.p0, &s.full[st]);                              // 128 h rows
-          tma_2d(B, &map_b, c0, (int)brow, &s.full[st]);                         // N Wd rows
+        if (lane == 0) {
+          tma_2d(A, &map_a, c0, t.p0, &s.full[st]);                              // 128 grouped x or h rows
+          tma_2d(B, &map_b, c0, (int)brow, &s.full[st]);                         // 128 Wg rows / N Wd rows
+          if (kGateUp) tma_2d(B + kBM * 128, &map_b, c0, (int)(brow + a.I), &s.full[st]);  // the same Wu rows
         }
       }
     }
@@ -400,9 +409,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;            // TMEM lanes 32q .. 32q + 31
-    const int row = q * 32 + lane;     // tile row of this thread
+    // Warp w reads TMEM lanes 32 (w % 4) .. (the tile's rows 32 q ..) and half
+    // of the tile's columns.  A 32-row group that lies wholly before the
+    // expert's last row goes out through a swizzled staging box and one TMA
+    // store (full 128-byte lines); a group cut by the expert's end is stored
+    // row by row by its live lanes, so no store touches the next expert's rows.
+    const int q = warp & 3;                     // TMEM lanes 32q .. 32q + 31
+    const int half = (warp - 2) >> 2;           // which half of the columns
+    uint8_t* boxes = s.out + (warp - 2) * 2 * kBoxBytes;
+    int nbox = 0;
     int j = 0;
+    auto next_box = [&]() -> uint8_t* {          // a staging box no earlier store still reads
+      uint8_t* b = boxes + (nbox & 1) * kBoxBytes;
+      ++nbox;
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+      return b;
+    };
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++j) {
       const int acc = j & 1;
       bool ok = true;
@@ -412,48 +435,70 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bar_try(&s.tfull[acc], (j >> 1) & 1);  // every lane observes the completed phase itself
       tc_fence_after();
       const TileInfo t = tile_info(s, n_u, ntiles, tile, n_cols);
-      const int p = t.p0 + row;
-      const bool live = p < t.pend;
+      const int r0 = t.p0 + q * 32;              // first grouped row of this warp's group
+      const int live_rows = min(32, max(0, t.pend - r0));
+      const bool live = lane < live_rows;
+      const bool boxed = live_rows == 32;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
-      if (kGateUp) {
-        __nv_bfloat16* hrow = a.h + (long long)(live ? p : 0) * a.I + t.n0;
-        for (int c = 0; c < kH1; c += 32) {
-          float g[32], u[32];
-          tc_ld32(tbase + c, g);
-          tc_ld32(tbase + kH1 + c, u);
-          if (live) {
+      if (live_rows > 0) {
+        if (kGateUp) {
+          // h columns [hc, hc + 64): gate at TMEM columns hc.., up at kH1 + hc..
+          const int hc = half * 64;
+          uint8_t* box = boxed ? next_box() : nullptr;
+          __nv_bfloat16* hrow = a.h + (long long)(r0 + lane) * a.I + t.n0 + hc;
+          for (int c = 0; c < 64; c += 32) {
+            float g[32], u[32];
+            tc_ld32(tbase + hc + c, g);
+            tc_ld32(tbase + kH1 + hc + c, u);
             uint32_t packed[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float h0 = g[2 * i] / (1.0f + expf(-g[2 * i])) * u[2 * i];
-              const float h1 = g[2 * i + 1] / (1.0f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+            for (int i = 0; i < 16; ++i) {  // silu(g) * u = g u / (1 + e^-g); h is rounded to bf16
+              const float h0 = __fdividef(g[2 * i] * u[2 * i], 1.0f + __expf(-g[2 * i]));
+              const float h1 = __fdividef(g[2 * i + 1] * u[2 * i + 1], 1.0f + __expf(-g[2 * i + 1]));
               const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
               packed[i] = *reinterpret_cast<const uint32_t*>(&hv);
             }
-            uint4* dst = reinterpret_cast<uint4*>(hrow + c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) {
+              const uint4 v = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+              if (boxed) box_put16(box, lane, (c >> 3) + i, v);
+              else if (live) reinterpret_cast<uint4*>(hrow + c)[i] = v;
+            }
           }
-        }
-      } else {
-        const float wt = live ? __ldg(&a.topk_w[__ldg(&a.rows_by_u[p])]) : 0.0f;
-        float* yrow = a.yp + (long long)(live ? p : 0) * a.H + t.n0;
-        for (int c = 0; c < n_cols; c += 32) {
-          float v[32];
-          tc_ld32(tbase + c, v);
-          if (live) {
-            float4* dst = reinterpret_cast<float4*>(yrow + c);
+          if (boxed) {
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) tma_store_2d(&map_out, t.n0 + hc, r0, box);
+          }
+        } else {
+          // output columns [t.n0 + half * n_cols / 2, ...) in chunks of 32
+          const float wt = live ? __ldg(&a.topk_w[__ldg(&a.rows_by_u[r0 + lane])]) : 0.0f;
+          const int cw = n_cols / 2;
+          float* yrow = a.yp + (long long)(r0 + lane) * a.H + t.n0 + half * cw;
+          for (int c = 0; c < cw; c += 32) {
+            float v[32];
+            tc_ld32(tbase + half * cw + c, v);
+            uint8_t* box = boxed ? next_box() : nullptr;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(wt * v[4 * i], wt * v[4 * i + 1], wt * v[4 * i + 2], wt * v[4 * i + 3]);
+            for (int i = 0; i < 8; ++i) {
+              const float4 f = make_float4(wt * v[4 * i], wt * v[4 * i + 1], wt * v[4 * i + 2], wt * v[4 * i + 3]);
+              if (boxed) box_put16(box, lane, i, *reinterpret_cast<const uint4*>(&f));
+              else if (live) reinterpret_cast<float4*>(yrow + c)[i] = f;
+            }
+            if (boxed) {
+              fence_async_smem();
+              __syncwarp();
+              if (lane == 0) tma_store_2d(&map_out, t.n0 + half * cw + c, r0, box);
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) bar_arrive(&s.tempty[acc]);  // this warp's quarter of the accumulator is read
+      if (lane == 0) bar_arrive(&s.tempty[acc]);  // this warp's part of the accumulator is read
     }
+    if (lane == 0) bulk_wait_all();  // every TMA store of this warp has completed
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -467,10 +512,10 @@ using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, 
                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// A 2D bf16 tensor map, `cols` x `rows` (cols innermost, row pitch `pitch`
+// A 2D tensor map, `cols` x `rows` (cols innermost, row pitch `pitch`
 // bytes), box `box_cols` x `box_rows`, 128-byte swizzle, zero fill outside.
-cudaError_t bf16_map(CUtensorMap* m, const void* base, unsigned long long cols, unsigned long long rows,
-                     unsigned long long pitch, uint32_t box_cols, uint32_t box_rows) {
+cudaError_t tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, unsigned long long cols,
+                    unsigned long long rows, unsigned long long pitch, uint32_t box_cols, uint32_t box_rows) {
   static EncodeTiled enc = nullptr;
   if (!enc) enc = reinterpret_cast<EncodeTiled>(driver_fn("cuTensorMapEncodeTiled"));
   if (!enc) return cudaErrorNotSupported;
@@ -479,10 +524,14 @@ cudaError_t bf16_map(CUtensorMap* m, const void* base, unsigned long long cols, 
   const cuuint64_t strides[1] = {pitch};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  const CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+cudaError_t bf16_map(CUtensorMap* m, const void* base, unsigned long long cols, unsigned long long rows,
+                     unsigned long long pitch, uint32_t box_cols, uint32_t box_rows) {
+  return tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, cols, rows, pitch, box_cols, box_rows);
 }
 
 int tc_sms() {
@@ -522,9 +571,9 @@ cudaError_t launch_prefill_gemms(const PrefillArgs& p, int num_slots, cudaStream
   a.hdr = p.hdr; a.u_offset = p.u_offset; a.unique_slot = p.unique_slot; a.rows_by_u = p.rows_by_u;
   a.topk_w = p.topk_w; a.h = static_cast<__nv_bfloat16*>(p.h); a.yp = p.yp; a.status = p.status;
   a.H = H; a.I = I; a.k = p.k; a.R = R;
-  CUtensorMap mx, mw1, mh, mwd;
-  // x [T][H]: one-row boxes for the gathered A rows
-  if ((e = bf16_map(&mx, p.x, H, p.T, 2ull * H, kBK, 1)) != cudaSuccess) return e;
+  CUtensorMap mx, mw1, mh, mwd, mh_out, myp_out;
+  // xp [R][H]: the x rows in grouped order
+  if ((e = bf16_map(&mx, p.xp, H, R, 2ull * H, kBK, kBM)) != cudaSuccess) return e;
   // the pool as rows of H: Wg rows [s*3I, s*3I + I), Wu rows [s*3I + I, s*3I + 2I)
   if ((e = bf16_map(&mw1, p.pool, H, 3ull * I * num_slots, 2ull * H, kBK, kBM)) != cudaSuccess) return e;
   // h [R][I]
@@ -532,17 +581,20 @@ cudaError_t launch_prefill_gemms(const PrefillArgs& p, int num_slots, cudaStream
   // the pool as rows of I: Wd rows [s*3H + 2H, s*3H + 3H)
   const int n2 = H % 256 == 0 ? 256 : 128;
   if ((e = bf16_map(&mwd, p.pool, I, 3ull * H * num_slots, 2ull * I, kBK, n2)) != cudaSuccess) return e;
+  // output boxes of 32 rows x 128 bytes: h (64 bf16 columns) and yp (32 fp32 columns)
+  if ((e = bf16_map(&mh_out, p.h, I, R, 2ull * I, 64, 32)) != cudaSuccess) return e;
+  if ((e = tmap_2d(&myp_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.yp, H, R, 4ull * H, 32, 32)) != cudaSuccess) return e;
   const int grid = tc_sms();
   a.n_tile = kN1;
   a.slot_rows = 3LL * I;
   if (marks && (e = cudaEventRecord(marks[0], st)) != cudaSuccess) return e;
-  tc_gemm_kernel<true><<<grid, kTcThreads, kTcSmem, st>>>(mx, mw1, a);
+  tc_gemm_kernel<true><<<grid, kTcThreads, kTcSmem, st>>>(mx, mw1, mh_out, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (marks && (e = cudaEventRecord(marks[1], st)) != cudaSuccess) return e;
   a.n_tile = n2;
   a.slot_rows = 3LL * H;
   if (marks && (e = cudaEventRecord(marks[2], st)) != cudaSuccess) return e;
-  tc_gemm_kernel<false><<<grid, kTcThreads, kTcSmem, st>>>(mh, mwd, a);
+  tc_gemm_kernel<false><<<grid, kTcThreads, kTcSmem, st>>>(mh, mwd, myp_out, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (marks && (e = cudaEventRecord(marks[3], st)) != cudaSuccess) return e;
   return cudaSuccess;
