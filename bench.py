@@ -41,8 +41,8 @@ L2_BYTES = 129 * 1024 * 1024
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=496)
-    p.add_argument("--warmup", type=int, default=16)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=8)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=W.QWEN35B_DECODE.name, choices=sorted(W.ALL))
     p.add_argument("--fetch-mode", type=int, default=1, help="0 copy engine, 1 SM pull")
@@ -55,14 +55,17 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-link", action="store_true")
-    p.add_argument("--prefill", action="store_true",
-                   help="also measure the 16,384-token prefill chunk (40 layers) and report it under 'prefill'")
     p.add_argument("--trace", action="store_true", help="print one step's per-layer timeline to stderr")
     p.add_argument("--prefill-gemm-only", action="store_true",
                    help="only time the prefill chunk's two tensor-core GEMMs (all hits, no fetch) and print them")
-    p.add_argument("--cpu-seconds", type=float, default=15.0)
-    p.add_argument("--timing-steps", type=int, default=64,
-                   help="steps of the second timed pass (graphs with per-phase events) for the roofline")
+    p.add_argument("--cpu-steps", type=int, default=2,
+                   help="reference arm: decode steps of the oracle sample timed per step")
+    p.add_argument("--cpu-baseline-steps", type=int, default=8,
+                   help="decode steps of the oracle sample behind cpu_baseline")
+    p.add_argument("--no-blocks", action="store_true",
+                   help="skip the 4/8-stream, prefill and fp8 blocks (the headline decode only)")
+    p.add_argument("--timing-steps", type=int, default=32,
+                   help="steps of the timing pass (graphs with event nodes around every kernel)")
     return p.parse_args()
 
 
@@ -172,51 +175,74 @@ def barrier(world):
 
 # --------------------------------------------------------------------- oracle arm
 
-def oracle_sample(w: W.Workload, seconds: float, logits=None):
-    """Time the CPU oracle (routing, LRU simulation, fp64 FFN) on consecutive
-    steps of workload w until `seconds` of oracle time have passed (at least
-    one step).  Input generation (the expert blobs, hidden states) is not
-    timed.  The cache simulation starts cold at step 0.  Returns (tokens/s,
-    steps, oracle seconds)."""
+def _oracle_ffn_job(w, layer, x, idx, gates):
+    """One layer event's oracle FFN in a worker process: the unique experts'
+    blobs are generated first (input preparation, not timed), then the
+    dequantisation and the fp64 SwiGLU FFN are timed.  Returns (pid, s)."""
     from oracle import ffn as offn
+    uniq = sorted({int(v) for v in np.asarray(idx).ravel()})
+    raw = {e: synth.expert_blobs(w.seed, w.hidden, w.inter, w.wdtype, [w.blob_of(layer, e)]) for e in uniq}
+    t0 = time.perf_counter()
+    blobs = {e: offn.dequant_blob(b, w.hidden, w.inter, w.wdtype) for e, b in raw.items()}
+    offn.moe_ffn(x, idx, gates, lambda e: blobs[e])
+    return os.getpid(), time.perf_counter() - t0
+
+
+def oracle_sample(w: W.Workload, steps: int, workers: int, logits=None):
+    """The CPU oracle on the first `steps` decode steps of workload w: routing
+    and the LRU cache simulation run in order on one host thread (they are a
+    sequential decision stream); the FFN of every layer event runs in a pool
+    of `workers` spawned processes.  Oracle time = the decision stream's time
+    + the busiest worker's FFN time.  Returns (tokens/s, oracle seconds)."""
+    import concurrent.futures
+    import multiprocessing
+
     from oracle import routing as orouting
     from oracle.cache import ExpertCacheOracle
     if logits is None:
-        logits = W.router_logits(w.replace(steps=min(w.steps, 64)))
+        logits = W.router_logits(w.replace(steps=steps))
     ref = ExpertCacheOracle(w.num_layers, w.num_experts, w.num_slots)
-    spent = 0.0
-    steps = 0
-    while steps < logits.shape[0]:
-        for l in range(w.num_layers):
-            topk = orouting.topk(logits[steps, l], w.top_k)
-            raw = {e: synth.expert_blobs(w.seed, w.hidden, w.inter, w.wdtype, [w.blob_of(l, e)])
-                   for e in sorted({int(v) for v in topk.ravel()})}
-            x = W.hidden_states(w, steps, l)
-            t0 = time.perf_counter()
-            idx, gw = orouting.route(logits[steps, l], w.top_k)
-            ref.event(l, idx)
-            blobs = {e: offn.dequant_blob(b, w.hidden, w.inter, w.wdtype) for e, b in raw.items()}
-            offn.moe_ffn(x, idx, gw, lambda e: blobs[e])
-            spent += time.perf_counter() - t0
-        steps += 1
-        if spent >= seconds:
-            break
-    return steps * w.tokens / spent, steps, spent
+    t_dec = 0.0
+    busy = {}
+    # one thread per worker process: no BLAS or generator thread pools on top of the processes
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+                                              "SYNTH_THREADS")}
+    os.environ.update(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1", SYNTH_THREADS="1")
+    try:
+        pool = concurrent.futures.ProcessPoolExecutor(workers, mp_context=multiprocessing.get_context("spawn"))
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    with pool:
+        futs = []
+        for s in range(steps):
+            for l in range(w.num_layers):
+                t0 = time.perf_counter()
+                idx, gw = orouting.route(logits[s, l], w.top_k)
+                ref.event(l, idx)
+                t_dec += time.perf_counter() - t0
+                futs.append(pool.submit(_oracle_ffn_job, w, l, W.hidden_states(w, s, l), idx, gw))
+        for f in futs:
+            pid, dt = f.result()
+            busy[pid] = busy.get(pid, 0.0) + dt
+    spent = t_dec + max(busy.values())
+    return steps * w.tokens / spent, spent
 
 
-def cpu_baseline_subprocess(w: W.Workload, seconds: float):
-    """Run the oracle sample in a child process pinned to one BLAS thread."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    code = ("import json,sys; sys.path.insert(0, %r); import bench; from synth import workloads as W; "
-            "v, s, dt = bench.oracle_sample(W.ALL[%r], %r); print(json.dumps([v, s, dt]))") % (ROOT, w.name, seconds)
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
-    if r.returncode != 0:
-        raise RuntimeError("oracle baseline failed: " + r.stderr[-2000:])
-    v, s, dt = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {s} decode steps x {w.num_layers} layers of {w.name} (routing, LRU simulation, "
-                      f"fp64 SwiGLU FFN), {dt:.1f} s on 1 host thread"}
+def cpu_workers() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def cpu_baseline(w: W.Workload, steps: int):
+    workers = cpu_workers()
+    v, dt = oracle_sample(w, steps, workers)
+    return {"value": v, "unit": "tokens/s", "cores": workers, "kind": "oracle",
+            "sample": f"first {steps} decode steps x {w.num_layers} layers of {w.name} (cold cache): routing and "
+                      f"LRU simulation in order on one thread, fp64 SwiGLU FFN of each layer event over "
+                      f"{workers} worker processes; {dt:.1f} s of oracle time (decisions + busiest worker)"}
 
 
 def workload_config(w: W.Workload, world: int, n_blobs: int) -> dict:
@@ -234,16 +260,15 @@ def run_reference(args, w):
         return
     if args.slots:
         w = w.replace(num_slots=args.slots)
-    # each step: the oracle over a bounded sample of steps of the same workload
+    # each step: the oracle over a bounded sample (the first decode steps of
+    # the same workload, cold cache), all host cores
+    workers = cpu_workers()
+    logits = W.router_logits(w.replace(steps=args.cpu_steps))
     per = []
-    total_steps = 0
-    seconds = max(1.0, min(args.cpu_seconds, 20.0) / max(1, args.steps))
-    logits = W.router_logits(w.replace(steps=min(w.steps, 64)))
     for i in range(args.warmup + args.steps):
-        v, s, dt = oracle_sample(w, seconds, logits)
+        v, dt = oracle_sample(w, args.cpu_steps, workers, logits)
         if i >= args.warmup:
-            per.append(dt / max(1, s))
-            total_steps += s
+            per.append(dt / args.cpu_steps)
     ms = 1e3 * statistics.mean(per)
     value = w.tokens / (ms / 1e3)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
@@ -251,9 +276,9 @@ def run_reference(args, w):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(w, args.gpus, args.bank_blobs or w.blobs),
             "impl": "reference",
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{total_steps} decode steps (cold cache start) of {w.name}, "
-                                       "single host thread"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": workers, "kind": "oracle",
+                             "sample": f"each step: the first {args.cpu_steps} decode steps (cold cache) of "
+                                       f"{w.name}; decisions on one thread, FFN over {workers} worker processes"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -424,11 +449,12 @@ def ffn_only(w, dev, peak):
             "misses": st1["misses"] - st0["misses"]}
 
 
-def link_ceilings(cache, w, dev, bank):
+def link_ceilings(w, dev, bank, n_blobs):
     """Host-link ceilings measured on this machine, outside the timed region:
     the copy engine (one cudaMemcpyAsync per blob, as the copy-engine fetch
-    does) and the SM-pull fetch kernel alone on a cold cache (T=32 i.i.d.
-    tokens: ~100+ misses per layer event)."""
+    does; best of 3 rounds of 32 blobs) and the SM-pull fetch kernel alone
+    (a fresh cache routes 32 i.i.d. tokens at one layer: ~100 misses, all
+    pulled by one kernel) at 8 layers spread over the bank."""
     import torch
 
     import synth as S
@@ -447,16 +473,13 @@ def link_ceilings(cache, w, dev, bank):
         torch.cuda.synchronize(dev)
         best_ce = max(best_ce, n * eb / (s0.elapsed_time(s1) / 1e3) / 1e9)
     del d
-    c = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, 1024, 32, bank,
-                    cache.bank_blobs, fetch_mode=1, device=dev)
-    best_pull = 0.0
-    spread = []  # the same over layers spread across the bank (its far pages)
-    try:
-        for l in list(range(4)) + [9, 19, 29, 39]:
-            if l >= w.num_layers:
-                continue
+    pulls = []
+    for l in np.linspace(0, w.num_layers - 1, 8).astype(int).tolist():
+        c = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, 1024, 32, bank,
+                        n_blobs, fetch_mode=1, device=dev)
+        try:
             lg = torch.from_numpy(S.router_iid(7, 0, l, 32, w.num_experts)).to(dev)
-            st0 = c.stats()
+            st0 = c.stats()              # the route kernel counts the misses' bytes
             c.route_classify(l, lg)
             c.synchronize()
             c.timing_enable(True)
@@ -464,21 +487,212 @@ def link_ceilings(cache, w, dev, bank):
             c.synchronize()
             tm = c.timing()
             st1 = c.stats()
-            c.timing_enable(False)
-            gbs = (st1["bytes_fetched"] - st0["bytes_fetched"]) / (tm["fetch_ms"] / 1e3) / 1e9
-            if 0 < l < 4:
-                best_pull = max(best_pull, gbs)
-            elif l >= 4:
-                spread.append(gbs)
+            pulls.append((st1["bytes_fetched"] - st0["bytes_fetched"]) / (tm["fetch_ms"] / 1e3) / 1e9)
+        finally:
             c.close()
-            c = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, 1024, 32, bank,
-                            cache.bank_blobs, fetch_mode=1, device=dev)
+    return {"copy_engine_gbs": best_ce, "sm_pull_gbs": float(np.mean(pulls)), "sm_pull_max_gbs": float(max(pulls)),
+            "sm_pull_per_layer_gbs": [round(v, 1) for v in pulls],
+            "how": "copy engine: best of 3 x 32 one-blob cudaMemcpyAsync H2D from the pinned bank; SM pull: "
+                   "pull_misses_kernel alone, ~100 missed blobs of one layer per launch, 8 layers across the bank"}
+
+
+class DecodeBench:
+    """One decode workload through captured step graphs on one cache: the
+    cache is first filled to steady state by `fill` untimed steps of the same
+    routing stream (the miss rate of the first steps is compulsory misses of a
+    cold cache, not the workload's), then `warmup` untimed steps, then the
+    timed passes.  Step s of the routing/hidden-state stream is used once."""
+
+    def __init__(self, w, dev, bank, n_blobs, args, steps_needed, rank=0):
+        import torch
+
+        from expert_cache_host_layer_gb300.pipeline import ExpertCache, StepGraph
+        self.w, self.dev, self.args = w, dev, args
+        self.L, self.T = w.num_layers, w.tokens
+        wl = w.replace(steps=steps_needed, seed=w.seed + rank)  # independent replicas per rank
+        self.logits_h = W.router_logits(wl)  # [S][L][T][E]
+        self.x_h = np.stack([np.stack([W.hidden_states(wl, s, l) for l in range(self.L)])
+                             for s in range(steps_needed)])
+        self.act = torch.float32 if w.wdtype == synth.W_F32 else torch.bfloat16
+        self.logits_d = torch.from_numpy(self.logits_h).to(dev)
+        self.x_d = torch.from_numpy(self.x_h).to(dev, self.act)
+        self.lg_buf = torch.empty_like(self.logits_d[0])
+        self.x_buf = torch.empty_like(self.x_d[0])
+        self.y_buf = torch.empty((self.L, self.T, w.hidden), dtype=torch.float32, device=dev)
+        self.double = not args.serial
+        self.cache = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots,
+                                 self.T, bank, n_blobs, fetch_mode=args.fetch_mode, pull_ctas=args.pull_ctas,
+                                 copy_streams=args.copy_streams, fetch_warps=args.fetch_warps, device=dev)
+        self.stream = self.cache.stream
+        self.StepGraph = StepGraph
+        self.graphs = self._graphs(False)
+        self.next = 0  # next step of the stream
+
+    def _graphs(self, timing):
+        return [self.StepGraph(self.cache, list(self.lg_buf), list(self.x_buf), list(self.y_buf), self.double,
+                               timing=timing) for _ in range(2)]
+
+    def regraph(self):
+        """After a resize the slot pool may have moved: capture the graphs again."""
+        for g in self.graphs:
+            g.close()
+        self.graphs = self._graphs(False)
+
+    def step(self, gs, i):
+        s = self.next
+        self.lg_buf.copy_(self.logits_d[s], non_blocking=True)
+        self.x_buf.copy_(self.x_d[s], non_blocking=True)
+        gs[i % 2].launch()
+        self.next += 1
+
+    def run(self, n):
+        for i in range(n):
+            self.step(self.graphs, i)
+        self.cache.synchronize()
+
+    def timed(self, n, world=1, sampler=None):
+        """n steps timed with CUDA events on the compute stream, barrier and
+        synchronize on both sides; returns (ms, stats delta)."""
+        import torch
+        self.cache.synchronize()
+        st0 = self.cache.stats()
+        if sampler:
+            sampler.start()
+        barrier(world)
+        torch.cuda.synchronize(self.dev)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(self.stream)
+        for i in range(n):
+            self.step(self.graphs, i)
+        ev1.record(self.stream)
+        self.cache.synchronize()
+        torch.cuda.synchronize(self.dev)
+        barrier(world)
+        clocks = sampler.stop() if sampler else None
+        st1 = self.cache.stats()
+        return ev0.elapsed_time(ev1), {k: st1[k] - st0[k] for k in st1}, clocks
+
+    def e2e(self, n, world=1):
+        """n steps end to end through the C ABI: each step copies its logits and
+        hidden states from pinned host memory, runs, and copies y back to
+        pinned host memory; wall clock around the whole."""
+        import torch
+        s0 = self.next
+        lg_pin = torch.from_numpy(self.logits_h[s0:s0 + n]).pin_memory()
+        x_pin = torch.from_numpy(self.x_h[s0:s0 + n]).to(self.act).pin_memory()
+        y_pin = torch.empty((n, self.L, self.T, self.w.hidden), dtype=torch.float32).pin_memory()
+        self.cache.synchronize()
+        barrier(world)
+        torch.cuda.synchronize(self.dev)
+        t0 = time.perf_counter()
+        for i in range(n):
+            self.lg_buf.copy_(lg_pin[i], non_blocking=True)
+            self.x_buf.copy_(x_pin[i], non_blocking=True)
+            self.graphs[i % 2].launch()
+            y_pin[i].copy_(self.y_buf, non_blocking=True)
+        self.cache.synchronize()
+        torch.cuda.synchronize(self.dev)
+        dt = max_over_ranks(time.perf_counter() - t0, world)
+        self.next += n
+        return {"value": world * n * self.T / dt, "unit": "tokens/s", "ms_per_step": 1e3 * dt / n,
+                "h2d_bytes_per_step": int(lg_pin[0].numel() * 4 + x_pin[0].numel() * x_pin.element_size()),
+                "d2h_bytes_per_step": int(self.y_buf.numel() * 4)}
+
+    def timing_pass(self, n):
+        """n steps through graphs with event nodes around every route, fetch and
+        FFN launch, plus each layer's plan read back after the step.  Per
+        layer l the FFN window w_l is the fused kernel's duration (it also
+        copies layer l+1's misses over the host link); layer 0's misses are
+        copied by a pull kernel at the step's start."""
+        tg = self._graphs(True)
+        L, eb = self.L, self.w.expert_bytes
+        ffn, route, fetch0, nmiss, nuniq, step_ms = [], [], [], [], [], []
+        try:
+            for i in range(n):
+                self.step(tg, i)
+                r, fe, f, st_ms = tg[i % 2].timing()
+                plans = [self.cache.plan(l) for l in range(L)]
+                ffn.append(np.asarray(f))
+                route.append(np.asarray(r))
+                fetch0.append(float(fe[0]))
+                nmiss.append(np.array([len(p["miss_expert"]) for p in plans]))
+                nuniq.append(np.array([len(p["unique"]) for p in plans]))
+                step_ms.append(st_ms)
+        finally:
+            for g in tg:
+                g.close()
+        ffn, route, nmiss, nuniq = np.stack(ffn), np.stack(route), np.stack(nmiss), np.stack(nuniq)
+        # FFN windows that carried no copy: the FFN alone, in the pipeline
+        carried = np.zeros_like(nmiss)
+        carried[:, :-1] = nmiss[:, 1:]   # FFN(l) copies layer l+1's misses
+        plain = ffn[carried == 0]
+        f_alone = float(np.median(plain)) if plain.size else float(np.median(ffn))
+        exposed = np.clip(ffn - f_alone, 0.0, None).sum(axis=1) + np.asarray(fetch0)
+        # host link: bytes over the windows that moved them
+        link_bytes = float(nmiss.sum()) * eb
+        link_ms = float(ffn[carried > 0].sum() + np.asarray(fetch0)[nmiss[:, 0] > 0].sum())
+        hbm_bytes = (nuniq + carried) * eb   # per FFN launch: expert reads + copied blobs written
+        return {"steps": n, "ffn_us_per_launch": 1e3 * float(ffn.mean()),
+                "ffn_us_alone_in_pipeline": 1e3 * f_alone,
+                "ffn_ms_per_step": float(ffn.sum(axis=1).mean()),
+                "route_us_per_launch": 1e3 * float(route.mean()),
+                "step_ms_with_event_nodes": float(np.mean(step_ms)),
+                "gaps_ms_per_step": float(np.mean(step_ms) - ffn.sum(axis=1).mean() - np.mean(fetch0)),
+                "exposed_copy_ms_per_step": float(exposed.mean()),
+                "link_gbs": link_bytes / (link_ms / 1e3) / 1e9 if link_ms > 0 else None,
+                "miss_bytes_per_step": link_bytes / n,
+                "ffn_hbm_bytes_per_launch": float(hbm_bytes.mean()),
+                "ffn_read_bytes_per_launch": float((nuniq * eb).mean()),
+                "note": "route runs on its own stream ahead of the FFNs (off the critical path); the FFN "
+                        "windows are serial on the compute stream: step = layer-0 pull + FFN windows + gaps"}
+
+    def close(self):
+        for g in self.graphs:
+            g.close()
+        self.cache.close()
+
+
+def decode_block(w, dev, bank, n_blobs, args, steps, warmup, fill, timing_steps, peak, resize=None):
+    """A compact decode measurement of workload w (its own cache): fill,
+    warm-up, `steps` timed, then a timing pass.  `resize` = (slots, fill2):
+    after the first timed pass, resize the cache at a safe point, refill for
+    fill2 steps and time again."""
+    need = fill + warmup + steps + timing_steps + (resize[1] + warmup + steps if resize else 0)
+    b = DecodeBench(w, dev, bank, n_blobs, args, need)
+    try:
+        b.run(fill + warmup)
+        ms, d, _ = b.timed(steps)
+        tp = b.timing_pass(timing_steps)
+        out = {"workload": w.name, "tokens": w.tokens, "slots": w.num_slots, "steps": steps, "warmup": warmup,
+               "fill_steps": fill, "tokens_per_s": steps * w.tokens / (ms / 1e3), "ms_per_step": ms / steps,
+               "miss_rate": d["misses"] / max(1, d["unique_experts"]),
+               "roofline_ffn": {"bound": "hbm", "unit": "GB/s", "peak": peak,
+                                "achieved": tp["ffn_read_bytes_per_launch"] / (tp["ffn_us_per_launch"] / 1e6) / 1e9,
+                                "achieved_alone_in_pipeline":
+                                    tp["ffn_read_bytes_per_launch"] / (tp["ffn_us_alone_in_pipeline"] / 1e6) / 1e9},
+               "timing": tp}
+        r = out["roofline_ffn"]
+        r["frac"] = r["achieved"] / peak
+        r["frac_alone_in_pipeline"] = r["achieved_alone_in_pipeline"] / peak
+        if resize:
+            slots, fill2 = resize
+            b.cache.synchronize()
+            t0 = time.perf_counter()
+            b.cache.resize(slots)
+            resize_ms = 1e3 * (time.perf_counter() - t0)
+            b.regraph()
+            b.run(fill2 + warmup)
+            ms2, d2, _ = b.timed(steps)
+            out["after_resize"] = {"slots": slots, "resize_ms": resize_ms, "fill_steps": fill2,
+                                   "tokens_per_s": steps * w.tokens / (ms2 / 1e3), "ms_per_step": ms2 / steps,
+                                   "miss_rate": d2["misses"] / max(1, d2["unique_experts"])}
+        return out
     finally:
-        c.close()
-    return {"copy_engine_gbs": best_ce, "sm_pull_gbs": best_pull,
-            "sm_pull_spread_gbs": float(np.mean(spread)) if spread else None,
-            "how": "best of a few isolated runs: 32 x one-blob cudaMemcpyAsync H2D from pinned memory; "
-                   "pull_misses_kernel on a cold cache (first layers' blobs; spread: layers across the bank)"}
+        b.close()
+
+
+FILL_STEPS = 64  # steady state: the miss rate of the decode stream is counted from step 64 on
 
 
 def run_ours(args, w):
@@ -487,7 +701,7 @@ def run_ours(args, w):
     rank, local, world = dist_setup(args.gpus)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    from expert_cache_host_layer_gb300.pipeline import ExpertCache, StepGraph, pinned_bank
+    from expert_cache_host_layer_gb300.pipeline import pinned_bank
 
     if args.slots:
         w = w.replace(num_slots=args.slots)
@@ -496,189 +710,102 @@ def run_ours(args, w):
     bank = pinned_bank(n_blobs * w.expert_bytes)
     synth.expert_blobs(w.seed, w.hidden, w.inter, w.wdtype, np.arange(n_blobs), out_ptr=bank.data_ptr())
     gen_s = time.perf_counter() - t_setup
-
-    steps_total = args.warmup + args.steps + args.timing_steps
-    wl = w.replace(steps=steps_total, seed=w.seed + rank)  # independent replicas per rank
-    logits_h = W.router_logits(wl)                             # [S][L][T][E]
-    x_h = np.stack([np.stack([W.hidden_states(wl, s, l) for l in range(w.num_layers)]) for s in range(steps_total)])
-    act = torch.float32 if w.wdtype == synth.W_F32 else torch.bfloat16
-    logits_d = torch.from_numpy(logits_h).to(dev)
-    x_d = torch.from_numpy(x_h).to(dev, act)
+    peak, peak_kind = measured_peaks()
+    K, Wm = args.steps, args.warmup
     L, T = w.num_layers, w.tokens
-    # fixed per-layer buffers the captured step reads and writes
-    lg_buf = torch.empty_like(logits_d[0])
-    x_buf = torch.empty_like(x_d[0])
-    y_buf = torch.empty((L, T, w.hidden), dtype=torch.float32, device=dev)
-    double = not args.serial
+    fill = FILL_STEPS
 
-    def make_cache():
-        return ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots, T, bank,
-                           n_blobs, fetch_mode=args.fetch_mode, pull_ctas=args.pull_ctas,
-                           copy_streams=args.copy_streams, fetch_warps=args.fetch_warps, device=dev)
-
-    use_graph = True
-    cache = make_cache()
-    stream = cache.stream
-    # plain graphs for the timed steps; graphs with per-phase event nodes (which
-    # slow a step down) only for the second, roofline pass
-    graphs = [StepGraph(cache, list(lg_buf), list(x_buf), list(y_buf), double) for _ in range(2)]
-    tgraphs = [StepGraph(cache, list(lg_buf), list(x_buf), list(y_buf), double, timing=True) for _ in range(2)]
-
-    def step(s, i, gs):
-        lg_buf.copy_(logits_d[s], non_blocking=True)
-        x_buf.copy_(x_d[s], non_blocking=True)
-        gs[i % 2].launch()
-
-    for s in range(args.warmup):
-        step(s, s, graphs)
-    cache.synchronize()
-    st0 = cache.stats()
+    b = DecodeBench(w, dev, bank, n_blobs, args, fill + Wm + 3 * K + args.timing_steps, rank)
+    b.run(fill + Wm)
+    # the timed steps (the line's value), then e2e, then the same timed pass again
     sampler = ClockSampler(local)
-    sampler.start()
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for i, s in enumerate(range(args.warmup, args.warmup + args.steps)):
-        step(s, i, graphs)
-    ev1.record(stream)
-    cache.synchronize()
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    clocks = sampler.stop()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    st1 = cache.stats()
-
-    # ---- second timed pass: per-layer route / fetch / FFN event times -----
-    acc = {"route": 0.0, "fetch": 0.0, "ffn": 0.0, "n": 0, "step": 0.0}
-    if args.fetch_mode == 0:  # copy-engine fetches are timed by the library's copy thread
-        cache.timing_enable(True)
-    t_first = args.warmup + args.steps
-    for i, s in enumerate(range(t_first, t_first + args.timing_steps)):
-        step(s, i, tgraphs)
-        if i > 0:  # the previous step's events (it is done or nearly so)
-            r, fe, f, st_ms = tgraphs[(i - 1) % 2].timing()
-            acc["route"] += r.sum(); acc["fetch"] += fe.sum(); acc["ffn"] += f.sum(); acc["n"] += 1
-            acc["step"] += st_ms
-    cache.synchronize()
-    if args.timing_steps:
-        r, fe, f, st_ms = tgraphs[(args.timing_steps - 1) % 2].timing()
-        acc["route"] += r.sum(); acc["fetch"] += fe.sum(); acc["ffn"] += f.sum(); acc["n"] += 1
-        acc["step"] += st_ms
-    tm = {"route_ms": acc["route"], "fetch_ms": acc["fetch"], "ffn_ms": acc["ffn"],
-          "route_n": acc["n"] * L, "fetch_n": acc["n"] * L, "ffn_n": acc["n"] * L}
-    if args.fetch_mode == 0:
-        ct = cache.timing()
-        tm["fetch_ms"], tm["fetch_n"] = ct["fetch_ms"], ct["fetch_n"]
-        cache.timing_enable(False)
-    st2 = cache.stats()
-    if args.trace and rank == 0 and args.timing_steps:
-        tr = tgraphs[(args.timing_steps - 1) % 2].trace()
-        print("layer  route_b route_e  fetch_b fetch_e  ffn_b  ffn_e  (us from step start)", file=sys.stderr)
-        for l in range(L):
-            print(f"{l:5d} " + " ".join(f"{1e3 * v:7.1f}" for v in tr[l]), file=sys.stderr)
-    elapsed_ms = max_over_ranks(elapsed_ms, world)
-    tokens = world * args.steps * T
+    ms1, d, clocks = b.timed(K, world, sampler)
+    e2e = None if args.no_e2e else b.e2e(K, world)
+    ms2, _, _ = b.timed(K, world)
+    tp = b.timing_pass(args.timing_steps)
+    if args.trace and rank == 0:
+        print(json.dumps(tp), file=sys.stderr)
+    launches = d["kernel_launches"]
+    b.close()
+    elapsed_ms = max_over_ranks(ms1, world)
+    tokens = world * K * T
     value = tokens / (elapsed_ms / 1e3)
 
-    d = {k: st1[k] - st0[k] for k in st1}    # the timed steps
-    d2 = {k: st2[k] - st1[k] for k in st1}   # the roofline pass
-    eb = w.expert_bytes
-    ffn_bytes_per_launch = d2["unique_experts"] * eb / max(1, tm["ffn_n"])
-    ffn_ms = tm["ffn_ms"] / max(1, tm["ffn_n"])
-    peak, peak_kind = measured_peaks()
-    achieved = ffn_bytes_per_launch / (ffn_ms / 1e3) / 1e9 if ffn_ms > 0 else None
-    fetch_gbs = d2["bytes_fetched"] / max(1e-9, tm["fetch_ms"] / 1e3) / 1e9 if tm["fetch_ms"] > 0 else None
-    n_tsteps = max(1, acc["n"])
-    for g in graphs + tgraphs:
-        g.close()
-
-    # ---- end to end through the C ABI with host buffers -------------------
-    e2e = None
-    if not args.no_e2e:
-        lg_pin = torch.from_numpy(logits_h[args.warmup:]).pin_memory()
-        x_pin = torch.from_numpy(x_h[args.warmup:]).to(act).pin_memory()
-        y_pin = torch.empty((args.steps, L, T, w.hidden), dtype=torch.float32).pin_memory()
-        cache2 = make_cache()
-        g2 = StepGraph(cache2, list(lg_buf), list(x_buf), list(y_buf), double) if use_graph else None
-        for s in range(args.warmup):  # same warm state as the device-timed run
-            lg_buf.copy_(logits_d[s]); x_buf.copy_(x_d[s])
-            g2.launch() if g2 else cache2.run_step(list(lg_buf), list(x_buf), list(y_buf), double_buffer=double)
-        cache2.synchronize()
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        for i in range(args.steps):
-            lg_buf.copy_(lg_pin[i], non_blocking=True)
-            x_buf.copy_(x_pin[i], non_blocking=True)
-            g2.launch() if g2 else cache2.run_step(list(lg_buf), list(x_buf), list(y_buf), double_buffer=double)
-            y_pin[i].copy_(y_buf, non_blocking=True)
-        cache2.synchronize()  # polls: the copy thread may still have copies to enqueue
-        torch.cuda.synchronize(dev)
-        e2e_s = max_over_ranks(time.perf_counter() - t0, world)
-        if g2:
-            g2.close()
-        cache2.close()
-        e2e = {"value": world * args.steps * T / e2e_s, "unit": "tokens/s",
-               "h2d_bytes_per_step": int(lg_pin[0].numel() * 4 + x_pin[0].numel() * x_pin.element_size()),
-               "d2h_bytes_per_step": int(y_buf.numel() * 4)}
-
+    ffn_alone = ffn_only(w, dev, peak) if rank == 0 and T <= 8 else None
     link = None
     if rank == 0 and not args.no_link:
         try:
-            link = link_ceilings(cache, w, dev, bank)
+            link = link_ceilings(w, dev, bank, n_blobs)
         except Exception as ex:
             link = {"error": str(ex)[:200]}
-    ffn_alone = None
-    if rank == 0 and T <= 8:
-        ffn_alone = ffn_only(w, dev, peak)
-    prefill = None
-    if rank == 0 and args.prefill:
-        prefill = prefill_measure(dev, measured_bf16_tflops())
-
+    blocks = {}
+    if rank == 0 and not args.no_blocks:
+        for wb in (W.QWEN35B_DECODE_B4, W.QWEN35B_DECODE_B8):
+            blocks[wb.name] = decode_block(wb, dev, bank, n_blobs, args, max(8, K // 2), 3, fill, 16, peak)
+        blocks["prefill"] = prefill_measure(dev, measured_bf16_tflops())
+        blocks["prefill"]["gemm_alone"] = prefill_gemm_only(dev, measured_bf16_tflops())
+        wd = W.DSV4_DECODE
+        dbank = pinned_bank(wd.blobs * wd.expert_bytes)
+        synth.expert_blobs(wd.seed, wd.hidden, wd.inter, wd.wdtype, np.arange(wd.blobs), out_ptr=dbank.data_ptr())
+        blocks[wd.name] = decode_block(wd, dev, dbank, wd.blobs, args, max(8, K // 2), 3, 40, 8, peak,
+                                       resize=(wd.resize_slots, 24))
+        blocks[wd.name]["bank"] = f"aliased: {wd.blobs} physical blobs of {wd.expert_bytes} B for " \
+                                  f"{wd.keys} (layer, expert) keys"
+        del dbank
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
-            cpu = cpu_baseline_subprocess(w, args.cpu_seconds)
+            cpu = cpu_baseline(w, args.cpu_baseline_steps)
         except Exception as ex:  # reported, not fatal
-            cpu = {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": f"failed: {ex}"[:300]}
+            cpu = {"value": None, "unit": "tokens/s", "cores": cpu_workers(), "kind": "oracle",
+                   "sample": f"failed: {ex}"[:300]}
 
     if rank == 0:
+        eb = w.expert_bytes
+        bytes_launch = tp["ffn_hbm_bytes_per_launch"]
+        achieved = bytes_launch / (tp["ffn_us_per_launch"] / 1e6) / 1e9
+        link_ceiling = (link or {}).get("sm_pull_gbs") or None
+        need_ms = tp["miss_bytes_per_step"] / (link_ceiling * 1e9) * 1e3 if link_ceiling else None
+        ffn_ms = L * ffn_alone["launch_us"] / 1e3 if ffn_alone else None
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": Wm, "ms_per_step": elapsed_ms / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.wdtype == synth.W_BF16 else
             ("f32" if w.wdtype == synth.W_F32 else "fp8e4m3"), "data": "synthetic",
-            "config": dict(workload_config(w, world, n_blobs),
-                           fetch_mode=["copy_engine", "sm_pull"][args.fetch_mode], double_buffer=double,
-                           step_graph=use_graph),
+            "config": dict(workload_config(w, world, n_blobs), fetch_mode=["copy_engine", "sm_pull"][args.fetch_mode],
+                           double_buffer=not args.serial, step_graph=True, cache_fill_steps=fill,
+                           cache_fill="the routing stream's first 64 steps run untimed before the warm-up, so "
+                                      "the timed steps see the steady-state miss rate, not a cold cache's"),
             "miss_rate": d["misses"] / max(1, d["unique_experts"]),
-            "exposed_copy_ms_per_step": (elapsed_ms / args.steps - L * ffn_alone["launch_us"] / 1e3)
-            if ffn_alone else None,
+            "repeat_ms_per_step": [ms1 / K, ms2 / K],
             "expert_gemm_gbs": achieved,
-            "miss_copy": {"gbs": fetch_gbs, "bytes_per_step": d["bytes_fetched"] / args.steps,
-                          "mode": ["copy_engine", "sm_pull"][args.fetch_mode], "link": link},
-            "phase_ms_per_step": dict({k: tm[f"{k}_ms"] / n_tsteps for k in ("route", "fetch", "ffn")},
-                                      step=acc["step"] / n_tsteps, steps=acc["n"],
-                                      note="sums of per-layer kernel times from a second timed pass with "
-                                           "timing graphs (event nodes around every phase)"),
+            "exposed_copy_ms_per_step": tp["exposed_copy_ms_per_step"],
+            "miss_copy": {"gbs": tp["link_gbs"], "bytes_per_step": d["bytes_fetched"] / K,
+                          "mode": ["copy_engine", "sm_pull"][args.fetch_mode], "link": link,
+                          "link_time_needed_ms": need_ms, "ffn_time_ms": ffn_ms,
+                          "fits_link_budget": (need_ms <= ffn_ms) if need_ms and ffn_ms else None,
+                          "how": "gbs = miss bytes of the timing pass / the durations of the kernels that "
+                                 "copied them (each fused FFN copies the next layer's misses; layer 0's come "
+                                 "from a pull kernel); fits_link_budget: miss bytes / sm_pull ceiling <= "
+                                 "L x FFN-alone time"},
+            "per_kernel": tp,
             "roofline": {"kernel": "ffn_fused_kernel: one cooperative launch per layer (gate/up, SwiGLU, down, "
-                                   "combine), timed by event nodes around it in the timing pass",
+                                   "combine) that also copies the next layer's misses; CUDA event nodes "
+                                   "around each launch in the timing pass",
                          "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak if achieved else None,
-                         "peak_kind": peak_kind, "traffic": FFN_TRAFFIC_PER_LAUNCH.get(w.name),
-                         "bytes_per_launch": ffn_bytes_per_launch,
-                         "launch_us": ffn_ms * 1e3, "ffn_only": ffn_alone},
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": FFN_TRAFFIC_PER_LAUNCH.get(w.name),
+                         "bytes_per_launch": bytes_launch,
+                         "bytes_def": "n_unique x expert_bytes read + n_miss(next layer) x expert_bytes written",
+                         "launch_us": tp["ffn_us_per_launch"], "ffn_only": ffn_alone},
             "cpu_baseline": cpu,
-            "prefill": prefill,
+            "blocks": blocks,
             "e2e": e2e,
-            "gpu_launches": d["kernel_launches"],
+            "gpu_launches": launches,
             "clocks": clocks,
             "setup_s": {"bank_generate": round(gen_s, 1)},
         }
         print(json.dumps(line), flush=True)
-    cache.close()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

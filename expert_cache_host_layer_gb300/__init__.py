@@ -85,6 +85,7 @@ def _load():
         "ft_reset_stats": (st, [P]),
         "ft_get_pool": (st, [P, ctypes.POINTER(P), ctypes.POINTER(I64)]),
         "ft_get_copy_stream": (st, [P, ctypes.POINTER(P)]),
+        "ft_debug_pause_copies": (st, [P, I32]),
         "ft_timing_enable": (st, [P, I32]),
         "ft_get_timing": (st, [P, ctypes.POINTER(ft_timing)]),
         "ft_step_graph_create": (st, [P, P, P, P, I32, I32, I32, ctypes.POINTER(P)]),
@@ -205,6 +206,10 @@ def ft_get_copy_stream(cache: int) -> int:
     p = ctypes.c_void_p()
     _check(_lib.ft_get_copy_stream(cache, ctypes.byref(p)), "ft_get_copy_stream")
     return p.value or 0
+
+
+def ft_debug_pause_copies(cache: int, paused: bool):
+    _check(_lib.ft_debug_pause_copies(cache, int(bool(paused))), "ft_debug_pause_copies")
 
 
 def ft_timing_enable(cache: int, on: bool):

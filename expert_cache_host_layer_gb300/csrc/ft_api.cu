@@ -209,6 +209,7 @@ struct ft_cache {
   std::atomic<bool> stop{false};
   std::atomic<long long> copied_events{0};  // events whose copies (and ready flag) are enqueued
   std::atomic<int> copy_status{0};          // first error of the copy thread (ft_status)
+  std::atomic<bool> copies_paused{false};   // test knob: the copy thread serves no event while set
   std::mutex pool_mu;                       // guards pool and C against a resize while copies are issued
   // counters
   std::atomic<long long> launches{0}, memcpys{0};
@@ -244,6 +245,10 @@ void helper_loop(ft_cache* c) {
   long long e = 0;
   int idle = 0;
   while (!c->stop.load(std::memory_order_relaxed)) {
+    if (c->copies_paused.load(std::memory_order_acquire)) {
+      std::this_thread::sleep_for(std::chrono::microseconds(50));
+      continue;
+    }
     RingEntry* r = c->ring_host + (e % kRing);
     const int stamp = __atomic_load_n(&r->event, __ATOMIC_ACQUIRE);
     if (stamp > (int)e) {
@@ -969,6 +974,13 @@ ft_status ft_get_pool(ft_cache* c, void** pool, int64_t* num_slots) {
   if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
   if (pool) *pool = c->pool;
   if (num_slots) *num_slots = c->C;
+  return FT_OK;
+}
+
+ft_status ft_debug_pause_copies(ft_cache* c, int32_t paused) {
+  if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
+  if (c->cfg.fetch_mode != FT_FETCH_COPY_ENGINE) return fail(FT_ERR_STATE, "the cache has no copy thread");
+  c->copies_paused.store(paused != 0, std::memory_order_release);
   return FT_OK;
 }
 

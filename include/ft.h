@@ -266,6 +266,14 @@ ft_status ft_get_pool(ft_cache* cache, void** pool, int64_t* num_slots);
  * first one when copy_streams is 2). */
 ft_status ft_get_copy_stream(ft_cache* cache, void** stream);
 
+/* Test and debug knob, copy-engine mode only: while `paused` is 1 the
+ * library's copy thread serves no event, so FFN kernels that wait for a
+ * layer's copies run into their bounded wait (about one second), record
+ * FT_ERR_TIMEOUT and finish; the next synchronous call reports it.  Setting 0
+ * lets the thread continue where it stopped.  Errors: FT_ERR_INVALID_ARG,
+ * FT_ERR_STATE (SM-pull cache: no copy thread). */
+ft_status ft_debug_pause_copies(ft_cache* cache, int32_t paused);
+
 /* Enable (1) or disable (0) per-phase CUDA-event timing; enabling clears the
  * totals.  ft_get_timing waits for the streams and returns the totals. */
 ft_status ft_timing_enable(ft_cache* cache, int32_t on);

@@ -78,6 +78,10 @@ def _ptr(a: np.ndarray) -> int:
 
 
 def threads() -> int:
+    """Generator threads: SYNTH_THREADS if set (worker processes use 1), else the host's cores."""
+    env = os.environ.get("SYNTH_THREADS")
+    if env:
+        return max(1, min(64, int(env)))
     return max(1, min(64, os.cpu_count() or 1))
 
 

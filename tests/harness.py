@@ -84,12 +84,14 @@ def oracle_ffn(w: W.Workload, bank, n_blobs, layer, x, idx, gates):
 def run_parity(w: W.Workload, steps: int | None = None, fetch_mode: int = 1, double_buffer: bool = True,
                bank_blobs: int | None = None, check_tables_every: int = 1, ffn_every: int = 1,
                check_slots: bool = True, copy_streams: int = 1, logits=None, device="cuda:0",
-               ffn_tokens=None):
+               ffn_tokens=None, ffn_workers: int = 0):
     """Run `steps` steps of workload w through libft and the oracle.
 
     ffn_tokens: compare the FFN output on these token rows only; a callable
     ffn_tokens(layer, topk_idx) returns the rows for that layer event (None:
-    every row).  Decisions are always compared in full.  Returns a report dict; raises AssertionError on the
+    every row).  Decisions are always compared in full.
+    ffn_workers: check the FFN outputs in that many spawned host processes
+    (tests/oracle_worker.py) while the GPU run goes on; 0 checks inline.  Returns a report dict; raises AssertionError on the
     first mismatch.
     """
     from expert_cache_host_layer_gb300.pipeline import ExpertCache
@@ -108,7 +110,19 @@ def run_parity(w: W.Workload, steps: int | None = None, fetch_mode: int = 1, dou
     ys = [torch.empty((T, w.hidden), dtype=cache.out_dtype, device=dev) for _ in range(L)]
     report = {"events": 0, "ffn_checked": 0, "max_err": 0.0, "max_rms_err": 0.0, "slots_checked": 0}
     ev_counter = [0]
-    step_state = {}
+    pool, pending = None, []
+    if ffn_workers:
+        import concurrent.futures
+        import multiprocessing
+
+        from tests import oracle_worker
+        pool = concurrent.futures.ProcessPoolExecutor(ffn_workers, mp_context=multiprocessing.get_context("spawn"))
+
+    def check_ffn(t, mx, rm):
+        report["max_err"] = max(report["max_err"], mx)
+        report["max_rms_err"] = max(report["max_rms_err"], rm)
+        report["ffn_checked"] += 1
+        assert mx <= TOL[w.wdtype], f"event {t}: FFN max err {mx:.3e} x RMS > {TOL[w.wdtype]}"
 
     try:
         for s in range(steps):
@@ -151,13 +165,13 @@ def run_parity(w: W.Workload, steps: int | None = None, fetch_mode: int = 1, dou
                     ridx, rw, ev = refs[l]
                     sel = ffn_tokens(l, ridx) if callable(ffn_tokens) else ffn_tokens
                     tok = np.arange(T) if sel is None else np.asarray(sel)
-                    yr = oracle_ffn(w, bank, n_blobs, l, xs_h[l][tok], ridx[tok], rw[tok])
                     yg = ys[l].float().cpu().numpy()[tok]
-                    mx, rm = ffn_error(yg, yr)
-                    report["max_err"] = max(report["max_err"], mx)
-                    report["max_rms_err"] = max(report["max_rms_err"], rm)
-                    report["ffn_checked"] += 1
-                    assert mx <= TOL[w.wdtype], f"event {t}: FFN max err {mx:.3e} x RMS > {TOL[w.wdtype]}"
+                    if pool is not None:
+                        pending.append((t, pool.submit(oracle_worker.ffn_error_job, w, n_blobs, l, xs_h[l][tok],
+                                                       ridx[tok], rw[tok], yg)))
+                    else:
+                        yr = oracle_ffn(w, bank, n_blobs, l, xs_h[l][tok], ridx[tok], rw[tok])
+                        check_ffn(t, *ffn_error(yg, yr))
             if check_slots:  # slots filled this step hold their key's blob, byte for byte
                 _, rsk, rts = ref.tables()
                 first = refs[0][2].t
@@ -168,6 +182,8 @@ def run_parity(w: W.Workload, steps: int | None = None, fetch_mode: int = 1, dou
                     want = bank_blob(bank, w, n_blobs, key // w.num_experts, key % w.num_experts)
                     assert np.array_equal(got, want), f"step {s}: slot {slot} bytes differ from key {key}'s blob"
                     report["slots_checked"] += 1
+        for t, fut in pending:
+            check_ffn(t, *fut.result())
         st = cache.stats()
         report["events"] = ev_counter[0]
         report["stats"] = st
@@ -176,6 +192,8 @@ def run_parity(w: W.Workload, steps: int | None = None, fetch_mode: int = 1, dou
         assert st["evictions"] == ref.n_evict, (st["evictions"], ref.n_evict)
     finally:
         cache.close()
+        if pool is not None:
+            pool.shutdown(cancel_futures=True)
     return report
 
 

@@ -56,10 +56,14 @@ def test_qwen35b_multistream(w):
 
 
 def test_dsv4_fp8_with_resize():
-    """fp8 block-scaled experts, 1024 steps, shrink 2383 -> 1191 slots before step 512."""
+    """fp8 block-scaled experts, 1024 steps, shrink 2383 -> 1191 slots before
+    step 512.  Every 61st layer event's FFN (403 events, about 2 s of oracle
+    time each) is checked by a pool of host worker processes while the GPU
+    run continues."""
     w = W.DSV4_DECODE
-    rep = run_parity(w, check_tables_every=97, ffn_every=197)
+    rep = run_parity(w, check_tables_every=97, ffn_every=61, ffn_workers=12)
     assert rep["events"] == 1024 * 24 and rep["resize_moves"] > 0
+    assert rep["ffn_checked"] == len(range(0, 1024 * 24, 61))
     print("dsv4:", rep)
 
 
@@ -76,6 +80,16 @@ def test_qwen35b_step_graph_replay(fetch_mode):
     from tests.harness import run_parity_graph
     rep = run_parity_graph(W.QWEN35B_DECODE, steps=40, bank_blobs=512, ffn_every=13, fetch_mode=fetch_mode)
     assert rep["events"] == 40 * 40
+
+
+@pytest.mark.parametrize("w", [W.QWEN35B_DECODE_B4, W.QWEN35B_DECODE_B8], ids=["b4", "b8"])
+def test_qwen35b_multistream_step_graph_replay(w):
+    """4 and 8 decode streams sharing the 1740-slot cache, replayed through a
+    captured step graph (routing of every layer runs ahead of the FFNs, each
+    fetch inside the FFN kernel before it) against the oracle."""
+    from tests.harness import run_parity_graph
+    rep = run_parity_graph(w, steps=48, bank_blobs=1024, ffn_every=7)
+    assert rep["events"] == 48 * 40 and rep["ffn_checked"] > 0
 
 
 @pytest.mark.parametrize("fetch_mode", [0, 1])

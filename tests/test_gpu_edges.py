@@ -148,3 +148,38 @@ def test_resize_grow_and_to_new_pool():
             b = key % n
             assert np.array_equal(got, bank.numpy()[b * c.eb:(b + 1) * c.eb])
     c.close()
+
+
+def test_copy_thread_never_served_times_out_and_next_cache_works():
+    """Copy-engine mode with the library's copy thread paused: the layer's FFN
+    kernel waits for copies that never come, gives up after its bounded wait
+    (about one second), records FT_ERR_TIMEOUT and finishes; ft_synchronize
+    reports it once the thread resumes.  The GPU stays usable: a new cache
+    then runs a short decode in parity with the oracle."""
+    import time
+    w = W.TINY
+    bank, n = make_bank(w)
+    dev = torch.device("cuda:0")
+    c = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots, 1, bank, n,
+                    fetch_mode=ft.FT_FETCH_COPY_ENGINE, device=dev)
+    try:
+        ft.ft_debug_pause_copies(c.handle, True)
+        lg = torch.from_numpy(W.router_logits(w.replace(steps=1))[0, 0]).to(dev)
+        x = torch.zeros((1, w.hidden), device=dev)
+        y = torch.empty_like(x)
+        c.route_classify(0, lg)
+        c.fetch_misses(0)                   # a cold cache: every pick misses
+        c.moe_forward(0, x, y)
+        t0 = time.monotonic()
+        while time.monotonic() - t0 < 5.0 and torch.cuda.current_stream(dev).query() is False:
+            time.sleep(0.05)                # the FFN's own bounded wait ends it
+        assert torch.cuda.current_stream(dev).query(), "FFN kernel still running 5 s after its 1 s wait limit"
+        ft.ft_debug_pause_copies(c.handle, False)
+        with pytest.raises(ft.FtError) as e:
+            c.synchronize()
+        assert e.value.status == ft.FT_ERR_TIMEOUT
+    finally:
+        c.close()
+    from tests.harness import run_parity
+    rep = run_parity(w, steps=4, fetch_mode=0)
+    assert rep["events"] == 8
