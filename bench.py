@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-link", action="store_true")
     p.add_argument("--trace", action="store_true", help="print one step's per-layer timeline to stderr")
+    p.add_argument("--ffn-only", action="store_true",
+                   help="only time the decode FFN kernel with every expert a hit (no fetch) and print it")
     p.add_argument("--prefill-gemm-only", action="store_true",
                    help="only time the prefill chunk's two tensor-core GEMMs (all hits, no fetch) and print them")
     p.add_argument("--cpu-steps", type=int, default=2,
@@ -289,7 +291,7 @@ def run_reference(args, w):
 # (35B-shaped bf16 decode layer, 8 unique experts), mean of the two launches
 # of the ncu --set full capture summarised under profiles/.  It belongs to the
 # kernel as captured: set it to None whenever that kernel changes.
-FFN_TRAFFIC_PER_LAUNCH = {"qwen35b-a3b-shape-decode-b1": ((50.404352 + 0.292096) + (50.404608 + 0.148224)) / 2 * 1e6}
+FFN_TRAFFIC_PER_LAUNCH = {}
 
 
 def prefill_measure(dev, peak_tflops, steps=2):
@@ -814,6 +816,10 @@ def run_ours(args, w):
 def main():
     args = parse()
     w = W.ALL[args.workload]
+    if args.ffn_only:
+        import torch
+        print(json.dumps(ffn_only(w, torch.device("cuda", 0), measured_peaks()[0])), flush=True)
+        return
     if args.prefill_gemm_only:
         import torch
         print(json.dumps(prefill_gemm_only(torch.device("cuda", 0), measured_bf16_tflops())), flush=True)

@@ -613,8 +613,9 @@ ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t n
       CU(cudaMalloc(&c->pf_yp, sizeof(float) * prows * c->H));
       CU(cudaMalloc(&c->pf_pos, sizeof(int32_t) * prows));
     }
-    CU(cudaMalloc(&c->gbar, 3 * sizeof(unsigned)));
+    CU(cudaMalloc(&c->gbar, 4 * sizeof(unsigned)));
     CU(cudaMemset(c->gbar, 0, 3 * sizeof(unsigned)));
+    CU(cudaMemset(c->gbar + 3, 0xff, sizeof(unsigned)));
     if (g.fetch_mode == FT_FETCH_COPY_ENGINE) {  // event ring (mapped host) and ready flags (device)
       CU(cudaHostAlloc(reinterpret_cast<void**>(&c->ring_host), sizeof(RingEntry) * kRing, cudaHostAllocMapped));
       memset(c->ring_host, 0, sizeof(RingEntry) * kRing);
@@ -785,7 +786,8 @@ ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, v
   FfnArgs f{};
   f.hdr = pl.hdr; f.unique_slot = pl.unique_slot; f.u_offset = pl.u_offset; f.rows_by_u = pl.rows_by_u;
   f.topk_w = pl.topk_w; f.x = x; f.y = static_cast<float*>(y); f.pool = static_cast<const uint8_t*>(c->pool);
-  f.expert_bytes = (long long)c->eb; f.H = c->H; f.I = c->I; f.k = c->k; f.T = T; f.wdtype = c->wdtype; f.h = c->h_buf;
+  f.expert_bytes = (long long)c->eb; f.num_slots = (int)c->C;
+  f.H = c->H; f.I = c->I; f.k = c->k; f.T = T; f.wdtype = c->wdtype; f.h = c->h_buf;
   f.max_unique = std::min(T * c->k, c->E);
   f.status = c->tab.status;
   f.gbar = c->gbar;

@@ -125,11 +125,13 @@ struct FfnArgs {
   float* y;        // [T][H] f32
   const uint8_t* pool;
   long long expert_bytes;
+  int num_slots;   // slots of the pool (the fused kernel's tensor map of Wd spans them all)
   int H, I, k, T, wdtype;
   int max_unique;  // upper bound of the plan's n_unique (min(T*k, E)), sizes the grid
   float* h;        // [T*k][I] intermediate
   int32_t* status; // sticky status word (bounded waits record FT_ERR_TIMEOUT)
-  unsigned* gbar;  // [3] grid-barrier count and generation, finished-CTA count of the fused kernel (zeroed once)
+  unsigned* gbar;  // [4] of the fused kernel: [2] finished-CTA count (0 between launches), [3] the launch
+                   // whose y is zeroed (0xffffffff between launches); [0], [1] unused
   const int32_t* ready_flags;  // copy-engine mode: wait for ready_flags[e % kRing] == e (e = plan event); or null
   int32_t* done_host;          // copy-engine mode: device address of the mapped [kRing] words where the
                                // FFN stores e at done_host[e % kRing] once it no longer reads its slots; or null
@@ -173,9 +175,11 @@ cudaError_t launch_prefill_gemms(const PrefillArgs& a, int num_slots, cudaStream
 // Decode path: the gate/up+SwiGLU kernel, then the down+combine kernel.
 cudaError_t launch_decode_gateup(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_decode_down(const FfnArgs& a, cudaStream_t s);
-// Both in one cooperative kernel (gate/up, grid barrier, down, with Wd
-// prefetched during gate/up); cudaErrorNotSupported when the shape does not
-// fit its shared-memory budget (the caller then uses the two kernels).
+// Both in one kernel per layer (decode_fused.cu: units of intermediate rows,
+// each CTA adds its units' down projections into y; no grid barrier), launched
+// as a programmatic dependent of the previous kernel on the stream;
+// cudaErrorNotSupported when the shape does not fit it (the caller then uses
+// the two kernels).
 cudaError_t launch_decode_ffn_fused(const FfnArgs& a, cudaStream_t s);
 
 struct ResizeArgs {
