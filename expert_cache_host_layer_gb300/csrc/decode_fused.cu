@@ -173,7 +173,10 @@ __device__ __forceinline__ uint4 box_get16(const uint8_t* box, int r, int i) {
 }
 
 // MR: most rows (tokens) of one expert: 1 for single-token decode, else 8.
-template <int WT, int MR>
+// NCL: 16-byte chunks per lane of one Wg/Wu row (the row's chunks <= 32 NCL),
+// so the phase-A dot products unroll fully and every lane has NCL chunks of
+// loads in flight.
+template <int WT, int MR, int NCL>
 __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtensorMap wd_map, FfnArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   constexpr bool kF32 = WT == FT_W_F32;
@@ -323,7 +326,10 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
         float ag[MR], au[MR];
 #pragma unroll
         for (int q = 0; q < MR; ++q) ag[q] = au[q] = 0.0f;
-        for (int c = lane; c < nch; c += 32) {
+#pragma unroll
+        for (int ci = 0; ci < NCL; ++ci) {
+          const int c = ci * 32 + lane;
+          if (c >= nch) break;
           float fg[EPC], fu[EPC];
           decode_chunk<WT>(grow[c], fg);
           decode_chunk<WT>(urow[c], fu);
@@ -469,10 +475,10 @@ cudaError_t wd_map(CUtensorMap* m, const FfnArgs& a, int wsize) {
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorNotSupported;
 }
 
-template <int WT, int MR>
+template <int WT, int MR, int NCL>
 cudaError_t launch_typed(const FfnArgs& a, const Lay& lay, const CUtensorMap& map, cudaStream_t s) {
   static std::mutex mu;
-  static std::map<int, int> limit;  // device -> dynamic shared memory limit set so far (only grows)
+  static std::map<int, int> limit;  // device -> this instance's dynamic shared memory limit so far (only grows)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -480,9 +486,10 @@ cudaError_t launch_typed(const FfnArgs& a, const Lay& lay, const CUtensorMap& ma
     std::lock_guard<std::mutex> lk(mu);
     int& lim = limit[dev];
     if (lay.total > lim) {
-      e = cudaFuncSetAttribute(ffn_fused_kernel<WT, MR>, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
+      e = cudaFuncSetAttribute(ffn_fused_kernel<WT, MR, NCL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               lay.total);
       if (e == cudaSuccess)  // same split as the route and fetch kernels, so a route CTA can share an SM
-        e = cudaFuncSetAttribute(ffn_fused_kernel<WT, MR>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        e = cudaFuncSetAttribute(ffn_fused_kernel<WT, MR, NCL>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
       if (e != cudaSuccess) return e;
       lim = lay.total;
@@ -498,7 +505,7 @@ cudaError_t launch_typed(const FfnArgs& a, const Lay& lay, const CUtensorMap& ma
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, ffn_fused_kernel<WT, MR>, map, a);
+  return cudaLaunchKernelEx(&cfg, ffn_fused_kernel<WT, MR, NCL>, map, a);
 }
 
 template <int WT>
@@ -511,7 +518,11 @@ cudaError_t fused_typed(const FfnArgs& a, cudaStream_t s) {
   CUtensorMap map;
   cudaError_t e = wd_map(&map, a, WSZ);
   if (e != cudaSuccess) return e;
-  return a.T == 1 ? launch_typed<WT, 1>(a, lay, map, s) : launch_typed<WT, kMaxT>(a, lay, map, s);
+  const int nch = a.H * WSZ / 16;  // 16-byte chunks of one Wg/Wu row
+  if (nch <= 64)
+    return a.T == 1 ? launch_typed<WT, 1, 2>(a, lay, map, s) : launch_typed<WT, kMaxT, 2>(a, lay, map, s);
+  if (nch > 256) return cudaErrorNotSupported;
+  return a.T == 1 ? launch_typed<WT, 1, 8>(a, lay, map, s) : launch_typed<WT, kMaxT, 8>(a, lay, map, s);
 }
 
 }  // namespace

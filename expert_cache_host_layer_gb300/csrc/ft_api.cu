@@ -399,13 +399,17 @@ ft_status alloc_tables(Tables& t, int64_t C, int num_keys, bool with_keys) {
   if (with_keys) CU(cudaMalloc(&t.key_to_slot, sizeof(int32_t) * num_keys));
   CU(cudaMalloc(&t.slot_key, sizeof(int32_t) * C));
   CU(cudaMalloc(&t.slot_ts, sizeof(int32_t) * C));
-  CU(cudaMalloc(&t.order[0], sizeof(int2) * C));
-  CU(cudaMalloc(&t.order[1], sizeof(int2) * C));
-  CU(cudaMalloc(&t.order_cur, sizeof(int32_t) * 8));
-  t.status = t.order_cur + 1;
-  t.last_nu = t.order_cur + 2;
-  t.event_ctr = t.order_cur + 3;
-  t.pin_next = t.order_cur + 4;
+  t.log_cap = log_capacity(C);
+  CU(cudaMalloc(&t.log[0], sizeof(int2) * t.log_cap));
+  CU(cudaMalloc(&t.log[1], sizeof(int2) * t.log_cap));
+  CU(cudaMalloc(&t.pos, sizeof(int32_t) * C));
+  CU(cudaMalloc(&t.log_cur, sizeof(int32_t) * 8));
+  t.status = t.log_cur + 1;
+  t.last_nu = t.log_cur + 2;
+  t.event_ctr = t.log_cur + 3;
+  t.pin_next = t.log_cur + 4;
+  t.head = reinterpret_cast<uint32_t*>(t.log_cur + 5);
+  t.tail = reinterpret_cast<uint32_t*>(t.log_cur + 6);
   CU(cudaMalloc(&t.stats, sizeof(long long) * ST_COUNT));
   return FT_OK;
 }
@@ -414,9 +418,10 @@ void free_tables(Tables& t, bool with_keys) {
   if (with_keys) cudaFree(t.key_to_slot);
   cudaFree(t.slot_key);
   cudaFree(t.slot_ts);
-  cudaFree(t.order[0]);
-  cudaFree(t.order[1]);
-  cudaFree(t.order_cur);
+  cudaFree(t.log[0]);
+  cudaFree(t.log[1]);
+  cudaFree(t.pos);
+  cudaFree(t.log_cur);
   cudaFree(t.stats);
   Tables z{};
   z.key_to_slot = with_keys ? nullptr : t.key_to_slot;

@@ -26,15 +26,34 @@ struct Tables {
   int32_t* key_to_slot;  // [L*E]  slot of key l*E+e, -1 = absent
   int32_t* slot_key;     // [C]    key held by the slot, -1 = empty
   int32_t* slot_ts;      // [C]    event of last use, -1 = never
-  int2* order[2];        // [C]    (slot, key) of all slots in ascending (slot_ts, slot); ping-pong buffers
-  int32_t* order_cur;    // [1]    which order buffer is current
+  // The LRU order as an append-only log of (slot, key) entries: every slot
+  // has exactly one live entry, and the live entries from head to tail are in
+  // ascending (slot_ts, slot) order.  An event tombstones (slot = -1) the
+  // entries of its hits and takes its victims from the head, then appends its
+  // slots at the tail in slot order, so it touches O(|U|) entries, not C.
+  // Positions are 32-bit counters taken modulo log_cap (a power of two); when
+  // an event would not fit, the live entries are compacted into the other
+  // buffer first.
+  int2* log[2];          // [log_cap] ping-pong buffers
+  int32_t* pos;          // [C]    counter of each slot's live entry
+  uint32_t* head;        // [1]    counter of the first entry not yet passed
+  uint32_t* tail;        // [1]    counter one past the last entry
+  int32_t* log_cur;      // [1]    which log buffer is current
   int32_t* status;       // [1]    sticky device status (ft_status), 0 = ok
   int32_t* last_nu;      // [1]    |U| of the last event (its slots are the last entries of the order)
   int32_t* event_ctr;    // [1]    event number of the next classification
   int32_t* pin_next;     // [1]    1: the next event pins the last event's slots (0 after create / resize)
   long long* stats;      // [ST_COUNT]
   int32_t num_slots;
+  int32_t log_cap;
 };
+// Log capacity for C slots: room for the tombstones of many events between
+// compactions (a power of two).
+inline int32_t log_capacity(long long C) {
+  long long q = 4096;
+  while (q < 32 * C) q <<= 1;
+  return (int32_t)q;
+}
 
 // One layer's plan (device memory, library-owned), written by route_classify.
 struct Plan {

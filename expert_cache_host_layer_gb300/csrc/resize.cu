@@ -2,12 +2,12 @@
 // MoE Serving ...", design paragraph: when the VRAM budget changes the cache
 // is rebuilt at a safe point without restarting the engine).
 //
-// resize_tables (one CTA): walk the LRU order list (ascending (last use,
-// slot)); drop the first n_occupied - C' occupied entries; survivors below C'
-// stay put, survivors at or above C' take the lowest free slots below C' in
-// ascending old-slot order.  Writes the new slot tables and the move list.
-// rank_order: rebuilds the LRU order list of the new slots by ranking each
-// slot's (last use, slot) key.  move_blobs: copies the moved expert blobs.
+// resize_tables (one CTA): walk the live entries of the LRU log (ascending
+// (last use, slot)); drop the first n_occupied - C' occupied ones; survivors
+// below C' stay put, survivors at or above C' take the lowest free slots below
+// C' in ascending old-slot order.  Writes the new slot tables and the move
+// list.  rank_order: rebuilds the log of the new slots, compact, by ranking
+// each slot's (last use, slot) key.  move_blobs: copies the moved expert blobs.
 #include "ft_internal.h"
 
 namespace ft {
@@ -46,10 +46,12 @@ __global__ void __launch_bounds__(kThreads) resize_tables_kernel(ResizeArgs a) {
   __shared__ int s_warp[kWarps];
   const int tid = threadIdx.x;
   const int C = a.old_tab.num_slots, Cn = a.new_tab.num_slots;
-  const int cur = *a.old_tab.order_cur;
-  const int2* order = a.old_tab.order[cur];
-  int32_t* keep = reinterpret_cast<int32_t*>(a.old_tab.order[cur ^ 1]);  // scratch: 1 = survives
-  int32_t* free_list = reinterpret_cast<int32_t*>(a.new_tab.order[1]);   // scratch: free slots below C'
+  const int cur = *a.old_tab.log_cur;
+  const int2* lg = a.old_tab.log[cur];
+  const uint32_t qmask = (uint32_t)a.old_tab.log_cap - 1;
+  const uint32_t head = *a.old_tab.head, tail = *a.old_tab.tail;
+  int32_t* keep = reinterpret_cast<int32_t*>(a.old_tab.log[cur ^ 1]);  // scratch: 1 = survives
+  int32_t* free_list = reinterpret_cast<int32_t*>(a.new_tab.log[1]);   // scratch: free slots below C'
 
   // occupied count
   int occ_local = 0;
@@ -58,23 +60,24 @@ __global__ void __launch_bounds__(kThreads) resize_tables_kernel(ResizeArgs a) {
   block_excl_scan(occ_local, s_warp, n_occ);
   const int n_drop = n_occ > Cn ? n_occ - Cn : 0;
 
-  // drop the first n_drop occupied entries of the LRU order
+  // drop the first n_drop occupied live entries of the LRU log
   int carry = 0;
-  for (int base = 0; base < C; base += kThreads) {
-    const int p = base + tid;
+  for (uint32_t base = head; base != tail;) {
+    const uint32_t n = min((uint32_t)kThreads, tail - base);
     int s = -1, occ = 0;
-    if (p < C) {
-      s = order[p].x;
-      occ = a.old_tab.slot_key[s] >= 0;
+    if ((uint32_t)tid < n) {
+      s = lg[(base + tid) & qmask].x;
+      occ = s >= 0 && a.old_tab.slot_key[s] >= 0;
     }
     int tot;
     const int r = block_excl_scan(occ, s_warp, tot);
-    if (p < C) {
+    if (s >= 0) {
       const bool drop = occ && carry + r < n_drop;
       keep[s] = occ && !drop;
       if (drop) a.old_tab.key_to_slot[a.old_tab.slot_key[s]] = -1;
     }
     carry += tot;
+    base += n;
   }
   __syncthreads();
 
@@ -132,7 +135,9 @@ __global__ void __launch_bounds__(kThreads) resize_tables_kernel(ResizeArgs a) {
   }
   if (tid == 0) {
     *a.n_moves = n_moves;
-    *a.new_tab.order_cur = 0;
+    *a.new_tab.log_cur = 0;
+    *a.new_tab.head = 0;
+    *a.new_tab.tail = (uint32_t)Cn;
     *a.new_tab.status = *a.old_tab.status;
     *a.new_tab.last_nu = 0;
     *a.new_tab.event_ctr = *a.old_tab.event_ctr;
@@ -142,7 +147,8 @@ __global__ void __launch_bounds__(kThreads) resize_tables_kernel(ResizeArgs a) {
   }
 }
 
-// order[rank(s)] = (s, key of s) with rank by (slot_ts, slot) ascending over the new slots.
+// log[rank(s)] = (s, key of s), pos[s] = rank(s), with rank by (slot_ts, slot)
+// ascending over the new slots: the compact log of the new tables.
 __global__ void rank_order_kernel(Tables tab) {
   __shared__ int s_ts[1024];
   const int C = tab.num_slots;
@@ -160,7 +166,10 @@ __global__ void rank_order_kernel(Tables tab) {
         rank += o < my || (o == my && base + i < s);
       }
   }
-  if (s < C) tab.order[0][rank] = make_int2(s, tab.slot_key[s]);
+  if (s < C) {
+    tab.log[0][rank] = make_int2(s, tab.slot_key[s]);
+    tab.pos[s] = rank;
+  }
 }
 
 __global__ void move_blobs_kernel(const int32_t* moves, const int32_t* n_moves_p, const uint4* src, uint4* dst,

@@ -14,15 +14,14 @@
 //
 // Phase 2 (one CTA): dedup (the bit set in ascending order is U), hit
 // classification against key_to_slot, global-LRU victims, table updates and
-// the plan.  The LRU order is an explicit list of (slot, key) for all slots,
-// sorted by (last use, slot).  The previous event's slots are the last |U|
-// entries of that list (they were appended there), which is the pin rule
-// without any last-use lookup.  One pass of block-wide prefix sums over the
-// list (each thread owns 8 consecutive entries) finds the first |M|
-// candidates - entries that hold neither a hit of this event nor a pinned
-// slot - and compacts the list without this event's slots; those slots, which
-// all get last use = t, are appended in slot order.  That keeps the list
-// sorted without ever sorting it.
+// the plan.  The LRU order is an append-only log of (slot, key) entries with
+// one live entry per slot, live entries in (last use, slot) order from head to
+// tail.  The previous event appended its slots last, so they are the log's
+// last |U_{t-1}| entries: the pin rule is "stop before them".  An event
+// tombstones its hits' entries, takes the first |M| live entries from the
+// head as victims (one warp, a ballot per 32 entries), advances the head past
+// dead entries and appends its slots, in slot order, at the tail: O(|U|) work
+// plus the tombstones it passes, instead of a pass over all C slots.
 #include <cfloat>
 #include <climits>
 
@@ -33,7 +32,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSeg = 8;  // order entries per thread per pass
 
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
@@ -82,6 +80,7 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
   __shared__ int s_rowu[kMaxExperts];
   __shared__ int s_k2s[kMaxExperts];  // key_to_slot of this layer's experts
   __shared__ int s_flag;
+  __shared__ uint32_t s_head;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, k = a.k, T = a.T;
@@ -92,20 +91,16 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
   for (int i = tid; i < E; i += kThreads) s_cnt[i] = 0;
   // A single CTA runs phase 2 itself: start its table reads now so they
   // overlap the top-k work (the multi-CTA tail reads them after the ticket).
-  const int layer = a.layer, C = a.tab.num_slots;
+  const int layer = a.layer;
   int cur = 0, event = 0, n_prev = 0;
-  int2 ent0[kSeg];
+  uint32_t head = 0, tail = 0;
   if (single) {
-    cur = *a.tab.order_cur;
+    cur = *a.tab.log_cur;
     event = *a.tab.event_ctr;
     n_prev = *a.tab.pin_next ? *a.tab.last_nu : 0;
+    head = *a.tab.head;
+    tail = *a.tab.tail;
     for (int e = tid; e < E; e += kThreads) s_k2s[e] = a.tab.key_to_slot[layer * E + e];
-    const int2* order = a.tab.order[cur];
-#pragma unroll
-    for (int i = 0; i < kSeg; ++i) {
-      const int p = tid * kSeg + i;
-      ent0[i] = p < C ? order[p] : make_int2(-1, -1);
-    }
   }
   __syncthreads();
 
@@ -183,9 +178,11 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
 
   // ---------------- phase 2 (one CTA): dedup, classify, victims ------------
   if (!single) {
-    cur = *a.tab.order_cur;
+    cur = *a.tab.log_cur;
     event = *a.tab.event_ctr;
     n_prev = *a.tab.pin_next ? *a.tab.last_nu : 0;
+    head = *a.tab.head;
+    tail = *a.tab.tail;
     for (int e = tid; e < E; e += kThreads) s_k2s[e] = a.tab.key_to_slot[layer * E + e];
   }
   if (warp == 0) {
@@ -232,56 +229,80 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
   }
   const int n_miss = carry;
 
-  // one pass over the LRU order: victims = first n_miss candidates; kept
-  // entries are compacted into the other order buffer
-  const int2* order = a.tab.order[cur];
-  int2* norder = a.tab.order[cur ^ 1];
-  const int pin_from = C - n_prev;  // entries at or after this position are pinned
-  int carry_cand = 0, carry_hit = 0;
-  for (int base = 0; base < C; base += kThreads * kSeg) {
-    const int p0 = base + tid * kSeg;
-    int2 ent[kSeg];
-#pragma unroll
-    for (int i = 0; i < kSeg; ++i)
-      ent[i] = (single && base == 0) ? ent0[i] : (p0 + i < C ? order[p0 + i] : make_int2(-1, -1));
-    uint32_t hit_m = 0u, cand_m = 0u;
-#pragma unroll
-    for (int i = 0; i < kSeg; ++i) {
-      const int p = p0 + i;
-      if (p < C) {
-        const int key = ent[i].y;
-        bool hs = false;
-        if (key >= 0 && key / E == layer) {
-          const int e = key - layer * E;
-          hs = (s_bits[e >> 5] >> (e & 31)) & 1u;
-        }
-        if (hs) hit_m |= 1u << i;
-        else if (p < pin_from) cand_m |= 1u << i;
+  // the LRU log: compact it first if this event's entries would not fit
+  const uint32_t Q = (uint32_t)a.tab.log_cap, qmask = Q - 1;
+  if (tail - head + (uint32_t)n_u > Q) {
+    const int2* src = a.tab.log[cur];
+    int2* dst = a.tab.log[cur ^ 1];
+    int kept = 0;
+    for (uint32_t base = head; base != tail;) {
+      const uint32_t n = min((uint32_t)kThreads, tail - base);
+      int2 e = make_int2(-1, -1);
+      if ((uint32_t)tid < n) e = src[(base + tid) & qmask];
+      const int live = (uint32_t)tid < n && e.x >= 0;
+      int tot;
+      const int r = block_excl_scan(live, s_warp, tot);
+      if (live) {
+        dst[kept + r] = e;
+        a.tab.pos[e.x] = kept + r;
       }
+      kept += tot;
+      base += n;
     }
-    int tot;
-    const int packed = block_excl_scan((__popc(cand_m) << 16) | __popc(hit_m), s_warp, tot);
-    int cb = carry_cand + (packed >> 16), hb = carry_hit + (packed & 0xffff);
-#pragma unroll
-    for (int i = 0; i < kSeg; ++i) {
-      const int p = p0 + i;
-      if (p >= C) break;
-      const bool hs = (hit_m >> i) & 1u, cand = (cand_m >> i) & 1u;
-      const bool victim = cand && cb < n_miss;
-      if (victim) {
-        s_victim[cb] = ent[i].x;
-        s_evict[cb] = ent[i].y;
+    // the previous event's entries stay the last ones (compaction keeps the order)
+    cur ^= 1;
+    head = 0;
+    tail = (uint32_t)kept;
+    __syncthreads();
+  }
+  int2* lg = a.tab.log[cur];
+  // tombstone the hits' entries
+  for (int u = tid; u < n_u; u += kThreads)
+    if (s_mrank[u] < 0) lg[(uint32_t)a.tab.pos[s_uslot[u]] & qmask].x = -1;
+  __syncthreads();
+  // victims: the first n_miss live entries from the head, stopping before the
+  // previous event's entries (pinned); then the head passes the dead entries
+  const uint32_t pin_start = tail - (uint32_t)n_prev;
+  if (warp == 0) {
+    int found = 0;
+    uint32_t p = head;
+    while (found < n_miss && p != pin_start) {
+      const uint32_t n = min(32u, pin_start - p);
+      const int2 e = (uint32_t)lane < n ? lg[(p + lane) & qmask] : make_int2(-1, -1);
+      const bool live = (uint32_t)lane < n && e.x >= 0;
+      const unsigned m = __ballot_sync(0xffffffffu, live);
+      const int r = found + __popc(m & ((1u << lane) - 1u));
+      if (live && r < n_miss) {
+        s_victim[r] = e.x;
+        s_evict[r] = e.y;
+        lg[(p + lane) & qmask].x = -1;
       }
-      if (!hs && !victim) norder[p - hb - min(cb, n_miss)] = ent[i];
-      cb += cand;
-      hb += hs;
+      found = min(n_miss, found + __popc(m));
+      p += n;
     }
-    carry_cand += tot >> 16;
-    carry_hit += tot & 0xffff;
+    if (lane == 0) s_flag = found;
+    __syncwarp();
+    // head: first live entry at or after the old head (bounded by the tail)
+    uint32_t h = head;
+    while (h != tail) {
+      const uint32_t n = min(32u, tail - h);
+      const bool live = (uint32_t)lane < n && lg[(h + lane) & qmask].x >= 0;
+      const unsigned m = __ballot_sync(0xffffffffu, live);
+      if (m) {
+        h += __ffs(m) - 1;
+        break;
+      }
+      h += n;
+    }
+    if (lane == 0) s_head = h;
   }
   __syncthreads();
+  const bool capacity_ok = s_flag >= n_miss;
 
-  if (carry_cand < n_miss) {  // pool too small for this event: leave the tables as they are
+  if (!capacity_ok) {  // pool too small for this event: put the log back and leave the tables as they are
+    for (int u = tid; u < n_u; u += kThreads)
+      if (s_mrank[u] < 0) lg[(uint32_t)a.tab.pos[s_uslot[u]] & qmask].x = s_uslot[u];
+    for (int i = tid; i < s_flag; i += kThreads) lg[(uint32_t)a.tab.pos[s_victim[i]] & qmask].x = s_victim[i];
     if (tid == 0) {
       atomicCAS(a.tab.status, 0, (int)FT_ERR_CAPACITY);
       a.plan.hdr[PH_EVENT] = event;
@@ -291,6 +312,9 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
       *a.tab.last_nu = 0;
       *a.tab.event_ctr = event + 1;
       *a.tab.pin_next = 1;
+      *a.tab.log_cur = cur;
+      *a.tab.head = head;
+      *a.tab.tail = tail;
       if (a.ring) {
         RingEntry* r = a.ring + (event % kRing);
         r->layer = layer;
@@ -298,7 +322,7 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
       }
     }
   } else {
-    // the event's slots (hits and victims) go to the end in slot order
+    // the event's slots (hits and victims) go to the end of the log in slot order
     for (int u = tid; u < n_u; u += kThreads)
       if (s_mrank[u] >= 0) s_uslot[u] = s_victim[s_mrank[u]];
     __syncthreads();
@@ -306,7 +330,9 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
       const int s = s_uslot[u];
       int rank = 0;
       for (int q = 0; q < n_u; ++q) rank += s_uslot[q] < s;
-      norder[C - n_u + rank] = make_int2(s, layer * E + s_uexp[u]);
+      const uint32_t at = tail + (uint32_t)rank;
+      lg[at & qmask] = make_int2(s, layer * E + s_uexp[u]);
+      a.tab.pos[s] = (int32_t)at;
       a.tab.slot_ts[s] = event;
       a.plan.unique_expert[u] = s_uexp[u];
       a.plan.unique_slot[u] = s;
@@ -386,7 +412,9 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
       *a.tab.last_nu = n_u;
       *a.tab.event_ctr = event + 1;
       *a.tab.pin_next = 1;
-      *a.tab.order_cur = cur ^ 1;
+      *a.tab.log_cur = cur;
+      *a.tab.head = s_head;
+      *a.tab.tail = tail + (uint32_t)n_u;
     }
   }
   if (a.ring) {  // publish the entry: every field first, then the stamp (release, system scope)
@@ -408,11 +436,13 @@ __global__ void init_tables_kernel(Tables tab, int num_keys) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < tab.num_slots; i += stride) {
     tab.slot_key[i] = -1;
     tab.slot_ts[i] = -1;
-    tab.order[0][i] = make_int2(i, -1);  // all slots empty: (ts = -1, slot) order is slot order
-    tab.order[1][i] = make_int2(i, -1);
+    tab.log[0][i] = make_int2(i, -1);  // all slots empty: (ts = -1, slot) order is slot order
+    tab.pos[i] = i;
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
-    *tab.order_cur = 0;
+    *tab.log_cur = 0;
+    *tab.head = 0;
+    *tab.tail = (uint32_t)tab.num_slots;
     *tab.status = 0;
     *tab.last_nu = 0;
     *tab.event_ctr = 0;
