@@ -206,30 +206,32 @@ def oracle_sample(w: W.Workload, steps: int, workers: int, logits=None):
     ref = ExpertCacheOracle(w.num_layers, w.num_experts, w.num_slots)
     t_dec = 0.0
     busy = {}
-    # one thread per worker process: no BLAS or generator thread pools on top of the processes
+    # one thread per worker process: no BLAS or generator thread pools on top of the
+    # processes (the executor spawns its workers lazily, so the variables stay set
+    # for the pool's whole life)
     saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
                                               "SYNTH_THREADS")}
     os.environ.update(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1", SYNTH_THREADS="1")
     try:
-        pool = concurrent.futures.ProcessPoolExecutor(workers, mp_context=multiprocessing.get_context("spawn"))
+        with concurrent.futures.ProcessPoolExecutor(workers,
+                                                    mp_context=multiprocessing.get_context("spawn")) as pool:
+            futs = []
+            for s in range(steps):
+                for l in range(w.num_layers):
+                    t0 = time.perf_counter()
+                    idx, gw = orouting.route(logits[s, l], w.top_k)
+                    ref.event(l, idx)
+                    t_dec += time.perf_counter() - t0
+                    futs.append(pool.submit(_oracle_ffn_job, w, l, W.hidden_states(w, s, l), idx, gw))
+            for f in futs:
+                pid, dt = f.result()
+                busy[pid] = busy.get(pid, 0.0) + dt
     finally:
         for k, v in saved.items():
             if v is None:
                 os.environ.pop(k, None)
             else:
                 os.environ[k] = v
-    with pool:
-        futs = []
-        for s in range(steps):
-            for l in range(w.num_layers):
-                t0 = time.perf_counter()
-                idx, gw = orouting.route(logits[s, l], w.top_k)
-                ref.event(l, idx)
-                t_dec += time.perf_counter() - t0
-                futs.append(pool.submit(_oracle_ffn_job, w, l, W.hidden_states(w, s, l), idx, gw))
-        for f in futs:
-            pid, dt = f.result()
-            busy[pid] = busy.get(pid, 0.0) + dt
     spent = t_dec + max(busy.values())
     return steps * w.tokens / spent, spent
 
