@@ -289,11 +289,12 @@ def run_reference(args, w):
 
 # --------------------------------------------------------------------- our arm
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one ffn_fused_kernel launch
-# (35B-shaped bf16 decode layer, 8 unique experts), mean of the two launches
-# of the ncu --set full capture summarised under profiles/.  It belongs to the
-# kernel as captured: set it to None whenever that kernel changes.
+# dram__bytes_read.sum + dram__bytes_write.sum per ffn_fused_kernel launch from an ncu capture, keyed by
+# workload; they belong to the kernel as captured: drop an entry whenever that kernel changes.  The
+# in-pipeline launches (64 GB bank, copies riding along) are not captured (too large for a full capture);
+# the all-hit launches of --ffn-only are (profiles/ffn_fused_kernel_qwen35b_decode_allhit.md).
 FFN_TRAFFIC_PER_LAUNCH = {}
+FFN_ONLY_TRAFFIC_PER_LAUNCH = {"qwen35b-a3b-shape-decode-b1": (50.390784e6 + 4.608e3 + 50.390272e6 + 2.304e3) / 2}
 
 
 def prefill_measure(dev, peak_tflops, steps=2):
@@ -463,7 +464,7 @@ def ffn_only(w, dev, peak, layers=16, steps=32):
     kus = 1e3 * float(np.mean(win))
     moved = k * w.expert_bytes
     return {"kernel": "ffn_fused_kernel with no fetch (all hits)", "layers": layers, "steps": steps,
-            "launch_us": us, "kernel_window_us": kus,
+            "launch_us": us, "kernel_window_us": kus, "traffic": FFN_ONLY_TRAFFIC_PER_LAUNCH.get(w.name),
             "bytes_per_launch": moved, "achieved": moved / (us / 1e6) / 1e9, "peak": peak,
             "frac": moved / (us / 1e6) / 1e9 / peak, "unit": "GB/s",
             "achieved_window": moved / (kus / 1e6) / 1e9, "frac_window": moved / (kus / 1e6) / 1e9 / peak,
