@@ -73,6 +73,8 @@ def _load():
     sig = {
         "ft_expert_bytes": (ctypes.c_size_t, [I32, I32, I32]),
         "ft_cache_create": (st, [ctypes.POINTER(ft_cache_config), P, I64, P, ctypes.POINTER(P)]),
+        "ft_cache_overhead_bytes": (ctypes.c_uint64, [ctypes.POINTER(ft_cache_config), I64]),
+        "ft_slots_for_budget": (st, [ctypes.POINTER(ft_cache_config), ctypes.c_uint64, ctypes.POINTER(I64)]),
         "ft_cache_destroy": (st, [P]),
         "ft_cache_resize": (st, [P, P, I64]),
         "ft_route_classify": (st, [P, I32, P, I32, P, P]),
@@ -127,6 +129,16 @@ def library():
 
 def ft_expert_bytes(hidden: int, inter: int, wdtype: int) -> int:
     return int(_lib.ft_expert_bytes(hidden, inter, wdtype))
+
+
+def ft_cache_overhead_bytes(cfg: ft_cache_config, num_slots: int) -> int:
+    return int(_lib.ft_cache_overhead_bytes(ctypes.byref(cfg), num_slots))
+
+
+def ft_slots_for_budget(cfg: ft_cache_config, budget_bytes: int) -> int:
+    n = ctypes.c_int64()
+    _check(_lib.ft_slots_for_budget(ctypes.byref(cfg), budget_bytes, ctypes.byref(n)), "ft_slots_for_budget")
+    return n.value
 
 
 def ft_cache_create(cfg: ft_cache_config, slot_pool: int, num_slots: int, compute_stream: int = 0) -> int:

@@ -428,6 +428,48 @@ void free_tables(Tables& t, bool with_keys) {
   t = z;
 }
 
+// Device bytes of one cudaMalloc of n bytes, rounded to the allocation granularity.
+uint64_t dev_alloc(uint64_t n) { return (n + 511) & ~uint64_t(511); }
+
+// Checks the fields of a configuration that do not need a GPU; the message
+// goes to ft_last_error.
+ft_status check_config(const ft_cache_config& g) {
+  if (g.num_layers < 1 || g.num_experts < 1 || g.num_experts > kMaxExperts)
+    return fail(FT_ERR_INVALID_ARG, "num_layers must be >= 1 and num_experts in 1..%d", kMaxExperts);
+  if (g.top_k < 1 || g.top_k > kMaxTopK || g.top_k > g.num_experts)
+    return fail(FT_ERR_INVALID_ARG, "top_k must be in 1..min(num_experts, %d)", kMaxTopK);
+  const size_t eb = blob_bytes(g.hidden, g.inter, g.wdtype);
+  if (eb == 0) return fail(FT_ERR_INVALID_ARG, "unsupported hidden/inter/wdtype (%d, %d, %d)", g.hidden, g.inter, g.wdtype);
+  if (eb % 16) return fail(FT_ERR_INVALID_ARG, "expert_bytes %zu is not a multiple of 16", eb);
+  if (g.wdtype != FT_W_F32 && (g.hidden % 128 || g.inter % 128))
+    return fail(FT_ERR_INVALID_ARG, "bf16/fp8 experts need hidden and inter multiples of 128");
+  if (g.max_tokens < 1) return fail(FT_ERR_INVALID_ARG, "max_tokens must be >= 1");
+  if ((long long)g.max_tokens * g.top_k > (1LL << 30)) return fail(FT_ERR_INVALID_ARG, "max_tokens * top_k too large");
+  return FT_OK;
+}
+
+// Every device allocation ft_cache_create makes for C slots (the caller's pool
+// aside), each rounded to the allocation granularity.
+uint64_t cache_device_bytes(const ft_cache_config& g, int64_t C) {
+  const uint64_t L = g.num_layers, E = g.num_experts, H = g.hidden, I = g.inter;
+  const uint64_t rows = (uint64_t)g.max_tokens * g.top_k;
+  uint64_t b = 0;
+  // tables
+  b += dev_alloc(4 * L * E) + 2 * dev_alloc(4 * (uint64_t)C) + 2 * dev_alloc(8 * (uint64_t)log_capacity(C)) +
+       dev_alloc(4 * (uint64_t)C) + dev_alloc(32) + dev_alloc(8 * ST_COUNT);
+  // plans
+  const uint64_t per_plan = 4 * (PH_WORDS + 9 * E + 1 + 2 * rows) + 4 * rows;
+  b += dev_alloc(((per_plan + 255) & ~uint64_t(255)) * L);
+  // routing scratch, decode intermediate, FFN counters
+  b += dev_alloc(4 * (kMaxExperts / 32) + 4 * kMaxExperts + 64);
+  b += dev_alloc(4 * (uint64_t)std::min(g.max_tokens, kDecodeMaxTokens) * g.top_k * I);
+  b += dev_alloc(16);
+  if (g.max_tokens > kDecodeMaxTokens && prefill_supported((int)H, (int)I, g.wdtype, (int)E))
+    b += dev_alloc(2 * rows * I) + dev_alloc(2 * rows * H) + dev_alloc(4 * rows * H) + dev_alloc(4 * rows);
+  if (g.fetch_mode == FT_FETCH_COPY_ENGINE) b += dev_alloc(4 * kRing);
+  return b;
+}
+
 int capacity_bound(const ft_cache* c) {
   const long long rows = (long long)c->max_tokens * c->k;
   return (int)(2 * std::min<long long>(rows, c->E));
@@ -504,6 +546,32 @@ ft_status ft_cache_destroy(ft_cache* c) {
     }
   }
   delete c;
+  return FT_OK;
+}
+
+uint64_t ft_cache_overhead_bytes(const ft_cache_config* cfg, int64_t num_slots) {
+  if (!cfg || num_slots < 1 || check_config(*cfg) != FT_OK) return 0;
+  return cache_device_bytes(*cfg, num_slots);
+}
+
+ft_status ft_slots_for_budget(const ft_cache_config* cfg, uint64_t budget_bytes, int64_t* num_slots) {
+  if (!cfg || !num_slots) return fail(FT_ERR_INVALID_ARG, "null config or output pointer");
+  *num_slots = 0;
+  const ft_status st = check_config(*cfg);
+  if (st != FT_OK) return st;
+  const uint64_t eb = blob_bytes(cfg->hidden, cfg->inter, cfg->wdtype);
+  auto total = [&](int64_t C) { return (uint64_t)C * eb + cache_device_bytes(*cfg, C); };
+  int64_t lo = 0, hi = (int64_t)std::min<uint64_t>(budget_bytes / eb, INT32_MAX / 2);
+  while (lo < hi) {  // the most slots whose pool and tables fit the budget (total grows with C)
+    const int64_t mid = lo + (hi - lo + 1) / 2;
+    if (total(mid) <= budget_bytes) lo = mid;
+    else hi = mid - 1;
+  }
+  const long long bound = 2 * std::min<long long>((long long)cfg->max_tokens * cfg->top_k, cfg->num_experts);
+  if (lo < bound)
+    return fail(FT_ERR_CAPACITY, "a budget of %llu bytes holds %lld slots, below the capacity bound %lld",
+                (unsigned long long)budget_bytes, (long long)lo, bound);
+  *num_slots = lo;
   return FT_OK;
 }
 

@@ -17,7 +17,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (FT_FETCH_SM_PULL, FT_W_F32, ft_cache_create, ft_cache_destroy, ft_cache_resize, ft_expert_bytes,
+from . import (FT_FETCH_SM_PULL, FT_W_F32, ft_cache_create, ft_cache_destroy, ft_cache_overhead_bytes,
+               ft_cache_resize, ft_expert_bytes, ft_slots_for_budget,
                ft_fetch_misses, ft_get_copy_stream, ft_get_plan, ft_get_stats, ft_get_tables, ft_get_timing,
                ft_moe_forward, ft_reset_stats, ft_route_classify, ft_step_graph_create, ft_step_graph_destroy,
                ft_step_graph_launch, ft_step_graph_timing, ft_step_graph_trace, ft_synchronize, ft_timing_enable,
@@ -47,8 +48,46 @@ class ExpertCache:
         cfg = make_config(num_layers, num_experts, top_k, hidden, inter, wdtype, bank.data_ptr(),
                           bank.numel() * bank.element_size(), self.bank_blobs, max_tokens, fetch_mode, pull_ctas,
                           copy_streams, fetch_warps)
+        self.cfg = cfg
         self.handle = ft_cache_create(cfg, self.pool.data_ptr(), num_slots, self.stream.cuda_stream)
         self.copy_stream = torch.cuda.ExternalStream(ft_get_copy_stream(self.handle), device=self.device)
+
+    # ---- budget-driven sizing ---------------------------------------------
+    @staticmethod
+    def slots_for_budget(num_layers, num_experts, top_k, hidden, inter, wdtype, max_tokens, budget_bytes,
+                         fetch_mode=FT_FETCH_SM_PULL) -> int:
+        """The most slots whose pool plus the library's own device memory fit
+        in budget_bytes (ft_slots_for_budget)."""
+        cfg = make_config(num_layers, num_experts, top_k, hidden, inter, wdtype, 0, 0, 1, max_tokens, fetch_mode)
+        return ft_slots_for_budget(cfg, int(budget_bytes))
+
+    @staticmethod
+    def auto_budget(device="cuda:0", reserve_bytes=0) -> int:
+        """The free device memory now, minus what the caller keeps for other
+        work: the budget of an automatically sized cache."""
+        free, _ = torch.cuda.mem_get_info(torch.device(device))
+        return max(0, free - int(reserve_bytes))
+
+    @classmethod
+    def from_budget(cls, budget_bytes, num_layers, num_experts, top_k, hidden, inter, wdtype, max_tokens, bank,
+                    bank_blobs=None, fetch_mode=FT_FETCH_SM_PULL, **kw):
+        slots = cls.slots_for_budget(num_layers, num_experts, top_k, hidden, inter, wdtype, max_tokens,
+                                     budget_bytes, fetch_mode)
+        return cls(num_layers, num_experts, top_k, hidden, inter, wdtype, slots, max_tokens, bank, bank_blobs,
+                   fetch_mode=fetch_mode, **kw)
+
+    def device_bytes(self) -> int:
+        """Slot pool plus the library's device memory for the current size."""
+        return self.num_slots * self.eb + ft_cache_overhead_bytes(self.cfg, self.num_slots)
+
+    def resize_to_budget(self, budget_bytes):
+        """Move the cache, at a safe point, to the most slots the new budget
+        holds: into a new pool of that size (the old pool is released), so a
+        shrink gives the memory back.  Returns the new slot count."""
+        slots = ft_slots_for_budget(self.cfg, int(budget_bytes))
+        if slots != self.num_slots:
+            self.resize(slots, torch.empty(slots * self.eb, dtype=torch.uint8, device=self.device))
+        return slots
 
     # ---- thin wrappers ---------------------------------------------------
     def route_classify(self, layer, logits: torch.Tensor, topk_idx=None, topk_w=None):

@@ -141,6 +141,29 @@ typedef struct ft_plan_info {
 size_t ft_expert_bytes(int32_t hidden, int32_t inter, int32_t wdtype);
 
 /*
+ * Budget-driven sizing (the "automatic" cache size of the pages' runtime:
+ * "FreeToken vs vLLM on one RTX 3090", Runtime configurations; the cache is
+ * rebuilt when the VRAM budget changes: "FreeToken: Efficient Edge-Native MoE
+ * Serving ...", design paragraph).  No GPU work; usable before any device is
+ * touched.
+ *
+ * ft_cache_overhead_bytes: device bytes ft_cache_create allocates for a cache
+ * of `num_slots` slots with this configuration (slot tables, LRU log, plans,
+ * scratch, prefill buffers; each allocation rounded to 512 bytes), not
+ * counting the caller's slot pool.  0 for an invalid configuration.
+ *
+ * ft_slots_for_budget: the most slots C with C * expert_bytes plus the
+ * overhead of C slots within `budget_bytes` (a caller derives the budget from
+ * the free device memory minus what it keeps for everything else, and again
+ * when that changes; ft_cache_resize then moves the cache to the new size at a
+ * safe point).  Errors: FT_ERR_INVALID_ARG (configuration), FT_ERR_CAPACITY
+ * (the budget holds fewer slots than 2 * min(max_tokens * top_k,
+ * num_experts); *num_slots is 0).
+ */
+uint64_t ft_cache_overhead_bytes(const ft_cache_config* cfg, int64_t num_slots);
+ft_status ft_slots_for_budget(const ft_cache_config* cfg, uint64_t budget_bytes, int64_t* num_slots);
+
+/*
  * Create a cache over `num_slots` slots of the caller's device pool
  * `slot_pool` ([num_slots][expert_bytes], device, 256-byte aligned, owned by
  * the caller and valid until destroy or the next resize).  The cache starts

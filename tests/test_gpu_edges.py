@@ -183,3 +183,50 @@ def test_copy_thread_never_served_times_out_and_next_cache_works():
     from tests.harness import run_parity
     rep = run_parity(w, steps=4, fetch_mode=0)
     assert rep["events"] == 8
+
+
+def test_budget_shrink_and_regrow_mid_stream_matches_oracle():
+    """A 35B-shaped cache sized from a byte budget, shrunk to a smaller budget
+    after 10 steps (into a new, smaller pool: the memory goes back) and grown
+    to a larger one after 20, at safe points; decisions and tables against the
+    oracle given the same slot counts, fetched slots against the bank."""
+    w = W.QWEN35B_DECODE.replace(num_layers=6)
+    bank, n = make_bank(w, 256)
+    dev = torch.device("cuda:0")
+    eb = w.expert_bytes
+    budgets = [400 * eb, 130 * eb, 700 * eb]
+    c = ExpertCache.from_budget(budgets[0], w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, 1,
+                                bank, n, device=dev)
+    sizes = [c.num_slots]
+    assert c.device_bytes() <= budgets[0] < c.device_bytes() + eb
+    ref = ExpertCacheOracle(w.num_layers, w.num_experts, c.num_slots)
+    lg = W.router_logits(w.replace(steps=30))
+    x = torch.zeros((1, w.hidden), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((1, w.hidden), dtype=torch.float32, device=dev)
+    try:
+        for s in range(30):
+            if s in (10, 20):
+                slots = c.resize_to_budget(budgets[1 if s == 10 else 2])
+                ref.resize(slots)
+                sizes.append(slots)
+            for l in range(w.num_layers):
+                c.route_classify(l, torch.from_numpy(lg[s, l]).to(dev))
+                ev = ref.event(l, orouting.topk(lg[s, l], w.top_k))
+                p = c.plan(l)
+                assert p["miss_slot"].tolist() == ev.miss_slot.tolist(), (s, l)
+                assert p["evicted_key"].tolist() == ev.evicted_key.tolist(), (s, l)
+                c.fetch_misses(l)
+                c.moe_forward(l, x, y)
+            k2s, sk, ts = c.tables()
+            rk, rs, rt = ref.tables()
+            assert (k2s == rk).all() and (sk == rs).all() and (ts == rt).all(), f"step {s}"
+        assert sizes[1] < sizes[0] < sizes[2]
+        c.synchronize()
+        for slot in range(0, c.num_slots, 97):   # every fetched slot holds its key's blob
+            key = int(sk[slot])
+            if key >= 0:
+                got = c.pool[slot * eb:(slot + 1) * eb].cpu().numpy()
+                b = key % n
+                assert np.array_equal(got, bank.numpy()[b * eb:(b + 1) * eb]), slot
+    finally:
+        c.close()
