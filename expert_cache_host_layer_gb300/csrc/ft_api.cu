@@ -834,14 +834,14 @@ ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, v
   const Plan& pl = c->plans[layer];
   if (T > kDecodeMaxTokens) {  // prefill: grouped GEMMs
     if (!c->pf_yp)
-      return fail(FT_ERR_UNSUPPORTED, "T=%d > %d: the prefill path needs bf16 weights (H %% 128, I %% 128)", T,
+      return fail(FT_ERR_UNSUPPORTED, "T=%d > %d: the prefill path needs bf16 or fp8 weights (H %% 128, I %% 128)", T,
                   kDecodeMaxTokens);
     PrefillArgs p{};
     p.hdr = pl.hdr; p.unique_expert = pl.unique_expert; p.unique_slot = pl.unique_slot; p.u_offset = pl.u_offset;
     p.topk_idx = pl.topk_idx; p.topk_w = pl.topk_w; p.rows_by_u = pl.rows_by_u; p.pos = c->pf_pos;
     p.x = x; p.xp = c->pf_xp; p.h = c->pf_h; p.yp = c->pf_yp; p.y = static_cast<float*>(y);
     p.pool = static_cast<const uint8_t*>(c->pool); p.expert_bytes = (long long)c->eb;
-    p.H = c->H; p.I = c->I; p.k = c->k; p.T = T; p.E = c->E; p.status = c->tab.status;
+    p.H = c->H; p.I = c->I; p.k = c->k; p.T = T; p.E = c->E; p.status = c->tab.status; p.wdtype = c->wdtype;
     const bool tm = c->timing;
     if (tm) c->timers[PHASE_FFN].begin(c->compute);
     if (c->cap_ffn_ev) CU(cudaEventRecordWithFlags(c->cap_ffn_ev[2 * layer], c->compute, cudaEventRecordExternal));

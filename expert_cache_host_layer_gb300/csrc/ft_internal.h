@@ -181,6 +181,7 @@ struct PrefillArgs {
   long long expert_bytes;
   int32_t* status;           // sticky status word (bounded waits record FT_ERR_TIMEOUT)
   int H, I, k, T, E;
+  int wdtype;                // FT_W_BF16 or FT_W_FP8E4M3_B128
 };
 bool prefill_supported(int H, int I, int wdtype, int E);
 // marks (optional): events recorded before and after the gate/up GEMM, then

@@ -1,4 +1,4 @@
-// Prefill-path expert FFN (T > 8 tokens per layer event), bf16 weights: the
+// Prefill-path expert FFN (T > 8 tokens per layer event), bf16 or fp8 weights: the
 // token permutation, the two grouped GEMMs of the routed SwiGLU experts
 // (tcgen05 tensor cores, prefill_tc.cu) reading the weights straight from
 // their cache slots, and the combine.
@@ -122,7 +122,7 @@ int prefill_sms() {
 }  // namespace
 
 bool prefill_supported(int H, int I, int wdtype, int E) {
-  return wdtype == FT_W_BF16 && prefill_tc_supported(H, I) && E <= kMaxExperts;
+  return (wdtype == FT_W_BF16 || wdtype == FT_W_FP8E4M3_B128) && prefill_tc_supported(H, I) && E <= kMaxExperts;
 }
 
 cudaError_t launch_prefill_ffn(const PrefillArgs& a, int num_slots, cudaStream_t s, int* launches,

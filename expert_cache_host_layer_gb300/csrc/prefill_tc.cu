@@ -27,6 +27,16 @@
 // accumulator's columns [0, 128) are gate and [128, 256) up for the same 128 h
 // columns and SwiGLU needs no data exchange.
 //
+// fp8 weights (OCP e4m3 with one bf16 scale per 128 x 128 block): the tensor
+// cores multiply bf16 by bf16 here, because the activations stay bf16 (e4m3
+// activations would put about 4% error on each dot product).  So the producer
+// loads the fp8 B rows (64 bytes of each row per K block, 64-byte swizzle)
+// into the upper half of the stage's B area, and four converter warps (warps
+// 10-13) read them, multiply each by its block's scale (a K block of 64 lies
+// in one 128-wide scale block) and write bf16 into the 128-byte-swizzled
+// layout the MMA reads, over the whole B area (all reads happen before any
+// write: a named barrier separates them), then release the stage to the MMA.
+//
 // Every mbarrier wait is bounded (one second of %globaltimer).  A wait that
 // runs out records FT_ERR_TIMEOUT and sets a CTA-wide abort flag that ends
 // every later wait at once; the producer still waits (bounded) for the copies
@@ -39,6 +49,8 @@
 // "FreeToken: Efficient Edge-Native MoE Serving ...", ablation paragraph).
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <mutex>
 #include <set>
@@ -50,7 +62,9 @@ namespace ft {
 namespace {
 
 constexpr int kEpiWarps = 8;             // two per TMEM lane quarter, each taking half the columns
+constexpr int kCvtWarps = 4;             // fp8 weights: dequantising warps
 constexpr int kTcThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue
+constexpr int kTcThreadsFp8 = kTcThreads + kCvtWarps * 32;
 constexpr int kBM = 128;                 // grouped rows per tile (UMMA M)
 constexpr int kBK = 64;                  // K per ring stage: one 128-byte swizzle row of bf16
 constexpr int kStages = 3;
@@ -72,7 +86,7 @@ constexpr int kBoxBytes = 32 * 128;
 constexpr int kStageOutOff = kRingBytes;
 constexpr int kTableOff = kStageOutOff + kEpiWarps * 2 * kBoxBytes;
 constexpr int kBarOff = (kTableOff + kTableInts * 4 + 15) / 16 * 16;
-constexpr int kBarWords = 2 * kStages + 2 * 2 + 1;  // full, empty, tfull, tempty, drain
+constexpr int kBarWords = 3 * kStages + 2 * 2 + 1;  // full, empty, ready, tfull, tempty, drain
 constexpr int kTcSmem = kBarOff + kBarWords * 8 + 16 + 1024;  // + tmem holder, abort flag, alignment slack
 
 struct TcArgs {
@@ -87,6 +101,8 @@ struct TcArgs {
   int H, I, k, R;
   int n_tile;                  // UMMA N of this GEMM (gate/up 256; down 256 or 128)
   long long slot_rows;         // rows of one slot in the B tensor map (3I for gate/up, 3H for down)
+  const uint8_t* pool;         // fp8: the slots, for the block scales
+  long long expert_bytes;
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -136,6 +152,13 @@ __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int c0
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
           "r"(sa(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(sa(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(sa(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(sa(bar))
       : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -220,6 +243,7 @@ struct Smem {
   uint64_t* tfull;
   uint64_t* tempty;
   uint64_t* drain;
+  uint64_t* ready;   // fp8: the stage's B rows are dequantised
   uint32_t* tmem_holder;
   volatile int* abort_flag;
 };
@@ -238,6 +262,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.tfull = bars + 2 * kStages;
   s.tempty = bars + 2 * kStages + 2;
   s.drain = bars + 2 * kStages + 4;
+  s.ready = bars + 2 * kStages + 5;
   s.tmem_holder = reinterpret_cast<uint32_t*>(bars + kBarWords);
   s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_holder + 1);
   return s;
@@ -300,8 +325,8 @@ __device__ __forceinline__ TileInfo tile_info(const Smem& s, int n_u, int ntiles
 // else the down GEMM (A = h rows, B = Wd rows).  map_a and map_b load boxes of
 // 64 columns x 128 rows (x, h, Wg/Wu) or N rows (Wd); map_out stores 32-row
 // output boxes.
-template <bool kGateUp>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <bool kGateUp, bool kFp8>
+__global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_out, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -312,12 +337,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n_cols = kGateUp ? kH1 : a.n_tile;      // output columns per tile
   const int ntiles = (kGateUp ? a.I : a.H) / n_cols;
   const int KT = (kGateUp ? a.H : a.I) / kBK;
-  const uint32_t b_bytes = (uint32_t)N * kBK * 2;
+  const uint32_t b_bytes = (uint32_t)N * kBK * (kFp8 ? 1 : 2);  // bytes the producer loads into the B area
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       bar_init(&s.full[i], 1);
       bar_init(&s.empty[i], 1);
+      bar_init(&s.ready[i], kCvtWarps);
     }
     for (int i = 0; i < 2; ++i) {
       bar_init(&s.tfull[i], 1);
@@ -367,8 +393,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int c0 = kt * kBK;
         if (lane == 0) {
           tma_2d(A, &map_a, c0, t.p0, &s.full[st]);                              // 128 grouped x or h rows
-          tma_2d(B, &map_b, c0, (int)brow, &s.full[st]);                         // 128 Wg rows / N Wd rows
-          if (kGateUp) tma_2d(B + kBM * 128, &map_b, c0, (int)(brow + a.I), &s.full[st]);  // the same Wu rows
+          if (kFp8) {  // fp8 rows (64 bytes of each per K block) into the upper half of the B area
+            uint8_t* B8 = B + kBBytesMax / 2;
+            if (kGateUp) {
+              tma_3d(B8, &map_b, c0, t.n0, t.slot, &s.full[st]);                 // 128 Wg rows
+              tma_3d(B8 + kBM * 64, &map_b, c0, a.I + t.n0, t.slot, &s.full[st]);  // the same Wu rows
+            } else {
+              tma_3d(B8, &map_b, c0, t.n0, t.slot, &s.full[st]);                 // N Wd rows
+            }
+          } else {
+            tma_2d(B, &map_b, c0, (int)brow, &s.full[st]);                       // 128 Wg rows / N Wd rows
+            if (kGateUp) tma_2d(B + kBM * 128, &map_b, c0, (int)(brow + a.I), &s.full[st]);  // the same Wu rows
+          }
         }
       }
     }
@@ -389,10 +425,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t d = tmem + acc * kAccCols;
         for (int kt = 0; kt < KT; ++kt, ++it) {
           const int st = it % kStages;
-          if (!bwait(&s.full[st], (it / kStages) & 1, a.status, s.abort_flag)) {
+          if (!bwait(kFp8 ? &s.ready[st] : &s.full[st], (it / kStages) & 1, a.status, s.abort_flag)) {
             go = false;
             break;
           }
+          if (kFp8) bar_try(&s.full[st], (it / kStages) & 1);  // the A box landed too
           tc_fence_after();
           const uint32_t A = sa(s.ring + st * kStageBytes), B = A + kABytes;
 #pragma unroll
@@ -407,6 +444,87 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bwait(s.drain, 0, a.status, s.abort_flag, true);
     }
     __syncwarp();
+  } else if (warp >= 2 + kEpiWarps) {
+    // ------------------------------------------------------------ fp8 dequantising warps
+    if (kFp8) {
+      const int ctid = threadIdx.x - (2 + kEpiWarps) * 32;  // 0 .. 127: rows ctid and ctid + 128
+      const long long scale_off = 3LL * a.H * a.I;
+      const int hb = a.H / 128, ib = a.I / 128;
+      int it = 0;
+      bool go = true;
+      for (int tile = blockIdx.x; tile < total && go; tile += gridDim.x) {
+        const TileInfo t = tile_info(s, n_u, ntiles, tile, n_cols);
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(a.pool + (long long)t.slot * a.expert_bytes + scale_off);
+        for (int kt = 0; kt < KT; ++kt, ++it) {
+          const int st = it % kStages;
+          bool ok = true;
+          if (lane == 0) ok = bwait(&s.full[st], (it / kStages) & 1, a.status, s.abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (ok) bar_try(&s.full[st], (it / kStages) & 1);
+          uint8_t* B = s.ring + st * kStageBytes + kABytes;
+          const uint8_t* B8 = B + kBBytesMax / 2;
+          const int kb = (kt * kBK) >> 7;  // the 128-wide K block of this stage
+          uint4 raw[2][4];
+          float scl[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int r = ctid + h * 128;
+            scl[h] = 0.0f;
+            if (ok && r < N) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)  // 64-byte-swizzled fp8 row r
+                raw[h][i] = *reinterpret_cast<const uint4*>(B8 + r * 64 + ((i ^ ((r >> 1) & 3)) << 4));
+              int idx;
+              if (kGateUp)  // rows < 128: Wg rows n0.., else the same Wu rows
+                idx = (r < kBM ? 0 : ib * hb) + (t.n0 >> 7) * hb + kb;
+              else          // Wd rows n0 + r
+                idx = 2 * ib * hb + ((t.n0 + r) >> 7) * ib + kb;
+              scl[h] = __uint_as_float((uint32_t)__ldg(sc + idx) << 16);
+            }
+          }
+          // every fp8 row is read before any bf16 row is written; the four warps
+          // agree on stopping (a wait that ran out anywhere) at the same barrier
+          uint32_t stop;
+          asm volatile(
+              "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, 4, %2, q;\n\t"
+              "selp.u32 %0, 1, 0, p;\n\t}"
+              : "=r"(stop)
+              : "r"((uint32_t)(!ok || *s.abort_flag)), "n"(kCvtWarps * 32)
+              : "memory");
+          if (stop) {
+            go = false;
+            break;
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int r = ctid + h * 128;
+            if (r < N) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {  // 16 fp8 -> 16 bf16 = two 16-byte chunks of the bf16 row
+                const uint32_t w4[4] = {raw[h][i].x, raw[h][i].y, raw[h][i].z, raw[h][i].w};
+                uint32_t o[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[q] & 0xffffu), __NV_E4M3);
+                  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[q] >> 16), __NV_E4M3);
+                  const float2 fa = __half22float2(__half2(lo)), fb = __half22float2(__half2(hi));
+                  const __nv_bfloat162 ba = __floats2bfloat162_rn(fa.x * scl[h], fa.y * scl[h]);
+                  const __nv_bfloat162 bb = __floats2bfloat162_rn(fb.x * scl[h], fb.y * scl[h]);
+                  o[2 * q] = *reinterpret_cast<const uint32_t*>(&ba);
+                  o[2 * q + 1] = *reinterpret_cast<const uint32_t*>(&bb);
+                }
+                const int j0 = 2 * i, j1 = 2 * i + 1;  // 128-byte-swizzled bf16 row r
+                *reinterpret_cast<uint4*>(B + r * 128 + ((j0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4*>(B + r * 128 + ((j1 ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+              }
+            }
+          }
+          fence_async_smem();  // the tensor core reads these rows through the async proxy
+          __syncwarp();
+          if (lane == 0) bar_arrive(&s.ready[st]);
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     // Warp w reads TMEM lanes 32 (w % 4) .. (the tile's rows 32 q ..) and half
@@ -550,6 +668,31 @@ bool prefill_tc_supported(int H, int I) {
   return H % 128 == 0 && I % kH1 == 0 && H % kBK == 0 && I % kBK == 0;
 }
 
+// A 3D byte tensor map over rows of the slot pool: [slot][row < rows][cols
+// bytes] starting `offset` bytes into each slot, boxes of 64 bytes x box_rows
+// rows x 1 slot, 64-byte swizzle (the fp8 weight rows of a K block).
+cudaError_t fp8_rows_map(CUtensorMap* m, const uint8_t* pool, long long offset, unsigned long long cols,
+                         unsigned long long rows, int num_slots, long long expert_bytes, uint32_t box_rows) {
+  static EncodeTiled enc = nullptr;
+  if (!enc) enc = reinterpret_cast<EncodeTiled>(driver_fn("cuTensorMapEncodeTiled"));
+  if (!enc) return cudaErrorNotSupported;
+  const uint8_t* base = pool + offset;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (expert_bytes & 15) || (cols & 15)) return cudaErrorInvalidValue;
+  const cuuint64_t dims[3] = {cols, rows, (cuuint64_t)num_slots};
+  const cuuint64_t strides[2] = {cols, (cuuint64_t)expert_bytes};
+  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <bool kGateUp, bool kFp8>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(tc_gemm_kernel<kGateUp, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+}
+
 cudaError_t launch_prefill_gemms(const PrefillArgs& p, int num_slots, cudaStream_t st, const cudaEvent_t* marks) {
   static std::mutex mu;
   static std::set<int> ready;  // devices whose kernel attributes are set
@@ -559,42 +702,55 @@ cudaError_t launch_prefill_gemms(const PrefillArgs& p, int num_slots, cudaStream
   {
     std::lock_guard<std::mutex> lk(mu);
     if (!ready.count(dev)) {
-      e = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+      e = set_smem_attr<true, false>();
+      if (e == cudaSuccess) e = set_smem_attr<false, false>();
+      if (e == cudaSuccess) e = set_smem_attr<true, true>();
+      if (e == cudaSuccess) e = set_smem_attr<false, true>();
       if (e != cudaSuccess) return e;
       ready.insert(dev);
     }
   }
+  const bool fp8 = p.wdtype == FT_W_FP8E4M3_B128;
+  if (!fp8 && p.wdtype != FT_W_BF16) return cudaErrorNotSupported;
   const int H = p.H, I = p.I, R = p.T * p.k;
   TcArgs a{};
   a.hdr = p.hdr; a.u_offset = p.u_offset; a.unique_slot = p.unique_slot; a.rows_by_u = p.rows_by_u;
   a.topk_w = p.topk_w; a.h = static_cast<__nv_bfloat16*>(p.h); a.yp = p.yp; a.status = p.status;
   a.H = H; a.I = I; a.k = p.k; a.R = R;
+  a.pool = p.pool; a.expert_bytes = p.expert_bytes;
   CUtensorMap mx, mw1, mh, mwd, mh_out, myp_out;
   // xp [R][H]: the x rows in grouped order
   if ((e = bf16_map(&mx, p.xp, H, R, 2ull * H, kBK, kBM)) != cudaSuccess) return e;
-  // the pool as rows of H: Wg rows [s*3I, s*3I + I), Wu rows [s*3I + I, s*3I + 2I)
-  if ((e = bf16_map(&mw1, p.pool, H, 3ull * I * num_slots, 2ull * H, kBK, kBM)) != cudaSuccess) return e;
   // h [R][I]
   if ((e = bf16_map(&mh, p.h, I, R, 2ull * I, kBK, kBM)) != cudaSuccess) return e;
-  // the pool as rows of I: Wd rows [s*3H + 2H, s*3H + 3H)
   const int n2 = H % 256 == 0 ? 256 : 128;
-  if ((e = bf16_map(&mwd, p.pool, I, 3ull * H * num_slots, 2ull * I, kBK, n2)) != cudaSuccess) return e;
+  if (fp8) {
+    // Wg, Wu rows of every slot: [slot][2I rows][H bytes]; Wd rows: [slot][H rows][I bytes]
+    if ((e = fp8_rows_map(&mw1, p.pool, 0, H, 2ull * I, num_slots, p.expert_bytes, kBM)) != cudaSuccess) return e;
+    if ((e = fp8_rows_map(&mwd, p.pool, 2LL * H * I, I, H, num_slots, p.expert_bytes, n2)) != cudaSuccess) return e;
+  } else {
+    // the pool as rows of H: Wg rows [s*3I, s*3I + I), Wu rows [s*3I + I, s*3I + 2I)
+    if ((e = bf16_map(&mw1, p.pool, H, 3ull * I * num_slots, 2ull * H, kBK, kBM)) != cudaSuccess) return e;
+    // the pool as rows of I: Wd rows [s*3H + 2H, s*3H + 3H)
+    if ((e = bf16_map(&mwd, p.pool, I, 3ull * H * num_slots, 2ull * I, kBK, n2)) != cudaSuccess) return e;
+  }
   // output boxes of 32 rows x 128 bytes: h (64 bf16 columns) and yp (32 fp32 columns)
   if ((e = bf16_map(&mh_out, p.h, I, R, 2ull * I, 64, 32)) != cudaSuccess) return e;
   if ((e = tmap_2d(&myp_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.yp, H, R, 4ull * H, 32, 32)) != cudaSuccess) return e;
   const int grid = tc_sms();
+  const int threads = fp8 ? kTcThreadsFp8 : kTcThreads;
   a.n_tile = kN1;
   a.slot_rows = 3LL * I;
   if (marks && (e = cudaEventRecord(marks[0], st)) != cudaSuccess) return e;
-  tc_gemm_kernel<true><<<grid, kTcThreads, kTcSmem, st>>>(mx, mw1, mh_out, a);
+  if (fp8) tc_gemm_kernel<true, true><<<grid, threads, kTcSmem, st>>>(mx, mw1, mh_out, a);
+  else tc_gemm_kernel<true, false><<<grid, threads, kTcSmem, st>>>(mx, mw1, mh_out, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (marks && (e = cudaEventRecord(marks[1], st)) != cudaSuccess) return e;
   a.n_tile = n2;
   a.slot_rows = 3LL * H;
   if (marks && (e = cudaEventRecord(marks[2], st)) != cudaSuccess) return e;
-  tc_gemm_kernel<false><<<grid, kTcThreads, kTcSmem, st>>>(mh, mwd, myp_out, a);
+  if (fp8) tc_gemm_kernel<false, true><<<grid, threads, kTcSmem, st>>>(mh, mwd, myp_out, a);
+  else tc_gemm_kernel<false, false><<<grid, threads, kTcSmem, st>>>(mh, mwd, myp_out, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (marks && (e = cudaEventRecord(marks[3], st)) != cudaSuccess) return e;
   return cudaSuccess;

@@ -90,3 +90,38 @@ def static_profile(events, num_experts: int, num_slots: int, profile_events: int
             unique += 1
             misses += (l * num_experts + int(e)) not in resident
     return misses, unique
+
+
+def previous_step_prefetch_coverage(topk_trace, num_layers: int, num_experts: int, num_slots: int):
+    """How many of the global LRU cache's misses a prefetch predicted from the
+    previous step's routing could have hidden (the FreeToken MoE inference
+    guide, "FreeToken 解决的问题": the engine predicts the experts the next
+    token needs and streams them early).
+
+    Reading: the predictor for (step s, layer l) is the unique experts layer l
+    used at step s-1; a predicted expert helps only if it is not resident when
+    step s reaches layer l (a resident one would hit anyway).  The cache is the
+    method's global LRU (ExpertCacheOracle).  Returns (misses, covered,
+    predicted_not_resident): the misses, the misses that were predicted, and
+    the predicted experts that were not resident (the prefetch traffic it would
+    add, useful or not)."""
+    from .cache import ExpertCacheOracle
+    steps = topk_trace.shape[0]
+    cache = ExpertCacheOracle(num_layers, num_experts, num_slots)
+    prev = [None] * num_layers
+    misses = covered = wasted_or_useful = 0
+    for s in range(steps):
+        for l in range(num_layers):
+            pred = prev[l]
+            if pred is not None:
+                not_res = {int(e) for e in pred if cache.key_to_slot[l * num_experts + int(e)] < 0}
+            else:
+                not_res = set()
+            ev = cache.event(l, topk_trace[s, l])
+            m = {int(e) for e in ev.miss_expert}
+            if s > 0:  # the first step has no predictor
+                misses += len(m)
+                covered += len(m & not_res)
+                wasted_or_useful += len(not_res)
+            prev[l] = np.unique(topk_trace[s, l])
+    return misses, covered, wasted_or_useful

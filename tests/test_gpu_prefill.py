@@ -50,3 +50,24 @@ def test_prefill_16k_chunk(double_buffer):
     assert rep["events"] == 2 and rep["ffn_checked"] == 2
     assert rep["stats"]["unique_experts"] > 300  # nearly all 256 experts per layer
     print("prefill 16k:", {k: rep[k] for k in ("max_err", "max_rms_err", "miss_rate")})
+
+
+# fp8 e4m3 experts with bf16 128 x 128 block scales on the prefill path: the
+# weights are dequantised to bf16 (times their block's scale) in shared memory
+# and multiplied on the tensor cores.  A small shape (ragged tiles, 64 experts)
+# and the DeepSeek-V4-Flash-shaped layer dimensions (hidden 4096,
+# intermediate 2048) with 32 experts so the fp64 oracle stays quick.
+FP8_SMALL_PREFILL = W.DSV4_DECODE.replace(name="fp8-prefill-1024x512", num_layers=2, num_experts=64, hidden=1024,
+                                          inter=512, tokens=300, steps=1, num_slots=256, routing=W.ROUTE_ZIPF_IID,
+                                          resize_step=-1, bank_blobs=0)
+FP8_DSV4_DIMS_PREFILL = W.DSV4_DECODE.replace(name="fp8-prefill-dsv4-dims", num_layers=2, num_experts=32,
+                                              tokens=256, steps=1, num_slots=64, routing=W.ROUTE_ZIPF_IID,
+                                              resize_step=-1, bank_blobs=0)
+
+
+@pytest.mark.parametrize("w", [FP8_SMALL_PREFILL, FP8_DSV4_DIMS_PREFILL], ids=["1024x512", "dsv4-dims"])
+def test_fp8_prefill_parity(w):
+    from tests.harness import run_parity
+    rep = run_parity(w, steps=1, double_buffer=True)
+    assert rep["events"] == 2 and rep["ffn_checked"] == 2 and rep["slots_checked"] > 0
+    print("fp8 prefill:", {k: rep[k] for k in ("max_err", "max_rms_err", "miss_rate")})

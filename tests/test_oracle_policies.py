@@ -94,3 +94,54 @@ def test_policies_on_the_35b_decode_trace(w):
     print(f"miss rates ({w.name}, {w.num_slots} slots, {steps} steps):", {k: round(v, 4) for k, v in rates.items()})
     # the method's cache beats placing whole layers (the offload the pages compare against)
     assert rates["global_lru"] < rates["static_layers"]
+
+
+def test_previous_step_prefetch_coverage_against_a_textbook_lru():
+    """k = 1 traces (the global LRU is then a textbook LRU over keys): a miss
+    is covered when layer l used the same expert at the previous step and it
+    was evicted since; recomputed here with an OrderedDict, on traces small
+    enough that such evictions happen."""
+    import collections
+
+    from oracle import policies
+    rng = np.random.default_rng(5)
+    for L, E, C in ((4, 8, 3), (5, 6, 3), (6, 8, 4)):  # fewer slots than layers: last step's experts get evicted
+        steps = 60
+        tr = rng.integers(0, E, size=(steps, L, 1, 1)).astype(np.int32)
+        misses, covered, predicted = policies.previous_step_prefetch_coverage(tr, L, E, C)
+        lru = collections.OrderedDict()
+        m = c = p = 0
+        for s in range(steps):
+            for l in range(L):
+                key = l * E + int(tr[s, l, 0, 0])
+                prev = l * E + int(tr[s - 1, l, 0, 0]) if s > 0 else None
+                pred_missing = prev is not None and prev not in lru
+                hit = key in lru
+                if hit:
+                    lru.move_to_end(key)
+                else:
+                    if len(lru) == C:
+                        lru.popitem(last=False)
+                    lru[key] = True
+                if s > 0:
+                    m += not hit
+                    c += (not hit) and pred_missing and prev == key
+                    p += pred_missing
+        assert (misses, covered, predicted) == (m, c, p), (L, E, C)
+        assert covered > 0
+
+
+def test_previous_step_prefetch_covers_no_miss_on_the_decode_trace():
+    """On the 35B-shaped decode routing (70% of each step's experts kept from
+    the previous step) the previous step's experts are still resident when the
+    next step reaches their layer, so a predictor built from them covers none
+    of the misses: they are the newly drawn experts."""
+    from oracle import policies
+    from oracle import routing
+    w = W.QWEN35B_DECODE
+    steps = 40
+    lg = W.router_logits(w.replace(steps=steps))
+    tr = np.stack([np.stack([routing.topk(lg[s, l], w.top_k) for l in range(w.num_layers)]) for s in range(steps)])
+    misses, covered, predicted = policies.previous_step_prefetch_coverage(tr, w.num_layers, w.num_experts,
+                                                                          w.num_slots)
+    assert misses > 0 and covered == 0 and predicted == 0
