@@ -352,7 +352,7 @@ def prefill_measure(dev, peak_tflops, steps=2):
     return out
 
 
-def prefill_gemm_only(dev, peak_tflops, reps=6):
+def prefill_gemm_only(dev, peak_tflops, reps=6, w=None):
     """The prefill chunk's two tensor-core GEMMs alone, through the public
     API: a one-layer cache of 512 slots routes the same 16,384-token chunk
     every event, so after the first event every unique expert hits and no
@@ -362,7 +362,7 @@ def prefill_gemm_only(dev, peak_tflops, reps=6):
     import torch
 
     from expert_cache_host_layer_gb300.pipeline import ExpertCache, pinned_bank
-    w = W.QWEN35B_PREFILL
+    w = w or W.QWEN35B_PREFILL
     T, E, k = w.tokens, w.num_experts, w.top_k
     bank = pinned_bank(E * w.expert_bytes)
     synth.expert_blobs(w.seed, w.hidden, w.inter, w.wdtype, np.arange(E), out_ptr=bank.data_ptr())
@@ -395,7 +395,9 @@ def prefill_gemm_only(dev, peak_tflops, reps=6):
     g2 = tm["gemm2_ms"] / max(1, tm["gemm2_n"])
     ffn = tm["ffn_ms"] / max(1, tm["ffn_n"])
     both = (f1 + f2) / ((g1 + g2) / 1e3) / 1e12
-    return {"kernel": "tc_gemm_kernel (tcgen05.mma kind::f16, TMA tiles): gate/up + SwiGLU, then down",
+    return {"kernel": "tc_gemm_kernel (tcgen05.mma kind::f16, TMA tiles): gate/up + SwiGLU, then down"
+                      + (" (fp8 weights dequantised to bf16 in shared memory)" if w.wdtype == synth.W_FP8 else ""),
+            "workload": f"{w.name}: {T} tokens, hidden {w.hidden}, inter {w.inter}, {E} experts, top-{k}",
             "bound": "tensor", "unit": "TFLOP/s", "peak": peak_tflops, "launches": tm["gemm1_n"],
             "gateup_ms": g1, "down_ms": g2, "ffn_ms": ffn, "unique_experts": n_u,
             "gateup_tflops": f1 / (g1 / 1e3) / 1e12, "down_tflops": f2 / (g2 / 1e3) / 1e12,
@@ -405,6 +407,12 @@ def prefill_gemm_only(dev, peak_tflops, reps=6):
             "flop_per_layer": f1 + f2,
             "how": "one-layer cache, the same 16,384-token chunk every event (all hits after the first); "
                    "CUDA events around each GEMM launch on the compute stream"}
+
+
+# The prefill chunk at the DeepSeek-V4-Flash-shaped layer dimensions with fp8 block-scaled experts (no
+# configured workload prefills this shape: the chunk size is the 35B prefill's).
+FP8_PREFILL = W.DSV4_DECODE.replace(name="dsv4flash-shape-prefill-16k-fp8", tokens=16384, steps=1,
+                                    routing=W.ROUTE_ZIPF_IID, resize_step=-1, bank_blobs=0)
 
 
 def ffn_only(w, dev, peak, layers=16, steps=32):
@@ -769,6 +777,7 @@ def run_ours(args, w):
             blocks[wb.name] = decode_block(wb, dev, bank, n_blobs, args, max(8, K // 2), 3, fill, 16, peak)
         blocks["prefill"] = prefill_measure(dev, measured_bf16_tflops())
         blocks["prefill"]["gemm_alone"] = prefill_gemm_only(dev, measured_bf16_tflops())
+        blocks["prefill"]["gemm_alone_fp8"] = prefill_gemm_only(dev, measured_bf16_tflops(), w=FP8_PREFILL)
         wd = W.DSV4_DECODE
         dbank = pinned_bank(wd.blobs * wd.expert_bytes)
         synth.expert_blobs(wd.seed, wd.hidden, wd.inter, wd.wdtype, np.arange(wd.blobs), out_ptr=dbank.data_ptr())
@@ -845,7 +854,8 @@ def main():
         return
     if args.prefill_gemm_only:
         import torch
-        print(json.dumps(prefill_gemm_only(torch.device("cuda", 0), measured_bf16_tflops())), flush=True)
+        pw = FP8_PREFILL if w.wdtype == synth.W_FP8 else None
+        print(json.dumps(prefill_gemm_only(torch.device("cuda", 0), measured_bf16_tflops(), w=pw)), flush=True)
         return
     if args.impl == "reference":
         run_reference(args, w)

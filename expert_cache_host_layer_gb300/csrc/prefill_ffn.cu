@@ -6,7 +6,7 @@
 //   group_rows:  the T*k (token, pick) rows sorted by unique expert (ascending
 //                row within an expert): rows_by_u, and pos[row] = its place
 //   permute:     xp[p] = x[t] for the grouped row p of (t, j), so each GEMM
-//                tile's A rows are one contiguous block
+//                tile's A rows are one contiguous block (fp16 for fp8 experts)
 //   gate/up:     h[p][i] = silu(Wg[i] . x_t) * (Wu[i] . x_t)  (bf16 h; p the
 //                grouped place of row (t, j))
 //   down:        yp[p][c] = w_tj * (Wd[c] . h[p])              (fp32)
@@ -20,6 +20,7 @@
 // 3090", "Why the performance differs"; the prefill chunk of "FreeToken:
 // Efficient Edge-Native MoE Serving ...", ablation paragraph).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "ft_internal.h"
 
@@ -78,7 +79,14 @@ __global__ void __launch_bounds__(kPThreads) group_rows_kernel(PrefillArgs a) {
 }
 
 // ---------------------------------------------------------------- permute
-// One warp per grouped row: xp[p] = x[rows_by_u[p] / k], 16-byte chunks.
+// One warp per grouped row: xp[p] = x[rows_by_u[p] / k], 16-byte chunks; for
+// fp8 experts (whose GEMMs multiply fp16 operands) the bf16 values are
+// converted to fp16 on the way.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <bool kF16>
 __global__ void __launch_bounds__(kPThreads) permute_rows_kernel(PrefillArgs a) {
   const int R = a.T * a.k, n16 = a.H / 8;
   const int lane = threadIdx.x & 31;
@@ -88,7 +96,11 @@ __global__ void __launch_bounds__(kPThreads) permute_rows_kernel(PrefillArgs a) 
     const int t = __ldg(&a.rows_by_u[p]) / a.k;
     const uint4* src = x + (long long)t * n16;
     uint4* dst = xp + (long long)p * n16;
-    for (int i = lane; i < n16; i += 32) dst[i] = __ldg(src + i);
+    for (int i = lane; i < n16; i += 32) {
+      uint4 v = __ldg(src + i);
+      if (kF16) v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+      dst[i] = v;
+    }
   }
 }
 
@@ -130,7 +142,10 @@ cudaError_t launch_prefill_ffn(const PrefillArgs& a, int num_slots, cudaStream_t
   group_rows_kernel<<<a.E, kPThreads, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  permute_rows_kernel<<<8 * prefill_sms(), kPThreads, 0, s>>>(a);
+  if (a.wdtype == FT_W_FP8E4M3_B128)
+    permute_rows_kernel<true><<<8 * prefill_sms(), kPThreads, 0, s>>>(a);
+  else
+    permute_rows_kernel<false><<<8 * prefill_sms(), kPThreads, 0, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = launch_prefill_gemms(a, num_slots, s, marks)) != cudaSuccess) return e;
   combine_kernel<<<4 * prefill_sms(), kPThreads, 0, s>>>(a);
