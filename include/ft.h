@@ -246,11 +246,14 @@ ft_status ft_fetch_misses(ft_cache* cache, int32_t layer);
  *   y  device [T][H]: float32; fully overwritten
  * T must equal the T of the layer's last ft_route_classify.  The compute
  * stream first waits for the layer's fetch.  T <= 8 (decode) runs one fused
- * kernel per layer (gate/up, SwiGLU, down, combine; in SM-pull mode it also
- * copies the next requested layer's misses).  Larger T (prefill, bf16
- * weights only, hidden % 128 and inter % 64) groups the rows by expert and
- * runs the gate/up + SwiGLU and down projections as grouped tensor-core GEMMs,
- * then combines each token's picks in pick order.
+ * kernel per layer (gate/up, SwiGLU, down and the combine, adding into y in
+ * no fixed order, so y is reproducible to fp32 rounding; in SM-pull mode it
+ * also copies the next requested layer's misses), launched as a programmatic
+ * dependent of the kernel before it on the stream.  Larger T (prefill; bf16
+ * or fp8 weights, hidden and inter multiples of 128) groups the rows by
+ * expert and runs the gate/up + SwiGLU and down projections as grouped
+ * tensor-core GEMMs (fp8 weights dequantised to fp16 with their block scales
+ * on the way), then combines each token's picks in pick order.
  * Errors: FT_ERR_INVALID_ARG, FT_ERR_STATE (no fetch issued for the layer's
  * current plan), FT_ERR_UNSUPPORTED (a prefill T with other weight types or
  * shapes, or a cache created with max_tokens <= 8), FT_ERR_CUDA.
