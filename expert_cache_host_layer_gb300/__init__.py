@@ -5,8 +5,10 @@ plain pointers and sizes through ctypes; all work happens in the CUDA
 library.  PyTorch (when used) only provides device memory and streams: pass
 ``tensor.data_ptr()`` and ``stream.cuda_stream``.
 
-Importing this package loads ``_build/libft.so``.  If it was not built, the
-import fails with an error saying how to build it: there is no fallback.
+Importing this package loads ``_build/libft.so`` (with FT_CHECKED=1 in the
+environment, the bounds-checked build ``_build_checked/libft.so``).  If it was
+not built, the import fails with an error saying how to build it: there is no
+fallback.
 """
 from __future__ import annotations
 
@@ -14,7 +16,8 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libft.so")
+CHECKED = os.environ.get("FT_CHECKED", "") == "1"
+LIB_PATH = os.path.join(_HERE, "_build_checked" if CHECKED else "_build", "libft.so")
 
 FT_OK, FT_ERR_INVALID_ARG, FT_ERR_CUDA, FT_ERR_OOM, FT_ERR_CAPACITY, FT_ERR_STATE, FT_ERR_TIMEOUT, \
     FT_ERR_CHECKED, FT_ERR_UNSUPPORTED = range(9)
@@ -66,7 +69,7 @@ def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libft is not built ({LIB_PATH} missing); run "
                           "`python -c 'import __graft_entry__ as g; g.build()'` or "
-                          "`python expert_cache_host_layer_gb300/build.py`")
+                          "`python expert_cache_host_layer_gb300/build.py" + (" --checked`" if CHECKED else "`"))
     lib = ctypes.CDLL(LIB_PATH)
     P, I32, I64, U8P = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.POINTER(ctypes.c_uint8)
     st = ctypes.c_int
@@ -88,6 +91,8 @@ def _load():
         "ft_get_pool": (st, [P, ctypes.POINTER(P), ctypes.POINTER(I64)]),
         "ft_get_copy_stream": (st, [P, ctypes.POINTER(P)]),
         "ft_debug_pause_copies": (st, [P, I32]),
+        "ft_checked_build": (I32, []),
+        "ft_debug_set_key_slot": (st, [P, I32, I32]),
         "ft_timing_enable": (st, [P, I32]),
         "ft_get_timing": (st, [P, ctypes.POINTER(ft_timing)]),
         "ft_step_graph_create": (st, [P, P, P, P, I32, I32, I32, ctypes.POINTER(P)]),
@@ -222,6 +227,14 @@ def ft_get_copy_stream(cache: int) -> int:
 
 def ft_debug_pause_copies(cache: int, paused: bool):
     _check(_lib.ft_debug_pause_copies(cache, int(bool(paused))), "ft_debug_pause_copies")
+
+
+def ft_checked_build() -> bool:
+    return bool(_lib.ft_checked_build())
+
+
+def ft_debug_set_key_slot(cache: int, key: int, slot: int):
+    _check(_lib.ft_debug_set_key_slot(cache, int(key), int(slot)), "ft_debug_set_key_slot")
 
 
 def ft_timing_enable(cache: int, on: bool):

@@ -2,9 +2,13 @@
 
 Each .cu file compiles to an object in parallel; the objects link into
 ``_build/libft.so`` with the CUDA runtime linked statically, so the library
-loads next to any PyTorch build without sharing its runtime.
+loads next to any PyTorch build without sharing its runtime.  The checked
+build (``-DFT_CHECKED``: kernels bounds-check the table and plan indices they
+dereference and report FT_ERR_CHECKED instead of touching memory out of
+range) goes to ``_build_checked/libft.so``; the package loads it when the
+environment has FT_CHECKED=1.
 
-    python expert_cache_host_layer_gb300/build.py [--force]
+    python expert_cache_host_layer_gb300/build.py [--force] [--checked]
 """
 from __future__ import annotations
 
@@ -20,6 +24,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libft.so")
+OUT_CHECKED = os.path.join(HERE, "_build_checked")
+LIB_CHECKED = os.path.join(OUT_CHECKED, "libft.so")
 INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -41,24 +47,26 @@ def _deps():
     return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.h"))) + [os.path.join(INCLUDE, "ft.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OUT, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    out, lib = (OUT_CHECKED, LIB_CHECKED) if checked else (OUT, LIB)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(out, exist_ok=True)
     cc = nvcc()
     srcs = _sources()
-    objs = [os.path.join(OUT, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(out, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    extra = ["-DFT_CHECKED"] if checked else []
 
     def compile_one(src_obj):
         src, obj = src_obj
-        cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr}")
@@ -69,14 +77,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for msg in ex.map(compile_one, zip(srcs, objs)):
             if verbose and msg.strip():
                 print(msg, file=sys.stderr)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-lpthread", "-ldl", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, checked="--checked" in sys.argv))

@@ -87,13 +87,25 @@ struct DownLayout {
   }
 };
 
-// Copies the plan arrays the FFN kernels index into shared memory.
-__device__ __forceinline__ void stage_plan(const FfnArgs& a, int n_u, int32_t* s_slot, int32_t* s_off,
-                                           int32_t* s_rows) {
+// Copies the plan arrays the FFN kernels index into shared memory; in checked
+// builds, nonzero if one of this thread's entries is out of range.
+__device__ __forceinline__ int stage_plan(const FfnArgs& a, int n_u, int32_t* s_slot, int32_t* s_off,
+                                          int32_t* s_rows) {
   const int rows = a.T * a.k;
-  for (int i = threadIdx.x; i < n_u; i += blockDim.x) s_slot[i] = __ldg(&a.unique_slot[i]);
-  for (int i = threadIdx.x; i <= n_u; i += blockDim.x) s_off[i] = __ldg(&a.u_offset[i]);
-  for (int i = threadIdx.x; i < rows; i += blockDim.x) s_rows[i] = __ldg(&a.rows_by_u[i]);
+  int bad = 0;
+  for (int i = threadIdx.x; i < n_u; i += blockDim.x) {
+    s_slot[i] = __ldg(&a.unique_slot[i]);
+    if (kChecked) bad |= s_slot[i] < 0 || s_slot[i] >= a.num_slots;
+  }
+  for (int i = threadIdx.x; i <= n_u; i += blockDim.x) {
+    s_off[i] = __ldg(&a.u_offset[i]);
+    if (kChecked) bad |= s_off[i] < 0 || s_off[i] > rows;
+  }
+  for (int i = threadIdx.x; i < rows; i += blockDim.x) {
+    s_rows[i] = __ldg(&a.rows_by_u[i]);
+    if (kChecked) bad |= s_rows[i] < 0 || s_rows[i] >= rows;
+  }
+  return bad;
 }
 
 // ---------------------------------------------------------------- gate_up
@@ -129,12 +141,11 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_kernel(FfnArgs a) {
     const uint4* src = static_cast<const uint4*>(a.x);
     for (int i = threadIdx.x; i < n16; i += kThreads) reinterpret_cast<uint4*>(xs)[i] = src[i];
   }
-  stage_plan(a, n_u, p_slot, p_off, p_rows);
-  __syncthreads();
+  const bool plan_ok = plan_sync(stage_plan(a, n_u, p_slot, p_off, p_rows), a.status);
   pdl_launch_dependents();  // the down kernel may start streaming Wd now
 
   const int units_per_u = I / P;
-  const int n_units = n_u * units_per_u;
+  const int n_units = plan_ok ? n_u * units_per_u : 0;
   const long long row_bytes = (long long)H * WSZ;
   const uint32_t block_bytes = (uint32_t)(P * row_bytes);
 
@@ -235,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(FfnArgs a) {
   uint64_t* empty = full + NS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the plan was written by route_classify, which completed before the primary kernel started
-  const int n_u = min(__ldg(&a.hdr[PH_UNIQUE]), a.max_unique);
+  const int n_u_plan = min(__ldg(&a.hdr[PH_UNIQUE]), a.max_unique);
   if (threadIdx.x == 0) {
     wait_ready_flag(a);
     for (int s = 0; s < NS; ++s) {
@@ -244,8 +255,7 @@ __global__ void __launch_bounds__(kThreads, 2) down_kernel(FfnArgs a) {
     }
     mbar_init_fence();
   }
-  stage_plan(a, n_u, p_slot, p_off, p_rows);
-  __syncthreads();
+  const int n_u = plan_sync(stage_plan(a, n_u_plan, p_slot, p_off, p_rows), a.status) ? n_u_plan : 0;
   const int n_rb = H / RD;
   const long long row_bytes = (long long)I * WSZ;
   const uint32_t stage_bytes = (uint32_t)(RD * row_bytes);

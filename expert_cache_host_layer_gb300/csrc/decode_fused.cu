@@ -24,9 +24,9 @@
 // is reproducible only to fp32 rounding.
 //
 // The kernel is launched as a programmatic dependent of the kernel before it
-// on the stream: its barrier set-up and plan staging overlap the end of the
-// previous layer's FFN, and griddepcontrol.wait precedes every read of the
-// slots, x and y.
+// on the stream: its barrier set-up, plan staging and the first bulk copies
+// of a hit expert's rows overlap the end of the previous layer's FFN;
+// griddepcontrol.wait precedes every read of a missed expert's slot, x and y.
 //
 // Up to four more warps per CTA copy the NEXT layer's missed blobs from the
 // host bank (mapped pinned memory, read over the host link) into their victim
@@ -138,7 +138,8 @@ __device__ __forceinline__ uint4 ld_host16(const uint4* p) {  // streamed once: 
 // CTA i % grid.
 __device__ __forceinline__ void copy_next_misses(const PullArgs& p, int ct, int nw) {
   const long long kItem16 = (long long)nw * 32 * kCopyUnroll;
-  const int n_miss = __ldcg(&p.hdr[PH_MISS]);
+  int n_miss = __ldcg(&p.hdr[PH_MISS]);
+  if (!checked_ok(n_miss >= 0 && n_miss <= p.E, p.status)) n_miss = 0;
   const long long eb16 = p.expert_bytes >> 4;
   const long long per_blob = (eb16 + kItem16 - 1) / kItem16;
   const long long items = (long long)n_miss * per_blob;
@@ -149,6 +150,7 @@ __device__ __forceinline__ void copy_next_misses(const PullArgs& p, int ct, int 
     const long long c = it - (long long)m * per_blob;
     const int e = __ldcg(&p.miss_expert[m]);
     const int slot = __ldcg(&p.miss_slot[m]);
+    if (!checked_ok(slot >= 0 && slot < p.num_slots && e >= 0 && e < p.E, p.status)) continue;
     const long long blob = ((long long)p.layer * p.E + e) % p.bank_blobs;
     const uint4* src = bank + blob * eb16 + c * kItem16;
     uint4* dst = pool + (long long)slot * eb16 + c * kItem16;
@@ -196,14 +198,14 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bar_off);
   uint64_t* empty = full + kStagesF;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStagesF);
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem + lay.ring_off) + 1023) &
-                                             ~uintptr_t(1023));
+  // 1024-aligned by an offset from the shared array (not through an integer
+  // cast), so the compiler keeps the ring's loads shared-memory loads
+  uint8_t* ring = smem + lay.ring_off + ((1024u - (smem_addr(smem + lay.ring_off) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_u = min(__ldg(&a.hdr[PH_UNIQUE]), a.max_unique);
   const long long row_g = (long long)H * WSZ;
   const long long scale_off = 3LL * H * I * WSZ;
   const int upe = I / R;  // units per expert
-  const int n_units = n_u * upe;
   const int n_boxes = H / kBoxRows;
   const int event = __ldg(&a.hdr[PH_EVENT]);
   unsigned* done_ctr = a.gbar + 2;
@@ -218,15 +220,43 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
     *abort_flag = 0;
     mbar_init_fence();
   }
-  for (int i = threadIdx.x; i < n_u; i += kThreadsF) p_slot[i] = __ldg(&a.unique_slot[i]);
-  for (int i = threadIdx.x; i <= n_u; i += kThreadsF) p_off[i] = __ldg(&a.u_offset[i]);
+  int bad = 0;  // checked builds: a plan index out of range
+  for (int i = threadIdx.x; i < n_u; i += kThreadsF) {
+    p_slot[i] = __ldg(&a.unique_slot[i]);
+    if (kChecked) bad |= p_slot[i] < 0 || p_slot[i] >= a.num_slots;
+  }
+  for (int i = threadIdx.x; i <= n_u; i += kThreadsF) {
+    p_off[i] = __ldg(&a.u_offset[i]);
+    if (kChecked) bad |= p_off[i] < 0 || p_off[i] > rows_total;
+  }
   for (int i = threadIdx.x; i < rows_total; i += kThreadsF) {
     p_rows[i] = __ldg(&a.rows_by_u[i]);
     p_w[i] = __ldg(&a.topk_w[i]);
+    if (kChecked) bad |= p_rows[i] < 0 || p_rows[i] >= rows_total;
   }
-  __syncthreads();
-  pdl_launch_dependents();  // the next layer's FFN may queue up behind this one
+  // a bad plan is reported and computes nothing (the copy warps check their own indices)
+  const int n_units = plan_sync(bad, a.status) ? n_u * upe : 0;
+  // The first unit's Wg/Wu rows start streaming before the previous kernel is
+  // known to be complete when its expert was a hit: nothing writes a hit's
+  // slot now (the copies of this event go to its misses' victims; those of
+  // earlier events finished before the kernel before this one passed its own
+  // griddepcontrol.wait, which precedes its launch_dependents).
+  int i_pre = 0;
+  if (threadIdx.x == kCons * 32 && a.hit && (int)blockIdx.x < n_units) {
+    const int u = blockIdx.x / upe;
+    if (__ldg(&a.hit[u])) {
+      const int r0 = (blockIdx.x - u * upe) * R;
+      const uint8_t* blob = a.pool + (long long)p_slot[u] * a.expert_bytes;
+      const uint32_t b = (uint32_t)(P * row_g);
+      for (int r = r0; r < r0 + R && i_pre < kStagesF; r += P, ++i_pre) {
+        mbar_expect_tx(&full[i_pre], 2 * b);
+        bulk_g2s(ring + (size_t)i_pre * kStageF, blob + r * row_g, b, &full[i_pre]);
+        bulk_g2s(ring + (size_t)i_pre * kStageF + b, blob + ((long long)I + r) * row_g, b, &full[i_pre]);
+      }
+    }
+  }
   pdl_wait_primary();       // the previous kernel (and every slot write it made) is complete
+  pdl_launch_dependents();  // the next layer's FFN may queue up behind this one
   {
     const int n16 = T * H * act_bytes / 16;
     const uint4* src = static_cast<const uint4*>(a.x);
@@ -256,6 +286,7 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
         const int slot = p_slot[u];
         const uint8_t* blob = a.pool + (long long)slot * a.expert_bytes;
         for (int r = r0; r < r0 + R && go; r += P, ++i) {  // phase A: P Wg rows, then the same P Wu rows
+          if (i < i_pre) continue;  // issued before griddepcontrol.wait
           const int s = i % kStagesF;
           if (!stage_free(s)) {
             go = false;

@@ -25,7 +25,8 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 }
 
 __global__ void __launch_bounds__(kThreads) pull_misses_kernel(PullArgs a) {
-  const int n_miss = __ldcg(&a.hdr[PH_MISS]);
+  int n_miss = __ldcg(&a.hdr[PH_MISS]);
+  if (!checked_ok(n_miss >= 0 && n_miss <= a.E, a.status)) n_miss = 0;
   const long long eb16 = a.expert_bytes >> 4;
   const long long chunks_per_blob = (eb16 + kChunk16 - 1) / kChunk16;
   const long long items = (long long)n_miss * chunks_per_blob;
@@ -36,6 +37,7 @@ __global__ void __launch_bounds__(kThreads) pull_misses_kernel(PullArgs a) {
     const long long c = it - (long long)m * chunks_per_blob;
     const int e = __ldcg(&a.miss_expert[m]);
     const int slot = __ldcg(&a.miss_slot[m]);
+    if (!checked_ok(slot >= 0 && slot < a.num_slots && e >= 0 && e < a.E, a.status)) continue;
     const long long blob = ((long long)a.layer * a.E + e) % a.bank_blobs;
     const uint4* src = bank + blob * eb16 + c * kChunk16;
     uint4* dst = pool + (long long)slot * eb16 + c * kChunk16;

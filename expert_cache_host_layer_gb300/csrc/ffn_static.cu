@@ -21,6 +21,7 @@
 // kernels overlap on the GPU (different streams, or different host threads)
 // race on the array and produce garbage.  Serialise them on one stream.
 #include <algorithm>
+#include <climits>
 #include <mutex>
 #include <string>
 
@@ -184,7 +185,7 @@ extern "C" ft_status ft_moe_decode_ffn_static(int32_t hidden, int32_t inter, int
   FfnArgs f{};
   f.hdr = hdr; f.unique_slot = unique_slot; f.u_offset = u_offset; f.rows_by_u = rows_by_u; f.topk_w = topk_w;
   f.x = x; f.y = static_cast<float*>(y); f.pool = static_cast<const uint8_t*>(slot_pool);
-  f.expert_bytes = (long long)eb;
+  f.expert_bytes = (long long)eb; f.num_slots = (int)std::min<long long>(num_slots, INT_MAX);
   f.H = hidden; f.I = inter; f.k = top_k; f.T = T; f.wdtype = wdtype; f.h = h;
   f.max_unique = (int)std::min<long long>(rows, num_experts);
   f.status = status;

@@ -343,6 +343,7 @@ ft_status launch_pull(ft_cache* c, int layer) {
   p.hdr = pl.hdr; p.miss_expert = pl.miss_expert; p.miss_slot = pl.miss_slot;
   p.layer = layer; p.E = c->E; p.bank_blobs = c->cfg.bank_blobs; p.bank = c->bank_dev;
   p.pool = c->pool; p.expert_bytes = (long long)c->eb;
+  p.num_slots = (int)c->C; p.status = c->tab.status;
   const int ctas = c->cfg.pull_ctas > 0 ? c->cfg.pull_ctas : 64;
   if (c->timing) c->timers[PHASE_FETCH].begin(c->copy[0]);
   if (c->cap_fetch_ev) CU(cudaEventRecordWithFlags(c->cap_fetch_ev[2 * layer], c->copy[0], cudaEventRecordExternal));
@@ -396,6 +397,7 @@ ft_status device_status(ft_cache* c) {
 
 ft_status alloc_tables(Tables& t, int64_t C, int num_keys, bool with_keys) {
   t.num_slots = (int32_t)C;
+  t.num_keys = num_keys;
   if (with_keys) CU(cudaMalloc(&t.key_to_slot, sizeof(int32_t) * num_keys));
   CU(cudaMalloc(&t.slot_key, sizeof(int32_t) * C));
   CU(cudaMalloc(&t.slot_ts, sizeof(int32_t) * C));
@@ -857,7 +859,7 @@ ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, v
     return FT_OK;
   }
   FfnArgs f{};
-  f.hdr = pl.hdr; f.unique_slot = pl.unique_slot; f.u_offset = pl.u_offset; f.rows_by_u = pl.rows_by_u;
+  f.hdr = pl.hdr; f.unique_slot = pl.unique_slot; f.hit = pl.hit; f.u_offset = pl.u_offset; f.rows_by_u = pl.rows_by_u;
   f.topk_w = pl.topk_w; f.x = x; f.y = static_cast<float*>(y); f.pool = static_cast<const uint8_t*>(c->pool);
   f.expert_bytes = (long long)c->eb; f.num_slots = (int)c->C;
   f.H = c->H; f.I = c->I; f.k = c->k; f.T = T; f.wdtype = c->wdtype; f.h = c->h_buf;
@@ -876,6 +878,7 @@ ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, v
     f.nx.hdr = pn.hdr; f.nx.miss_expert = pn.miss_expert; f.nx.miss_slot = pn.miss_slot;
     f.nx.layer = nx; f.nx.E = c->E; f.nx.bank_blobs = c->cfg.bank_blobs; f.nx.bank = c->bank_dev;
     f.nx.pool = c->pool; f.nx.expert_bytes = (long long)c->eb;
+    f.nx.num_slots = (int)c->C; f.nx.status = c->tab.status;
     f.fetch_warps = c->cfg.fetch_warps > 0 ? c->cfg.fetch_warps : kDefaultFetchWarps;
     if (c->cap_fetch_ev) CU(cudaEventRecordWithFlags(c->cap_fetch_ev[2 * nx], c->compute, cudaEventRecordExternal));
   }
@@ -930,7 +933,7 @@ ft_status ft_cache_resize(ft_cache* c, void* new_pool, int64_t new_num_slots) {
   if (pa.type != cudaMemoryTypeDevice) return fail(FT_ERR_INVALID_ARG, "new_pool is not device memory");
   Tables nt{};
   nt.key_to_slot = c->tab.key_to_slot;
-  if (alloc_tables(nt, new_num_slots, 0, false) != FT_OK) {
+  if (alloc_tables(nt, new_num_slots, c->L * c->E, false) != FT_OK) {
     free_tables(nt, false);
     return FT_ERR_OOM;
   }
@@ -1056,6 +1059,17 @@ ft_status ft_debug_pause_copies(ft_cache* c, int32_t paused) {
   if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
   if (c->cfg.fetch_mode != FT_FETCH_COPY_ENGINE) return fail(FT_ERR_STATE, "the cache has no copy thread");
   c->copies_paused.store(paused != 0, std::memory_order_release);
+  return FT_OK;
+}
+
+int32_t ft_checked_build(void) { return kChecked ? 1 : 0; }
+
+ft_status ft_debug_set_key_slot(ft_cache* c, int32_t key, int32_t slot) {
+  if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
+  if (!kChecked) return fail(FT_ERR_STATE, "only the bounds-checked build takes a corrupted slot table");
+  if (key < 0 || (long long)key >= (long long)c->L * c->E) return fail(FT_ERR_INVALID_ARG, "key %d out of range", key);
+  CU(cudaDeviceSynchronize());
+  CU(cudaMemcpy(c->tab.key_to_slot + key, &slot, sizeof slot, cudaMemcpyHostToDevice));
   return FT_OK;
 }
 

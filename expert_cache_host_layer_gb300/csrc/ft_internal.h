@@ -11,9 +11,35 @@ namespace ft {
 
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
-constexpr int kDecodeMaxTokens = 8;
+constexpr int kDecodeMaxTokens = 8;   // T above this takes the grouped-GEMM path
 constexpr int kMaxFetchWarps = 4;      // copy warps of the fused decode FFN kernel
-constexpr int kDefaultFetchWarps = 2;  // of which take part by default  // T above this takes the grouped-GEMM path
+constexpr int kDefaultFetchWarps = 2;  // of which take part by default
+
+// Bounds checks of the table and plan indices the kernels dereference, in
+// builds made with -DFT_CHECKED: an index out of its range raises
+// FT_ERR_CHECKED in the sticky status word and the kernel skips that access
+// (no trap).  In other builds the checks compile away.
+#ifdef FT_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+__device__ __forceinline__ bool checked_ok(bool in_range, int32_t* status) {
+  if (!kChecked || in_range) return true;
+  if (status) atomicCAS(status, 0, (int)FT_ERR_CHECKED);
+  return false;
+}
+// __syncthreads after a CTA staged a plan; in checked builds also whether no
+// thread found an index out of range in what it staged (and the report).
+__device__ __forceinline__ bool plan_sync(int bad, int32_t* status) {
+  if (!kChecked) {
+    __syncthreads();
+    return true;
+  }
+  const bool ok = !__syncthreads_or(bad);
+  if (threadIdx.x == 0) checked_ok(ok, status);
+  return ok;
+}
 
 // Stats slots in the device counter array.
 enum { ST_EVENTS = 0, ST_UNIQUE, ST_HITS, ST_MISSES, ST_EVICT, ST_BYTES, ST_COUNT };
@@ -46,6 +72,7 @@ struct Tables {
   long long* stats;      // [ST_COUNT]
   int32_t num_slots;
   int32_t log_cap;
+  int32_t num_keys;      // L*E
 };
 // Log capacity for C slots: room for the tombstones of many events between
 // compactions (a power of two).
@@ -131,12 +158,15 @@ struct PullArgs {
   const void* bank;  // device address of the host bank
   void* pool;
   long long expert_bytes;
+  int num_slots;
+  int32_t* status;   // sticky status word (FT_ERR_CHECKED in checked builds)
 };
 cudaError_t launch_pull_misses(const PullArgs& a, int ctas, cudaStream_t s);
 
 struct FfnArgs {
   const int32_t* hdr;
   const int32_t* unique_slot;
+  const int32_t* hit;        // [n_unique] 1: the expert was in its slot before this event (no copy writes it now)
   const int32_t* u_offset;
   const int32_t* rows_by_u;
   const float* topk_w;

@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kPThreads) group_rows_kernel(PrefillArgs a) {
     int p = carry + before + x - cnt;
 #pragma unroll
     for (int i = 0; i < kGRows; ++i)
-      if (idx[i] == e) {
+      if (idx[i] == e && checked_ok(p >= 0 && p < rows, a.status)) {
         a.rows_by_u[p] = r0 + i;
         a.pos[r0 + i] = p;
         ++p;
@@ -93,7 +93,9 @@ __global__ void __launch_bounds__(kPThreads) permute_rows_kernel(PrefillArgs a) 
   const uint4* x = static_cast<const uint4*>(a.x);
   uint4* xp = static_cast<uint4*>(a.xp);
   for (int p = (blockIdx.x * kPThreads + threadIdx.x) >> 5; p < R; p += (gridDim.x * kPThreads) >> 5) {
-    const int t = __ldg(&a.rows_by_u[p]) / a.k;
+    const int row = __ldg(&a.rows_by_u[p]);
+    if (!checked_ok(row >= 0 && row < R, a.status)) continue;
+    const int t = row / a.k;
     const uint4* src = x + (long long)t * n16;
     uint4* dst = xp + (long long)p * n16;
     for (int i = lane; i < n16; i += 32) {
@@ -114,6 +116,7 @@ __global__ void __launch_bounds__(kPThreads) combine_kernel(PrefillArgs a) {
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < a.k; ++j) {
       const int p = __ldg(&a.pos[t * a.k + j]);
+      if (!checked_ok(p >= 0 && p < a.T * a.k, a.status)) continue;
       const float4 v = __ldcg(reinterpret_cast<const float4*>(a.yp + (long long)p * a.H) + q);
       s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
     }

@@ -108,6 +108,7 @@ struct TcArgs {
   long long slot_rows;         // rows of one slot in the B tensor map (3I for gate/up, 3H for down)
   const uint8_t* pool;         // fp8: the slots, for the block scales
   long long expert_bytes;
+  int num_slots;
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -256,7 +257,9 @@ struct Smem {
 
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
   Smem s;
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  // aligned by an offset from the shared array itself (not through an integer
+  // cast), so the compiler keeps every access derived from it a shared one
+  uint8_t* base = raw + ((1024u - (sa(raw) & 1023u)) & 1023u);
   s.ring = base;
   s.out = base + kStageOutOff;
   s.s_off = reinterpret_cast<int*>(base + kTableOff);
@@ -275,11 +278,22 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
 }
 
 // Tile table: s_off = u_offset, s_pre[u] = m-tiles of the experts before u,
-// s_slot = slot of each unique expert; warp 0 scans.  Returns the m-tile total.
+// s_slot = slot of each unique expert; warp 0 scans.  Returns the m-tile total
+// (0 for a plan that fails the checked builds' range checks).
 __device__ int build_table(const TcArgs& a, int n_u, const Smem& s) {
-  for (int u = threadIdx.x; u <= n_u; u += blockDim.x) s.s_off[u] = __ldg(&a.u_offset[u]);
-  for (int u = threadIdx.x; u < n_u; u += blockDim.x) s.s_slot[u] = __ldg(&a.unique_slot[u]);
-  __syncthreads();
+  int bad = kChecked && n_u < 0;
+  for (int u = threadIdx.x; u <= n_u; u += blockDim.x) {
+    s.s_off[u] = __ldg(&a.u_offset[u]);
+    if (kChecked) bad |= s.s_off[u] < 0 || s.s_off[u] > a.R;
+  }
+  for (int u = threadIdx.x; u < n_u; u += blockDim.x) {
+    s.s_slot[u] = __ldg(&a.unique_slot[u]);
+    if (kChecked) bad |= s.s_slot[u] < 0 || s.s_slot[u] >= a.num_slots;
+  }
+  if (!plan_sync(bad, a.status)) {
+    __syncthreads();  // the same barrier count as the table scan below
+    return 0;
+  }
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     const int per = (n_u + 31) / 32;
@@ -728,7 +742,7 @@ cudaError_t launch_prefill_gemms(const PrefillArgs& p, int num_slots, cudaStream
   a.hdr = p.hdr; a.u_offset = p.u_offset; a.unique_slot = p.unique_slot; a.rows_by_u = p.rows_by_u;
   a.topk_w = p.topk_w; a.h = static_cast<__nv_bfloat16*>(p.h); a.yp = p.yp; a.status = p.status;
   a.H = H; a.I = I; a.k = p.k; a.R = R;
-  a.pool = p.pool; a.expert_bytes = p.expert_bytes;
+  a.pool = p.pool; a.expert_bytes = p.expert_bytes; a.num_slots = num_slots;
   CUtensorMap mx, mw1, mh, mwd, mh_out, myp_out;
   // xp [R][H]: the x rows in grouped order
   if ((e = bf16_map(&mx, p.xp, H, R, 2ull * H, kBK, kBM)) != cudaSuccess) return e;

@@ -53,6 +53,10 @@ __global__ void __launch_bounds__(kThreads) resize_tables_kernel(ResizeArgs a) {
   int32_t* keep = reinterpret_cast<int32_t*>(a.old_tab.log[cur ^ 1]);  // scratch: 1 = survives
   int32_t* free_list = reinterpret_cast<int32_t*>(a.new_tab.log[1]);   // scratch: free slots below C'
 
+  if (kChecked) {  // every slot gets its keep flag from its live log entry; a corrupt log must not leave stale ones
+    for (int s = tid; s < C; s += kThreads) keep[s] = 0;
+    __syncthreads();
+  }
   // occupied count
   int occ_local = 0;
   for (int s = tid; s < C; s += kThreads) occ_local += a.old_tab.slot_key[s] >= 0;
@@ -67,6 +71,7 @@ __global__ void __launch_bounds__(kThreads) resize_tables_kernel(ResizeArgs a) {
     int s = -1, occ = 0;
     if ((uint32_t)tid < n) {
       s = lg[(base + tid) & qmask].x;
+      if (s >= 0 && !checked_ok(s < C && a.old_tab.slot_key[s] < a.old_tab.num_keys, a.old_tab.status)) s = -1;
       occ = s >= 0 && a.old_tab.slot_key[s] >= 0;
     }
     int tot;
@@ -121,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) resize_tables_kernel(ResizeArgs a) {
     const int mv = s < C && keep[s];
     int tot;
     const int r = block_excl_scan(mv, s_warp, tot);
-    if (mv) {
+    if (mv && checked_ok(n_movers + r < nfree, a.old_tab.status)) {
       const int d = free_list[n_movers + r];
       const int key = a.old_tab.slot_key[s];
       a.new_tab.slot_key[d] = key;

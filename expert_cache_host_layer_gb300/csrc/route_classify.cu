@@ -64,6 +64,14 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int& total) {
   return before + x - v;
 }
 
+// key_to_slot[key]; in checked builds a slot out of range, or one whose
+// slot_key is not the key, is reported and read as absent.
+__device__ __forceinline__ int checked_slot(const Tables& t, int key) {
+  const int s = t.key_to_slot[key];
+  if (!kChecked || s == -1) return s;
+  return checked_ok(s >= 0 && s < t.num_slots && t.slot_key[s] == key, t.status) ? s : -1;
+}
+
 template <int PL>  // logits per lane: E <= 32 * PL
 __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
   __shared__ uint32_t s_bits[kMaxExperts / 32];
@@ -100,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
     n_prev = *a.tab.pin_next ? *a.tab.last_nu : 0;
     head = *a.tab.head;
     tail = *a.tab.tail;
-    for (int e = tid; e < E; e += kThreads) s_k2s[e] = a.tab.key_to_slot[layer * E + e];
+    for (int e = tid; e < E; e += kThreads) s_k2s[e] = checked_slot(a.tab, layer * E + e);
   }
   __syncthreads();
 
@@ -183,7 +191,7 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
     n_prev = *a.tab.pin_next ? *a.tab.last_nu : 0;
     head = *a.tab.head;
     tail = *a.tab.tail;
-    for (int e = tid; e < E; e += kThreads) s_k2s[e] = a.tab.key_to_slot[layer * E + e];
+    for (int e = tid; e < E; e += kThreads) s_k2s[e] = checked_slot(a.tab, layer * E + e);
   }
   if (warp == 0) {
     int c = lane < nwords ? __popc(s_bits[lane]) : 0;
@@ -268,7 +276,9 @@ __global__ void __launch_bounds__(kThreads) route_classify_kernel(RouteArgs a) {
     uint32_t p = head;
     while (found < n_miss && p != pin_start) {
       const uint32_t n = min(32u, pin_start - p);
-      const int2 e = (uint32_t)lane < n ? lg[(p + lane) & qmask] : make_int2(-1, -1);
+      int2 e = (uint32_t)lane < n ? lg[(p + lane) & qmask] : make_int2(-1, -1);
+      if (kChecked && e.x >= 0 && !checked_ok(e.x < a.tab.num_slots && e.y >= -1 && e.y < a.tab.num_keys, a.tab.status))
+        e = make_int2(-1, -1);  // a corrupt entry is reported and never taken
       const bool live = (uint32_t)lane < n && e.x >= 0;
       const unsigned m = __ballot_sync(0xffffffffu, live);
       const int r = found + __popc(m & ((1u << lane) - 1u));

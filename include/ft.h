@@ -300,6 +300,21 @@ ft_status ft_get_copy_stream(ft_cache* cache, void** stream);
  * FT_ERR_STATE (SM-pull cache: no copy thread). */
 ft_status ft_debug_pause_copies(ft_cache* cache, int32_t paused);
 
+/* 1 if this library is the bounds-checked build (compiled with -DFT_CHECKED:
+ * every kernel checks the table and plan indices it dereferences; one out of
+ * range raises FT_ERR_CHECKED in the sticky device status, which the next
+ * synchronous call returns, and the access is skipped instead of made), else
+ * 0. */
+int32_t ft_checked_build(void);
+
+/* Test knob of the bounds-checked build: after the cache's work so far,
+ * overwrite the slot table entry of key (layer * E + expert) with `slot`, so
+ * that a test can hand the kernels an index out of range.  Errors:
+ * FT_ERR_INVALID_ARG (null cache, key outside [0, L*E)), FT_ERR_STATE (a
+ * build without the checks, whose kernels would read such a table out of
+ * range). */
+ft_status ft_debug_set_key_slot(ft_cache* cache, int32_t key, int32_t slot);
+
 /* Enable (1) or disable (0) per-phase CUDA-event timing; enabling clears the
  * totals.  ft_get_timing waits for the streams and returns the totals. */
 ft_status ft_timing_enable(ft_cache* cache, int32_t on);

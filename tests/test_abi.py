@@ -26,6 +26,12 @@ def lib_path():
     return __graft_entry__._build_module().build()
 
 
+@pytest.fixture(scope="module")
+def checked_lib_path(lib_path):
+    import __graft_entry__
+    return __graft_entry__._build_module().build(checked=True)
+
+
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("ft_cache_create", "ft_cache_resize", "ft_route_classify", "ft_fetch_misses",
@@ -37,6 +43,16 @@ def test_library_exports_every_declared_symbol(lib_path):
     lib = ctypes.CDLL(lib_path)
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
+
+
+def test_checked_build_exports_the_same_symbols(lib_path, checked_lib_path):
+    normal, checked = ctypes.CDLL(lib_path), ctypes.CDLL(checked_lib_path)
+    missing = [n for n in declared_functions() if not hasattr(checked, n)]
+    assert not missing, missing
+    assert normal.ft_checked_build() == 0 and checked.ft_checked_build() == 1
+    # the knob validates its arguments before anything else, in both builds
+    for lib in (normal, checked):
+        assert lib.ft_debug_set_key_slot(None, 0, 0) == 1  # FT_ERR_INVALID_ARG
 
 
 def test_binding_has_the_same_names(lib_path):
