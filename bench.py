@@ -294,7 +294,7 @@ def run_reference(args, w):
 # in-pipeline launches (64 GB bank, copies riding along) are not captured (too large for a full capture);
 # the all-hit launches of --ffn-only are (profiles/ffn_fused_kernel_qwen35b_decode_allhit.md).
 FFN_TRAFFIC_PER_LAUNCH = {}
-FFN_ONLY_TRAFFIC_PER_LAUNCH = {"qwen35b-a3b-shape-decode-b1": (50.390784e6 + 4.608e3 + 50.390272e6 + 2.304e3) / 2}
+FFN_ONLY_TRAFFIC_PER_LAUNCH = {"qwen35b-a3b-shape-decode-b1": (50.393088e6 + 11.776e3 + 50.393344e6 + 2.816e3) / 2}
 
 
 def prefill_measure(dev, peak_tflops, steps=2):
@@ -347,8 +347,9 @@ def prefill_measure(dev, peak_tflops, steps=2):
                 "miss_rate": (st1["misses"] - st0["misses"]) / max(1, st1["unique_experts"] - st0["unique_experts"])}
     finally:
         c.close()
-    out["note"] = ("step graph with timing event nodes, 40 layers, one 16,384-token chunk each; FFN = grouped "
-                   "mma.sync bf16 GEMMs (gate/up + SwiGLU, down) + combine; times from the event nodes")
+    out["note"] = ("step graph with timing event nodes, 40 layers, one 16,384-token chunk each; FFN = grouping, "
+                   "permutation, the two tcgen05 grouped GEMMs (gate/up + SwiGLU, down) and the combine; times "
+                   "from the event nodes")
     return out
 
 
@@ -396,7 +397,7 @@ def prefill_gemm_only(dev, peak_tflops, reps=6, w=None):
     ffn = tm["ffn_ms"] / max(1, tm["ffn_n"])
     both = (f1 + f2) / ((g1 + g2) / 1e3) / 1e12
     return {"kernel": "tc_gemm_kernel (tcgen05.mma kind::f16, TMA tiles): gate/up + SwiGLU, then down"
-                      + (" (fp8 weights dequantised to bf16 in shared memory)" if w.wdtype == synth.W_FP8 else ""),
+                      + (" (fp8 weights and their block scales dequantised to fp16 in shared memory; fp16 operands)" if w.wdtype == synth.W_FP8 else ""),
             "workload": f"{w.name}: {T} tokens, hidden {w.hidden}, inter {w.inter}, {E} experts, top-{k}",
             "bound": "tensor", "unit": "TFLOP/s", "peak": peak_tflops, "launches": tm["gemm1_n"],
             "gateup_ms": g1, "down_ms": g2, "ffn_ms": ffn, "unique_experts": n_u,
@@ -666,6 +667,17 @@ class DecodeBench:
         link_bytes = float(nmiss.sum()) * eb
         link_ms = float(ffn[carried > 0].sum() + np.asarray(fetch0)[nmiss[:, 0] > 0].sum())
         hbm_bytes = (nuniq + carried) * eb   # per FFN launch: expert reads + copied blobs written
+        # marginal host-link rate in the pipeline: each FFN window against the
+        # number of blobs its kernel copied (least squares); the slope is the
+        # link time one more blob costs, the intercept the window of an FFN
+        # that copies nothing (event nodes included)
+        xs, ys = carried.ravel().astype(np.float64), ffn.ravel().astype(np.float64)
+        marginal = None
+        if np.unique(xs).size > 1:
+            (b0, b1), *_ = np.linalg.lstsq(np.stack([np.ones_like(xs), xs], 1), ys, rcond=None)
+            marginal = {"us_per_blob": 1e3 * float(b1), "intercept_us": 1e3 * float(b0),
+                        "gbs": eb / (float(b1) / 1e3) / 1e9 if b1 > 0 else None,
+                        "launches_by_blobs_copied": {int(c): int((xs == c).sum()) for c in np.unique(xs)}}
         return {"steps": n, "ffn_us_per_launch": 1e3 * float(ffn.mean()),
                 "ffn_us_alone_in_pipeline": 1e3 * f_alone,
                 "ffn_ms_per_step": float(ffn.sum(axis=1).mean()),
@@ -674,6 +686,7 @@ class DecodeBench:
                 "gaps_ms_per_step": float(np.mean(step_ms) - ffn.sum(axis=1).mean() - np.mean(fetch0)),
                 "exposed_copy_ms_per_step": float(exposed.mean()),
                 "link_gbs": link_bytes / (link_ms / 1e3) / 1e9 if link_ms > 0 else None,
+                "link_marginal": marginal,
                 "miss_bytes_per_step": link_bytes / n,
                 "ffn_hbm_bytes_per_launch": float(hbm_bytes.mean()),
                 "ffn_read_bytes_per_launch": float((nuniq * eb).mean()),
@@ -814,18 +827,22 @@ def run_ours(args, w):
             "repeat_ms_per_step": [ms1 / K, ms2 / K],
             "expert_gemm_gbs": achieved,
             "exposed_copy_ms_per_step": tp["exposed_copy_ms_per_step"],
-            "miss_copy": {"gbs": tp["link_gbs"], "bytes_per_step": d["bytes_fetched"] / K,
+            "miss_copy": {"gbs": tp["link_gbs"], "gbs_marginal": (tp["link_marginal"] or {}).get("gbs"),
+                          "bytes_per_step": d["bytes_fetched"] / K,
                           "mode": ["copy_engine", "sm_pull"][args.fetch_mode], "link": link,
                           "link_time_needed_ms": need_ms, "ffn_time_ms": ffn_ms,
                           "fits_link_budget": (need_ms <= ffn_ms) if need_ms and ffn_ms else None,
                           "how": "gbs = miss bytes of the timing pass / the durations of the kernels that "
                                  "copied them (each fused FFN copies the next layer's misses; layer 0's come "
-                                 "from a pull kernel); fits_link_budget: miss bytes / sm_pull ceiling <= "
-                                 "L x FFN-alone time"},
+                                 "from a pull kernel; a window also holds the FFN's own start and the event "
+                                 "nodes); gbs_marginal = expert bytes / the extra window one more copied blob "
+                                 "costs (least squares over the timing pass's FFN launches); fits_link_budget: "
+                                 "miss bytes / sm_pull ceiling <= L x FFN-alone time"},
             "per_kernel": tp,
-            "roofline": {"kernel": "ffn_fused_kernel: one cooperative launch per layer (gate/up, SwiGLU, down, "
-                                   "combine) that also copies the next layer's misses; CUDA event nodes "
-                                   "around each launch in the timing pass",
+            "roofline": {"kernel": "ffn_fused_kernel: one launch per layer (gate/up, SwiGLU, down, combine; "
+                                   "a programmatic dependent of the previous layer's) that also copies the "
+                                   "next layer's misses; CUDA event nodes around each launch in the timing "
+                                   "pass",
                          "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": FFN_TRAFFIC_PER_LAUNCH.get(w.name),

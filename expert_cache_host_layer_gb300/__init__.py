@@ -92,6 +92,8 @@ def _load():
         "ft_get_copy_stream": (st, [P, ctypes.POINTER(P)]),
         "ft_debug_pause_copies": (st, [P, I32]),
         "ft_checked_build": (I32, []),
+        "ft_host_bank_alloc": (st, [ctypes.c_uint64, ctypes.POINTER(P)]),
+        "ft_host_bank_free": (st, [P]),
         "ft_debug_set_key_slot": (st, [P, I32, I32]),
         "ft_timing_enable": (st, [P, I32]),
         "ft_get_timing": (st, [P, ctypes.POINTER(ft_timing)]),
@@ -227,6 +229,16 @@ def ft_get_copy_stream(cache: int) -> int:
 
 def ft_debug_pause_copies(cache: int, paused: bool):
     _check(_lib.ft_debug_pause_copies(cache, int(bool(paused))), "ft_debug_pause_copies")
+
+
+def ft_host_bank_alloc(nbytes: int) -> int:
+    p = ctypes.c_void_p()
+    _check(_lib.ft_host_bank_alloc(int(nbytes), ctypes.byref(p)), "ft_host_bank_alloc")
+    return int(p.value)
+
+
+def ft_host_bank_free(host: int):
+    _check(_lib.ft_host_bank_free(host), "ft_host_bank_free")
 
 
 def ft_checked_build() -> bool:

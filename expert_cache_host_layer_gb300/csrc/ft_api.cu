@@ -1064,6 +1064,24 @@ ft_status ft_debug_pause_copies(ft_cache* c, int32_t paused) {
 
 int32_t ft_checked_build(void) { return kChecked ? 1 : 0; }
 
+ft_status ft_host_bank_alloc(uint64_t bytes, void** host) {
+  if (!host || bytes == 0) return fail(FT_ERR_INVALID_ARG, "null out pointer or zero bytes");
+  *host = nullptr;
+  const cudaError_t e = cudaHostAlloc(host, bytes, cudaHostAllocPortable | cudaHostAllocMapped);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    *host = nullptr;
+    return fail(FT_ERR_OOM, "cudaHostAlloc of %llu bytes: %s", (unsigned long long)bytes, cudaGetErrorString(e));
+  }
+  return FT_OK;
+}
+
+ft_status ft_host_bank_free(void* host) {
+  if (!host) return FT_OK;
+  CU(cudaFreeHost(host));
+  return FT_OK;
+}
+
 ft_status ft_debug_set_key_slot(ft_cache* c, int32_t key, int32_t slot) {
   if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
   if (!kChecked) return fail(FT_ERR_STATE, "only the bounds-checked build takes a corrupted slot table");

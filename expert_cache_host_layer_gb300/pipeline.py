@@ -18,6 +18,7 @@ from __future__ import annotations
 import torch
 
 from . import (FT_FETCH_SM_PULL, FT_W_F32, ft_cache_create, ft_cache_destroy, ft_cache_overhead_bytes,
+               ft_host_bank_alloc, ft_host_bank_free,
                ft_cache_resize, ft_expert_bytes, ft_slots_for_budget,
                ft_fetch_misses, ft_get_copy_stream, ft_get_plan, ft_get_stats, ft_get_tables, ft_get_timing,
                ft_moe_forward, ft_reset_stats, ft_route_classify, ft_step_graph_create, ft_step_graph_destroy,
@@ -206,8 +207,22 @@ class StepGraph:
 
 
 def pinned_bank(nbytes: int) -> torch.Tensor:
-    """A pinned host byte buffer for the expert bank (cudaHostAlloc through
-    torch).  Measured on GB300: the GPU reads such a bank over the host link
-    several times faster than a huge-page mapping page-locked afterwards with
-    cudaHostRegister, at the bank's scattered blob offsets."""
-    return torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    """A pinned, device-mapped host byte buffer of exactly nbytes for the
+    expert bank (ft_host_bank_alloc), as a CPU uint8 tensor that frees the
+    memory when the last view of it is gone.  (PyTorch's own pinned allocator
+    rounds a request up to a power of two: a 64.4 GB bank would pin 128 GB.)"""
+    import ctypes
+    import weakref
+
+    import numpy as np
+    ptr = ft_host_bank_alloc(nbytes)
+    raw = (ctypes.c_uint8 * nbytes).from_address(ptr)
+    weakref.finalize(raw, _free_bank, ptr)
+    return torch.from_numpy(np.ctypeslib.as_array(raw))
+
+
+def _free_bank(ptr: int):
+    try:
+        ft_host_bank_free(ptr)
+    except Exception:  # at interpreter exit the runtime may already be gone; the OS reclaims the memory
+        pass

@@ -141,6 +141,17 @@ typedef struct ft_plan_info {
 size_t ft_expert_bytes(int32_t hidden, int32_t inter, int32_t wdtype);
 
 /*
+ * The host tier: pinned, device-mapped host memory of exactly `bytes` bytes
+ * for an expert bank ("FreeToken: az VRAM ile büyük MoE modelleri", intro:
+ * the experts that do not fit stay in host RAM and are streamed from it),
+ * portable across the process's contexts, content undefined.  The caller owns
+ * it and frees it with ft_host_bank_free after the last cache that uses it is
+ * destroyed.  Errors: FT_ERR_INVALID_ARG (bytes 0, null out), FT_ERR_OOM.
+ */
+ft_status ft_host_bank_alloc(uint64_t bytes, void** host);
+ft_status ft_host_bank_free(void* host);
+
+/*
  * Budget-driven sizing (the "automatic" cache size of the pages' runtime:
  * "FreeToken vs vLLM on one RTX 3090", Runtime configurations; the cache is
  * rebuilt when the VRAM budget changes: "FreeToken: Efficient Edge-Native MoE
