@@ -561,6 +561,7 @@ class DecodeBench:
         self.StepGraph = StepGraph
         self.graphs = self._graphs(False)
         self.next = 0  # next step of the stream
+        self.last_launches = None  # (n_unique, blobs copied, window ms) per FFN launch of the last timing pass
 
     def _graphs(self, timing):
         return [self.StepGraph(self.cache, list(self.lg_buf), list(self.x_buf), list(self.y_buf), self.double,
@@ -657,16 +658,8 @@ class DecodeBench:
             for g in tg:
                 g.close()
         ffn, route, nmiss, nuniq = np.stack(ffn), np.stack(route), np.stack(nmiss), np.stack(nuniq)
-        # FFN windows that carried no copy: the FFN alone, in the pipeline
         carried = np.zeros_like(nmiss)
         carried[:, :-1] = nmiss[:, 1:]   # FFN(l) copies layer l+1's misses
-        plain = ffn[carried == 0]
-        f_alone = float(np.median(plain)) if plain.size else float(np.median(ffn))
-        exposed = np.clip(ffn - f_alone, 0.0, None).sum(axis=1) + np.asarray(fetch0)
-        # host link: bytes over the windows that moved them
-        link_bytes = float(nmiss.sum()) * eb
-        link_ms = float(ffn[carried > 0].sum() + np.asarray(fetch0)[nmiss[:, 0] > 0].sum())
-        hbm_bytes = (nuniq + carried) * eb   # per FFN launch: expert reads + copied blobs written
         # marginal host-link rate in the pipeline: each FFN window against the
         # number of blobs its kernel copied (least squares); the slope is the
         # link time one more blob costs, the intercept the window of an FFN
@@ -678,6 +671,22 @@ class DecodeBench:
             marginal = {"us_per_blob": 1e3 * float(b1), "intercept_us": 1e3 * float(b0),
                         "gbs": eb / (float(b1) / 1e3) / 1e9 if b1 > 0 else None,
                         "launches_by_blobs_copied": {int(c): int((xs == c).sum()) for c in np.unique(xs)}}
+        # the FFN alone, in the pipeline: the fit's intercept (at batch 4/8
+        # nearly every launch copies something, and the few that copy nothing
+        # are not typical), else the median window of the launches that copied
+        # nothing
+        plain = ffn[carried == 0]
+        if marginal and marginal["intercept_us"] > 0:
+            f_alone = marginal["intercept_us"] / 1e3
+        else:
+            f_alone = float(np.median(plain)) if plain.size else float(np.median(ffn))
+        exposed = np.clip(ffn - f_alone, 0.0, None).sum(axis=1) + np.asarray(fetch0)
+        # host link: bytes over the windows that moved them
+        link_bytes = float(nmiss.sum()) * eb
+        link_ms = float(ffn[carried > 0].sum() + np.asarray(fetch0)[nmiss[:, 0] > 0].sum())
+        hbm_bytes = (nuniq + carried) * eb   # per FFN launch: expert reads + copied blobs written
+        self.last_launches = (nuniq.ravel().astype(np.float64), carried.ravel().astype(np.float64),
+                              ffn.ravel().astype(np.float64))
         return {"steps": n, "ffn_us_per_launch": 1e3 * float(ffn.mean()),
                 "ffn_us_alone_in_pipeline": 1e3 * f_alone,
                 "ffn_ms_per_step": float(ffn.sum(axis=1).mean()),
@@ -691,7 +700,10 @@ class DecodeBench:
                 "ffn_hbm_bytes_per_launch": float(hbm_bytes.mean()),
                 "ffn_read_bytes_per_launch": float((nuniq * eb).mean()),
                 "note": "route runs on its own stream ahead of the FFNs (off the critical path); the FFN "
-                        "windows are serial on the compute stream: step = layer-0 pull + FFN windows + gaps"}
+                        "windows are serial on the compute stream: step = layer-0 pull + FFN windows + gaps; "
+                        "ffn_us_alone_in_pipeline = the intercept of link_marginal's fit (the window of an FFN "
+                        "that copies nothing, event nodes included); exposed copy = the windows beyond it + "
+                        "the layer-0 pull"}
 
     def close(self):
         for g in self.graphs:
@@ -699,7 +711,23 @@ class DecodeBench:
         self.cache.close()
 
 
-def decode_block(w, dev, bank, n_blobs, args, steps, warmup, fill, timing_steps, peak, resize=None):
+def bound_of_launches(launches, eb, hbm_gbs, link_gbs):
+    """Each FFN launch's lower bound: its expert reads at the HBM peak or the
+    blobs it copies at the host link's ceiling, whichever takes longer; the
+    mean bound against the mean measured window (event nodes included)."""
+    if launches is None or not link_gbs:
+        return None
+    nuniq, carried, ffn_ms = launches
+    bound_us = np.maximum(nuniq * eb / (hbm_gbs * 1e3), carried * eb / (link_gbs * 1e3))
+    link_bound = carried * eb / (link_gbs * 1e3) > nuniq * eb / (hbm_gbs * 1e3)
+    return {"bound_us_per_launch": float(bound_us.mean()), "measured_us_per_launch": float(1e3 * ffn_ms.mean()),
+            "frac": float(bound_us.mean() / (1e3 * ffn_ms.mean())), "link_bound_launches": float(link_bound.mean()),
+            "hbm_gbs": hbm_gbs, "link_gbs": link_gbs,
+            "how": "per launch max(n_unique x expert_bytes / HBM peak, blobs copied x expert_bytes / SM-pull "
+                   "ceiling measured alone); frac = mean bound / mean window of the timing pass"}
+
+
+def decode_block(w, dev, bank, n_blobs, args, steps, warmup, fill, timing_steps, peak, resize=None, link_gbs=None):
     """A compact decode measurement of workload w (its own cache): fill,
     warm-up, `steps` timed, then a timing pass.  `resize` = (slots, fill2):
     after the first timed pass, resize the cache at a safe point, refill for
@@ -721,6 +749,7 @@ def decode_block(w, dev, bank, n_blobs, args, steps, warmup, fill, timing_steps,
         r = out["roofline_ffn"]
         r["frac"] = r["achieved"] / peak
         r["frac_alone_in_pipeline"] = r["achieved_alone_in_pipeline"] / peak
+        r["hbm_or_link_bound"] = bound_of_launches(b.last_launches, w.expert_bytes, peak, link_gbs)
         if resize:
             slots, fill2 = resize
             b.cache.synchronize()
@@ -772,6 +801,7 @@ def run_ours(args, w):
     if args.trace and rank == 0:
         print(json.dumps(tp), file=sys.stderr)
     launches = d["kernel_launches"]
+    main_launches = b.last_launches
     b.close()
     elapsed_ms = max_over_ranks(ms1, world)
     tokens = world * K * T
@@ -784,10 +814,12 @@ def run_ours(args, w):
             link = link_ceilings(w, dev, bank, n_blobs)
         except Exception as ex:
             link = {"error": str(ex)[:200]}
+    link_pull = (link or {}).get("sm_pull_gbs")
     blocks = {}
     if rank == 0 and not args.no_blocks:
         for wb in (W.QWEN35B_DECODE_B4, W.QWEN35B_DECODE_B8):
-            blocks[wb.name] = decode_block(wb, dev, bank, n_blobs, args, max(8, K // 2), 3, fill, 16, peak)
+            blocks[wb.name] = decode_block(wb, dev, bank, n_blobs, args, max(8, K // 2), 3, fill, 16, peak,
+                                           link_gbs=link_pull)
         blocks["prefill"] = prefill_measure(dev, measured_bf16_tflops())
         blocks["prefill"]["gemm_alone"] = prefill_gemm_only(dev, measured_bf16_tflops())
         blocks["prefill"]["gemm_alone_fp8"] = prefill_gemm_only(dev, measured_bf16_tflops(), w=FP8_PREFILL)
@@ -795,7 +827,7 @@ def run_ours(args, w):
         dbank = pinned_bank(wd.blobs * wd.expert_bytes)
         synth.expert_blobs(wd.seed, wd.hidden, wd.inter, wd.wdtype, np.arange(wd.blobs), out_ptr=dbank.data_ptr())
         blocks[wd.name] = decode_block(wd, dev, dbank, wd.blobs, args, max(8, K // 2), 3, 40, 8, peak,
-                                       resize=(wd.resize_slots, 24))
+                                       resize=(wd.resize_slots, 24), link_gbs=link_pull)
         blocks[wd.name]["bank"] = f"aliased: {wd.blobs} physical blobs of {wd.expert_bytes} B for " \
                                   f"{wd.keys} (layer, expert) keys"
         del dbank
@@ -848,7 +880,8 @@ def run_ours(args, w):
                          "traffic": FFN_TRAFFIC_PER_LAUNCH.get(w.name),
                          "bytes_per_launch": bytes_launch,
                          "bytes_def": "n_unique x expert_bytes read + n_miss(next layer) x expert_bytes written",
-                         "launch_us": tp["ffn_us_per_launch"], "ffn_only": ffn_alone},
+                         "launch_us": tp["ffn_us_per_launch"], "ffn_only": ffn_alone,
+                         "hbm_or_link_bound": bound_of_launches(main_launches, w.expert_bytes, peak, link_pull)},
             "cpu_baseline": cpu,
             "blocks": blocks,
             "e2e": e2e,

@@ -92,7 +92,10 @@ constexpr int kStageOutOff = kRingBytes;
 constexpr int kTableOff = kStageOutOff + kEpiWarps * 2 * kBoxBytes;
 constexpr int kBarOff = (kTableOff + kTableInts * 4 + 15) / 16 * 16;
 constexpr int kBarWords = 3 * kStages + 2 * 2 + 1;  // full, empty, ready, tfull, tempty, drain
-constexpr int kTcSmem = kBarOff + kBarWords * 8 + 16 + 1024;  // + tmem holder, abort flag, alignment slack
+constexpr int kMaxKBlocks = 128;         // fp8: K / 128 of a GEMM (hidden, inter <= 16384)
+constexpr int kScaleOff = kBarOff + kBarWords * 8 + 16;   // after the tmem holder and the abort flag
+constexpr int kTcSmem = kScaleOff + 2 * kMaxKBlocks * 4 + 1024;  // + a tile's block scales, alignment slack
+static_assert(kTcSmem <= 227 * 1024, "shared memory of the tensor-core GEMM");
 
 struct TcArgs {
   const int32_t* hdr;
@@ -253,6 +256,7 @@ struct Smem {
   uint64_t* ready;   // fp8: the stage's B rows are dequantised
   uint32_t* tmem_holder;
   volatile int* abort_flag;
+  float* s_scale;    // fp8: the tile's block scales [2 row blocks][K / 128]
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
@@ -274,6 +278,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.ready = bars + 2 * kStages + 5;
   s.tmem_holder = reinterpret_cast<uint32_t*>(bars + kBarWords);
   s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_holder + 1);
+  s.s_scale = reinterpret_cast<float*>(base + kScaleOff);
   return s;
 }
 
@@ -475,6 +480,21 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
       for (int tile = blockIdx.x; tile < total && go; tile += gridDim.x) {
         const TileInfo t = tile_info(s, n_u, ntiles, tile, n_cols);
         const uint16_t* sc = reinterpret_cast<const uint16_t*>(a.pool + (long long)t.slot * a.expert_bytes + scale_off);
+        // the tile's block scales, one per (128-row block, 128-wide K block), read
+        // from the slot once per tile instead of once per stage and row
+        const int KB = KT / 2;
+        asm volatile("bar.sync 5, %0;" ::"n"(kCvtWarps * 32) : "memory");  // the previous tile's are read
+        for (int i = ctid; i < 2 * KB; i += kCvtWarps * 32) {
+          const int rb = i / KB, kb = i - rb * KB;
+          float v = 0.0f;
+          if (rb * kBM < N) {
+            const int idx = kGateUp ? (rb ? ib * hb : 0) + (t.n0 >> 7) * hb + kb  // Wg, then Wu row blocks
+                                    : 2 * ib * hb + ((t.n0 >> 7) + rb) * ib + kb;  // Wd row blocks
+            v = __uint_as_float((uint32_t)__ldg(sc + idx) << 16);
+          }
+          s.s_scale[i] = v;
+        }
+        asm volatile("bar.sync 5, %0;" ::"n"(kCvtWarps * 32) : "memory");
         for (int kt = 0; kt < KT; ++kt, ++it) {
           const int st = it % kStages;
           bool ok = true;
@@ -494,12 +514,7 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
 #pragma unroll
               for (int i = 0; i < 4; ++i)  // 64-byte-swizzled fp8 row r
                 raw[h][i] = *reinterpret_cast<const uint4*>(B8 + r * 64 + ((i ^ ((r >> 1) & 3)) << 4));
-              int idx;
-              if (kGateUp)  // rows < 128: Wg rows n0.., else the same Wu rows
-                idx = (r < kBM ? 0 : ib * hb) + (t.n0 >> 7) * hb + kb;
-              else          // Wd rows n0 + r
-                idx = 2 * ib * hb + ((t.n0 + r) >> 7) * ib + kb;
-              scl[h] = __uint_as_float((uint32_t)__ldg(sc + idx) << 16);
+              scl[h] = s.s_scale[(r >> 7) * KB + kb];  // gate/up: rows < 128 are Wg rows; down: rows n0 + r
             }
           }
           // every fp8 row is read before any 16-bit row is written; the four warps
@@ -690,7 +705,8 @@ int tc_sms() {
 }  // namespace
 
 bool prefill_tc_supported(int H, int I) {
-  return H % 128 == 0 && I % kH1 == 0 && H % kBK == 0 && I % kBK == 0;
+  return H % 128 == 0 && I % kH1 == 0 && H % kBK == 0 && I % kBK == 0 && H <= 128 * kMaxKBlocks &&
+         I <= 128 * kMaxKBlocks;
 }
 
 // A 3D byte tensor map over rows of the slot pool: [slot][row < rows][cols
