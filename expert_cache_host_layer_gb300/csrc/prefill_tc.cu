@@ -19,10 +19,11 @@
 //               fp32 accumulate), four per K block; tcgen05.commit frees each
 //               ring stage, and marks an accumulator full after its last block.
 //   warps 2-9   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//               lanes 32 (w % 4) .. and half of the columns), SwiGLU or the
-//               gate weight, then TMA stores of 32-row boxes staged in shared
-//               memory; the accumulator is handed back, so the epilogue of one
-//               tile overlaps the MMAs of the next.
+//               lanes 32 (w % 4) .. and half of the columns; with fp8 weights
+//               warps 2-5, each all the columns), SwiGLU or the gate weight,
+//               then TMA stores of 32-row boxes staged in shared memory; the
+//               accumulator is handed back, so the epilogue of one tile
+//               overlaps the MMAs of the next.
 // The gate/up B tile is 128 Wg rows followed by the same 128 Wu rows, so the
 // accumulator's columns [0, 128) are gate and [128, 256) up for the same 128 h
 // columns and SwiGLU needs no data exchange.
@@ -31,9 +32,10 @@
 // cores multiply 16-bit by 16-bit here, because the activations must stay
 // 16-bit (e4m3 activations would put about 4% error on each dot product).
 // The producer loads the fp8 B rows (64 bytes of each row per K block,
-// 64-byte swizzle) into the upper half of the stage's B area, and four
-// converter warps (warps 10-13) read them, multiply each by its block's scale
-// (a K block of 64 lies in one 128-wide scale block) and write fp16 into the
+// 64-byte swizzle) into the upper half of the stage's B area, and eight
+// converter warps (warps 6-13, one B row per thread) read them, multiply each
+// by its block's scale (staged in shared memory once per tile; a K block of 64
+// lies in one 128-wide scale block) and write fp16 into the
 // 128-byte-swizzled layout the MMA reads, over the whole B area (all reads
 // happen before any write: a named barrier separates them), then release the
 // stage to the MMA.  fp16 rather than bf16 because an e4m3 value times a bf16
@@ -67,9 +69,11 @@ namespace ft {
 namespace {
 
 constexpr int kEpiWarps = 8;             // two per TMEM lane quarter, each taking half the columns
-constexpr int kCvtWarps = 4;             // fp8 weights: dequantising warps
+constexpr int kEpiWarpsFp8 = 4;          // fp8: one per TMEM lane quarter, each taking all the columns
+constexpr int kCvtWarps = 8;             // fp8 weights: dequantising warps, one B row per thread
+constexpr int kCvtRows = 256 / (kCvtWarps * 32);
 constexpr int kTcThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue
-constexpr int kTcThreadsFp8 = kTcThreads + kCvtWarps * 32;
+constexpr int kTcThreadsFp8 = (2 + kEpiWarpsFp8 + kCvtWarps) * 32;
 constexpr int kBM = 128;                 // grouped rows per tile (UMMA M)
 constexpr int kBK = 64;                  // K per ring stage: one 128-byte swizzle row of bf16
 constexpr int kStages = 3;
@@ -356,6 +360,7 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
                    const __grid_constant__ CUtensorMap map_out, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const Smem s = carve(smem_raw);
+  constexpr int kEpi = kFp8 ? kEpiWarpsFp8 : kEpiWarps;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_u = min(__ldg(&a.hdr[PH_UNIQUE]), kMaxExperts);
   const int N = kGateUp ? kN1 : a.n_tile;           // UMMA N
@@ -372,7 +377,7 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       bar_init(&s.tfull[i], 1);
-      bar_init(&s.tempty[i], kEpiWarps);
+      bar_init(&s.tempty[i], kEpi);
     }
     bar_init(s.drain, 1);
     *s.abort_flag = 0;
@@ -469,10 +474,10 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
       bwait(s.drain, 0, a.status, s.abort_flag, true);
     }
     __syncwarp();
-  } else if (warp >= 2 + kEpiWarps) {
+  } else if (kFp8 && warp >= 2 + kEpi) {
     // ------------------------------------------------------------ fp8 dequantising warps
     if (kFp8) {
-      const int ctid = threadIdx.x - (2 + kEpiWarps) * 32;  // 0 .. 127: rows ctid and ctid + 128
+      const int ctid = threadIdx.x - (2 + kEpi) * 32;  // B rows ctid + h * (kCvtWarps * 32)
       const long long scale_off = 3LL * a.H * a.I;
       const int hb = a.H / 128, ib = a.I / 128;
       int it = 0;
@@ -504,11 +509,11 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
           uint8_t* B = s.ring + st * kStageBytes + kABytes;
           const uint8_t* B8 = B + kBBytesMax / 2;
           const int kb = (kt * kBK) >> 7;  // the 128-wide K block of this stage
-          uint4 raw[2][4];
-          float scl[2];
+          uint4 raw[kCvtRows][4];
+          float scl[kCvtRows];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int r = ctid + h * 128;
+          for (int h = 0; h < kCvtRows; ++h) {
+            const int r = ctid + h * (kCvtWarps * 32);
             scl[h] = 0.0f;
             if (ok && r < N) {
 #pragma unroll
@@ -531,8 +536,8 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
             break;
           }
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int r = ctid + h * 128;
+          for (int h = 0; h < kCvtRows; ++h) {
+            const int r = ctid + h * (kCvtWarps * 32);
             if (r < N) {
 #pragma unroll
               for (int i = 0; i < 4; ++i) {  // 16 fp8 -> 16 fp16 = two 16-byte chunks of the 16-bit row
@@ -568,7 +573,6 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
     // store (full 128-byte lines); a group cut by the expert's end is stored
     // row by row by its live lanes, so no store touches the next expert's rows.
     const int q = warp & 3;                     // TMEM lanes 32q .. 32q + 31
-    const int half = (warp - 2) >> 2;           // which half of the columns
     uint8_t* boxes = s.out + (warp - 2) * 2 * kBoxBytes;
     int nbox = 0;
     int j = 0;
@@ -593,7 +597,8 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
       const bool live = lane < live_rows;
       const bool boxed = live_rows == 32;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
-      if (live_rows > 0) {
+      for (int hh = 0; hh < (kEpi == 8 ? 1 : 2) && live_rows > 0; ++hh) {
+        const int half = kEpi == 8 ? (warp - 2) >> 2 : hh;  // which half of the columns
         if (kGateUp) {
           // h columns [hc, hc + 64): gate at TMEM columns hc.., up at kH1 + hc..
           const int hc = half * 64;
