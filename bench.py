@@ -698,17 +698,7 @@ class DecodeBench:
         ffn, route, nmiss, nuniq = np.stack(ffn), np.stack(route), np.stack(nmiss), np.stack(nuniq)
         carried = np.zeros_like(nmiss)
         carried[:, :-1] = nmiss[:, 1:]   # FFN(l) copies layer l+1's misses
-        # marginal host-link rate in the pipeline: each FFN window against the
-        # number of blobs its kernel copied (least squares); the slope is the
-        # link time one more blob costs, the intercept the window of an FFN
-        # that copies nothing (event nodes included)
-        xs, ys = carried.ravel().astype(np.float64), ffn.ravel().astype(np.float64)
-        marginal = None
-        if np.unique(xs).size > 1:
-            (b0, b1), *_ = np.linalg.lstsq(np.stack([np.ones_like(xs), xs], 1), ys, rcond=None)
-            marginal = {"us_per_blob": 1e3 * float(b1), "intercept_us": 1e3 * float(b0),
-                        "gbs": eb / (float(b1) / 1e3) / 1e9 if b1 > 0 else None,
-                        "launches_by_blobs_copied": {int(c): int((xs == c).sum()) for c in np.unique(xs)}}
+        marginal = marginal_link(carried, ffn, eb)
         # the FFN alone, in the pipeline: the fit's intercept (at batch 4/8
         # nearly every launch copies something, and the few that copy nothing
         # are not typical), else the median window of the launches that copied
@@ -747,6 +737,22 @@ class DecodeBench:
         for g in self.graphs:
             g.close()
         self.cache.close()
+
+
+def marginal_link(carried, window_ms, eb):
+    """The marginal host-link rate in the pipeline: each FFN window (ms)
+    against the number of blobs its kernel copied, least squares; the slope
+    is the link time one more blob costs, the intercept the window of an FFN
+    that copies nothing (event nodes included).  None without two distinct
+    copy counts."""
+    xs = np.asarray(carried, dtype=np.float64).ravel()
+    ys = np.asarray(window_ms, dtype=np.float64).ravel()
+    if np.unique(xs).size < 2:
+        return None
+    (b0, b1), *_ = np.linalg.lstsq(np.stack([np.ones_like(xs), xs], 1), ys, rcond=None)
+    return {"us_per_blob": 1e3 * float(b1), "intercept_us": 1e3 * float(b0),
+            "gbs": eb / (float(b1) / 1e3) / 1e9 if b1 > 0 else None,
+            "launches_by_blobs_copied": {int(c): int((xs == c).sum()) for c in np.unique(xs)}}
 
 
 def bound_of_launches(launches, eb, hbm_gbs, link_gbs):
