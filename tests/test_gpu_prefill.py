@@ -53,8 +53,8 @@ def test_prefill_16k_chunk(double_buffer):
 
 
 # fp8 e4m3 experts with bf16 128 x 128 block scales on the prefill path: the
-# weights are dequantised to bf16 (times their block's scale) in shared memory
-# and multiplied on the tensor cores.  A small shape (ragged tiles, 64 experts)
+# weights are dequantised to fp16 (times their block's scale) in shared memory
+# and multiplied with fp16 activations on the tensor cores.  A small shape (ragged tiles, 64 experts)
 # and the DeepSeek-V4-Flash-shaped layer dimensions (hidden 4096,
 # intermediate 2048) with 32 experts so the fp64 oracle stays quick.
 FP8_SMALL_PREFILL = W.DSV4_DECODE.replace(name="fp8-prefill-1024x512", num_layers=2, num_experts=64, hidden=1024,
