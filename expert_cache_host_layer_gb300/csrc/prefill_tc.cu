@@ -9,7 +9,8 @@
 // (N); a persistent grid walks the tiles in (m-tile, n-tile) order, m-tiles
 // expert by expert.  Every CTA runs three roles:
 //   warp 0      TMA producer: the A rows and the B rows of each 64-wide K
-//               block into a 3-stage shared-memory ring, 128-byte swizzled.
+//               block into a shared-memory ring (4 stages for gate/up, 3 for
+//               down, whose epilogue needs staging space), 128-byte swizzled.
 //               The A rows are one 2D box of 128 grouped rows: x rows already
 //               permuted into grouped order (gate/up) or h (down).  The B
 //               rows come from the slot pool viewed as one 2D tensor whose
@@ -20,10 +21,11 @@
 //               ring stage, and marks an accumulator full after its last block.
 //   warps 2-9   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
 //               lanes 32 (w % 4) .. and half of the columns; with fp8 weights
-//               warps 2-5, each all the columns), SwiGLU or the gate weight,
-//               then TMA stores of 32-row boxes staged in shared memory; the
-//               accumulator is handed back, so the epilogue of one tile
-//               overlaps the MMAs of the next.
+//               warps 2-5, each all the columns), SwiGLU or the gate weight;
+//               gate/up writes each lane's 128-byte pieces of its h row
+//               directly, down stores 32-row boxes staged in shared memory
+//               with TMA; the accumulator is handed back, so the epilogue of
+//               one tile overlaps the MMAs of the next.
 // The gate/up B tile is 128 Wg rows followed by the same 128 Wu rows, so the
 // accumulator's columns [0, 128) are gate and [128, 256) up for the same 128 h
 // columns and SwiGLU needs no data exchange.
@@ -76,7 +78,6 @@ constexpr int kTcThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue
 constexpr int kTcThreadsFp8 = (2 + kEpiWarpsFp8 + kCvtWarps) * 32;
 constexpr int kBM = 128;                 // grouped rows per tile (UMMA M)
 constexpr int kBK = 64;                  // K per ring stage: one 128-byte swizzle row of bf16
-constexpr int kStages = 3;
 constexpr int kN1 = 256;                 // gate/up UMMA N: 128 gate + 128 up columns
 constexpr int kH1 = kN1 / 2;             // h columns per gate/up tile
 constexpr int kAccCols = 256;            // TMEM columns per accumulator
@@ -87,19 +88,26 @@ constexpr int kStageBytes = kABytes + kBBytesMax;
 constexpr int kTableInts = 3 * (kMaxExperts + 1);
 constexpr unsigned long long kWaitNs = 1000000000ull;
 
-// Dynamic shared memory: [ring (1024-aligned)][output staging][tile table][barriers].
-// Each epilogue warp owns two 4 KB staging boxes (32 rows x 128 bytes, the
-// layout of a 128-byte-swizzled TMA store box), used alternately.
-constexpr int kRingBytes = kStages * kStageBytes;
+// Dynamic shared memory: [ring (1024-aligned)][output staging][tile table][barriers][fp8 scales].
+// The down GEMM's epilogue stores through staging boxes: each epilogue warp
+// owns two 4 KB boxes (32 rows x 128 bytes, the layout of a 128-byte-swizzled
+// TMA store box), used alternately.  The gate/up GEMM's epilogue writes its
+// 128-byte pieces of h rows directly, and its ring has a stage more instead.
 constexpr int kBoxBytes = 32 * 128;
-constexpr int kStageOutOff = kRingBytes;
-constexpr int kTableOff = kStageOutOff + kEpiWarps * 2 * kBoxBytes;
-constexpr int kBarOff = (kTableOff + kTableInts * 4 + 15) / 16 * 16;
-constexpr int kBarWords = 3 * kStages + 2 * 2 + 1;  // full, empty, ready, tfull, tempty, drain
 constexpr int kMaxKBlocks = 128;         // fp8: K / 128 of a GEMM (hidden, inter <= 16384)
-constexpr int kScaleOff = kBarOff + kBarWords * 8 + 16;   // after the tmem holder and the abort flag
-constexpr int kTcSmem = kScaleOff + 2 * kMaxKBlocks * 4 + 1024;  // + a tile's block scales, alignment slack
-static_assert(kTcSmem <= 227 * 1024, "shared memory of the tensor-core GEMM");
+template <bool kGateUp>
+struct TcLayout {
+  static constexpr int kStages = kGateUp ? 4 : 3;
+  static constexpr bool kStaged = !kGateUp;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kStageOutOff = kRingBytes;
+  static constexpr int kTableOff = kStageOutOff + (kStaged ? kEpiWarps * 2 * kBoxBytes : 0);
+  static constexpr int kBarOff = (kTableOff + kTableInts * 4 + 15) / 16 * 16;
+  static constexpr int kBarWords = 3 * kStages + 2 * 2 + 1;  // full, empty, ready, tfull, tempty, drain
+  static constexpr int kScaleOff = kBarOff + kBarWords * 8 + 16;  // after the tmem holder and the abort flag
+  static constexpr int kSmem = kScaleOff + 2 * kMaxKBlocks * 4 + 1024;  // + a tile's block scales, alignment slack
+  static_assert(kSmem <= 227 * 1024, "shared memory of the tensor-core GEMM");
+};
 
 struct TcArgs {
   const int32_t* hdr;
@@ -263,26 +271,29 @@ struct Smem {
   float* s_scale;    // fp8: the tile's block scales [2 row blocks][K / 128]
 };
 
+template <bool kGateUp>
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
+  using L = TcLayout<kGateUp>;
+  constexpr int kStages = L::kStages;
   Smem s;
   // aligned by an offset from the shared array itself (not through an integer
   // cast), so the compiler keeps every access derived from it a shared one
   uint8_t* base = raw + ((1024u - (sa(raw) & 1023u)) & 1023u);
   s.ring = base;
-  s.out = base + kStageOutOff;
-  s.s_off = reinterpret_cast<int*>(base + kTableOff);
+  s.out = base + L::kStageOutOff;
+  s.s_off = reinterpret_cast<int*>(base + L::kTableOff);
   s.s_pre = s.s_off + (kMaxExperts + 1);
   s.s_slot = s.s_pre + (kMaxExperts + 1);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kBarOff);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L::kBarOff);
   s.full = bars;
   s.empty = bars + kStages;
   s.tfull = bars + 2 * kStages;
   s.tempty = bars + 2 * kStages + 2;
   s.drain = bars + 2 * kStages + 4;
   s.ready = bars + 2 * kStages + 5;
-  s.tmem_holder = reinterpret_cast<uint32_t*>(bars + kBarWords);
+  s.tmem_holder = reinterpret_cast<uint32_t*>(bars + L::kBarWords);
   s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_holder + 1);
-  s.s_scale = reinterpret_cast<float*>(base + kScaleOff);
+  s.s_scale = reinterpret_cast<float*>(base + L::kScaleOff);
   return s;
 }
 
@@ -359,7 +370,8 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_out, TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  const Smem s = carve(smem_raw);
+  constexpr int kStages = TcLayout<kGateUp>::kStages;
+  const Smem s = carve<kGateUp>(smem_raw);
   constexpr int kEpi = kFp8 ? kEpiWarpsFp8 : kEpiWarps;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_u = min(__ldg(&a.hdr[PH_UNIQUE]), kMaxExperts);
@@ -595,7 +607,7 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
       const int r0 = t.p0 + q * 32;              // first grouped row of this warp's group
       const int live_rows = min(32, max(0, t.pend - r0));
       const bool live = lane < live_rows;
-      const bool boxed = live_rows == 32;
+      const bool boxed = TcLayout<kGateUp>::kStaged && live_rows == 32;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + acc * kAccCols;
       for (int hh = 0; hh < (kEpi == 8 ? 1 : 2) && live_rows > 0; ++hh) {
         const int half = kEpi == 8 ? (warp - 2) >> 2 : hh;  // which half of the columns
@@ -736,7 +748,8 @@ cudaError_t fp8_rows_map(CUtensorMap* m, const uint8_t* pool, long long offset, 
 
 template <bool kGateUp, bool kFp8>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(tc_gemm_kernel<kGateUp, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  return cudaFuncSetAttribute(tc_gemm_kernel<kGateUp, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              TcLayout<kGateUp>::kSmem);
 }
 
 cudaError_t launch_prefill_gemms(const PrefillArgs& p, int num_slots, cudaStream_t st, const cudaEvent_t* marks) {
@@ -788,15 +801,16 @@ cudaError_t launch_prefill_gemms(const PrefillArgs& p, int num_slots, cudaStream
   a.n_tile = kN1;
   a.slot_rows = 3LL * I;
   if (marks && (e = cudaEventRecord(marks[0], st)) != cudaSuccess) return e;
-  if (fp8) tc_gemm_kernel<true, true><<<grid, threads, kTcSmem, st>>>(mx, mw1, mh_out, a);
-  else tc_gemm_kernel<true, false><<<grid, threads, kTcSmem, st>>>(mx, mw1, mh_out, a);
+  constexpr int kSmem1 = TcLayout<true>::kSmem, kSmem2 = TcLayout<false>::kSmem;
+  if (fp8) tc_gemm_kernel<true, true><<<grid, threads, kSmem1, st>>>(mx, mw1, mh_out, a);
+  else tc_gemm_kernel<true, false><<<grid, threads, kSmem1, st>>>(mx, mw1, mh_out, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (marks && (e = cudaEventRecord(marks[1], st)) != cudaSuccess) return e;
   a.n_tile = n2;
   a.slot_rows = 3LL * H;
   if (marks && (e = cudaEventRecord(marks[2], st)) != cudaSuccess) return e;
-  if (fp8) tc_gemm_kernel<false, true><<<grid, threads, kTcSmem, st>>>(mh, mwd, myp_out, a);
-  else tc_gemm_kernel<false, false><<<grid, threads, kTcSmem, st>>>(mh, mwd, myp_out, a);
+  if (fp8) tc_gemm_kernel<false, true><<<grid, threads, kSmem2, st>>>(mh, mwd, myp_out, a);
+  else tc_gemm_kernel<false, false><<<grid, threads, kSmem2, st>>>(mh, mwd, myp_out, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (marks && (e = cudaEventRecord(marks[3], st)) != cudaSuccess) return e;
   return cudaSuccess;
