@@ -172,7 +172,7 @@ struct ft_cache {
   // [rows][H], grouped place of each row; allocated only when max_tokens > 8
   void* pf_h = nullptr;
   void* pf_xp = nullptr;              // bf16 x rows in grouped order [rows][H]
-  float* pf_yp = nullptr;
+  void* pf_yp = nullptr;
   int32_t* pf_pos = nullptr;
   unsigned* gbar = nullptr;           // grid-barrier words of the fused FFN kernel
   bool fused_ok = true;               // false once the fused FFN kernel reported it cannot run
@@ -467,7 +467,7 @@ uint64_t cache_device_bytes(const ft_cache_config& g, int64_t C) {
   b += dev_alloc(4 * (uint64_t)std::min(g.max_tokens, kDecodeMaxTokens) * g.top_k * I);
   b += dev_alloc(16);
   if (g.max_tokens > kDecodeMaxTokens && prefill_supported((int)H, (int)I, g.wdtype, (int)E))
-    b += dev_alloc(2 * rows * I) + dev_alloc(2 * rows * H) + dev_alloc(4 * rows * H) + dev_alloc(4 * rows);
+    b += dev_alloc(2 * rows * I) + dev_alloc(2 * rows * H) + dev_alloc(2 * rows * H) + dev_alloc(4 * rows);
   if (g.fetch_mode == FT_FETCH_COPY_ENGINE) b += dev_alloc(4 * kRing);
   return b;
 }
@@ -685,7 +685,7 @@ ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t n
       const long long prows = (long long)g.max_tokens * g.top_k;
       CU(cudaMalloc(&c->pf_h, sizeof(uint16_t) * prows * c->I));
       CU(cudaMalloc(&c->pf_xp, sizeof(uint16_t) * prows * c->H));
-      CU(cudaMalloc(&c->pf_yp, sizeof(float) * prows * c->H));
+      CU(cudaMalloc(&c->pf_yp, sizeof(uint16_t) * prows * c->H));
       CU(cudaMalloc(&c->pf_pos, sizeof(int32_t) * prows));
     }
     CU(cudaMalloc(&c->gbar, 4 * sizeof(unsigned)));

@@ -205,7 +205,7 @@ struct PrefillArgs {
   const void* x;             // [T][H] bf16
   void* xp;                  // [T*k][H] bf16 scratch: the x row of each grouped row
   void* h;                   // [T*k][I] bf16 scratch
-  float* yp;                 // [T*k][H] fp32 scratch
+  void* yp;                  // [T*k][H] fp16 scratch: each row's gate-weighted down projection
   float* y;                  // [T][H] fp32 out
   const uint8_t* pool;
   long long expert_bytes;

@@ -9,7 +9,7 @@
 //                tile's A rows are one contiguous block (fp16 for fp8 experts)
 //   gate/up:     h[p][i] = silu(Wg[i] . x_t) * (Wu[i] . x_t)  (bf16 h; p the
 //                grouped place of row (t, j))
-//   down:        yp[p][c] = w_tj * (Wd[c] . h[p])              (fp32)
+//   down:        yp[p][c] = w_tj * (Wd[c] . h[p])              (fp16; fp32 accumulation)
 //   combine:     y[t][c] = sum over j < k, ascending, of yp[pos[t*k+j]][c]
 //
 // The combine sums each token's picks in a fixed order: the result does not
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kPThreads) permute_rows_kernel(PrefillArgs a) 
 }
 
 // ---------------------------------------------------------------- combine
-// y[t][c] = sum_{j<k} yp[pos[t*k+j]][c], four columns per thread.
+// y[t][c] = sum_{j<k} yp[pos[t*k+j]][c] in fp32, four columns per thread.
 __global__ void __launch_bounds__(kPThreads) combine_kernel(PrefillArgs a) {
   const int q4 = a.H / 4;
   const long long n = (long long)a.T * q4;
@@ -117,8 +117,10 @@ __global__ void __launch_bounds__(kPThreads) combine_kernel(PrefillArgs a) {
     for (int j = 0; j < a.k; ++j) {
       const int p = __ldg(&a.pos[t * a.k + j]);
       if (!checked_ok(p >= 0 && p < a.T * a.k, a.status)) continue;
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(a.yp + (long long)p * a.H) + q);
-      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+      const uint2 v = __ldcg(reinterpret_cast<const uint2*>(static_cast<const __half*>(a.yp) + (long long)p * a.H) + q);
+      const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+      const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+      s.x += lo.x; s.y += lo.y; s.z += hi.x; s.w += hi.y;
     }
     reinterpret_cast<float4*>(a.y + (long long)t * a.H)[q] = s;
   }

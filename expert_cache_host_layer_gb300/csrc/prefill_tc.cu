@@ -3,7 +3,7 @@
 // routed SwiGLU experts, reading the weights straight from their cache slots.
 //
 //   gate/up:  h[p][i]  = silu(Wg[i] . x_t) * (Wu[i] . x_t)   bf16 h, p = grouped row of (t, j)
-//   down:     yp[p][c] = w_tj * (Wd[c] . h[p])               fp32
+//   down:     yp[p][c] = w_tj * (Wd[c] . h[p])               fp16 (fp32 accumulation)
 //
 // A tile is 128 grouped rows of one expert (M) by a block of output columns
 // (N); a persistent grid walks the tiles in (m-tile, n-tile) order, m-tiles
@@ -116,7 +116,7 @@ struct TcArgs {
   const int32_t* rows_by_u;    // [R] row ids t*k + j in grouped order
   const float* topk_w;         // [R]
   __nv_bfloat16* h;            // [R][I]
-  float* yp;                   // [R][H]
+  __half* yp;                  // [R][H]
   int32_t* status;
   int H, I, k, R;
   int n_tile;                  // UMMA N of this GEMM (gate/up 256; down 256 or 128)
@@ -646,19 +646,26 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
             if (lane == 0) tma_store_2d(&map_out, t.n0 + hc, r0, box);
           }
         } else {
-          // output columns [t.n0 + half * n_cols / 2, ...) in chunks of 32
+          // output columns [t.n0 + half * n_cols / 2, ...) in chunks of 64, rounded to fp16
           const float wt = live ? __ldg(&a.topk_w[__ldg(&a.rows_by_u[r0 + lane])]) : 0.0f;
           const int cw = n_cols / 2;
-          float* yrow = a.yp + (long long)(r0 + lane) * a.H + t.n0 + half * cw;
-          for (int c = 0; c < cw; c += 32) {
-            float v[32];
+          __half* yrow = a.yp + (long long)(r0 + lane) * a.H + t.n0 + half * cw;
+          for (int c = 0; c < cw; c += 64) {
+            float v[64];
             tc_ld32(tbase + half * cw + c, v);
+            tc_ld32(tbase + half * cw + c + 32, v + 32);
             uint8_t* box = boxed ? next_box() : nullptr;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const float4 f = make_float4(wt * v[4 * i], wt * v[4 * i + 1], wt * v[4 * i + 2], wt * v[4 * i + 3]);
-              if (boxed) box_put16(box, lane, i, *reinterpret_cast<const uint4*>(&f));
-              else if (live) reinterpret_cast<float4*>(yrow + c)[i] = f;
+              uint32_t w4[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const __half2 hv = __floats2half2_rn(wt * v[8 * i + 2 * q], wt * v[8 * i + 2 * q + 1]);
+                w4[q] = *reinterpret_cast<const uint32_t*>(&hv);
+              }
+              const uint4 u = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              if (boxed) box_put16(box, lane, i, u);
+              else if (live) reinterpret_cast<uint4*>(yrow + c)[i] = u;
             }
             if (boxed) {
               fence_async_smem();
@@ -774,7 +781,7 @@ cudaError_t launch_prefill_gemms(const PrefillArgs& p, int num_slots, cudaStream
   const int H = p.H, I = p.I, R = p.T * p.k;
   TcArgs a{};
   a.hdr = p.hdr; a.u_offset = p.u_offset; a.unique_slot = p.unique_slot; a.rows_by_u = p.rows_by_u;
-  a.topk_w = p.topk_w; a.h = static_cast<__nv_bfloat16*>(p.h); a.yp = p.yp; a.status = p.status;
+  a.topk_w = p.topk_w; a.h = static_cast<__nv_bfloat16*>(p.h); a.yp = static_cast<__half*>(p.yp); a.status = p.status;
   a.H = H; a.I = I; a.k = p.k; a.R = R;
   a.pool = p.pool; a.expert_bytes = p.expert_bytes; a.num_slots = num_slots;
   CUtensorMap mx, mw1, mh, mwd, mh_out, myp_out;
@@ -793,9 +800,9 @@ cudaError_t launch_prefill_gemms(const PrefillArgs& p, int num_slots, cudaStream
     // the pool as rows of I: Wd rows [s*3H + 2H, s*3H + 3H)
     if ((e = bf16_map(&mwd, p.pool, I, 3ull * H * num_slots, 2ull * I, kBK, n2)) != cudaSuccess) return e;
   }
-  // output boxes of 32 rows x 128 bytes: h (64 bf16 columns) and yp (32 fp32 columns)
+  // output boxes of 32 rows x 128 bytes: h (64 bf16 columns) and yp (64 fp16 columns)
   if ((e = bf16_map(&mh_out, p.h, I, R, 2ull * I, 64, 32)) != cudaSuccess) return e;
-  if ((e = tmap_2d(&myp_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.yp, H, R, 4ull * H, 32, 32)) != cudaSuccess) return e;
+  if ((e = tmap_2d(&myp_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.yp, H, R, 2ull * H, 64, 32)) != cudaSuccess) return e;
   const int grid = tc_sms();
   const int threads = fp8 ? kTcThreadsFp8 : kTcThreads;
   a.n_tile = kN1;

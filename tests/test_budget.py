@@ -38,8 +38,11 @@ def test_overhead_grows_with_slots_and_counts_the_prefill_buffers():
         o = ft.ft_cache_overhead_bytes(c, n)
         assert o >= prev
         prev = o
-    # a 16,384-token chunk needs x, h and per-row outputs for 131,072 rows: far more than decode
-    assert ft.ft_cache_overhead_bytes(cfg(T=16384), 3072) > ft.ft_cache_overhead_bytes(c, 3072) + 131072 * 2048 * 6
+    # a 16,384-token chunk needs the grouped x rows, h and the per-row outputs (all 16-bit) for
+    # 131,072 rows: far more than decode
+    rows = 131072
+    assert ft.ft_cache_overhead_bytes(cfg(T=16384), 3072) > \
+        ft.ft_cache_overhead_bytes(c, 3072) + rows * (2048 * 2 + 512 * 2 + 2048 * 2)
     assert ft.ft_cache_overhead_bytes(c, 0) == 0
 
 
