@@ -18,8 +18,9 @@
 //             into y[t][c] with a fp32 reduction in global memory.
 // So the down projection of a unit needs only that unit's h: there is no
 // exchange of h between CTAs and no grid barrier.  y is zeroed once per
-// launch by CTA 0, which then raises a per-launch flag; the other CTAs wait
-// (bounded) for the flag before their first addition, long after it is set.
+// launch by CTA 0, which then sets a flag to the launch's event number; the
+// other CTAs wait (bounded) for that value before their first addition, long
+// after it is set.
 // The additions into y from different units arrive in no fixed order, so y
 // is reproducible only to fp32 rounding.
 //
@@ -457,8 +458,12 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
     cons_sync();  // the next unit may overwrite h'
   }
 
-  // ---- the last CTA to finish resets the flag and, in copy-engine mode, tells
-  // the copy thread that this event's slots are no longer read
+  // ---- copy-engine mode: the last CTA to finish resets the flag and tells the
+  // copy thread that this event's slots are no longer read.  With SM pull the
+  // CTAs just leave: the flag keeps this launch's event, which the next
+  // launch (a later event: ft_moe_forward takes each event once) never waits
+  // for, so no count of finished CTAs delays the end of the kernel.
+  if (!a.done_host) return;
   cons_sync();
   if (ctid == 0) {
     __threadfence();

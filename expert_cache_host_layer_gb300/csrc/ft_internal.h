@@ -179,8 +179,9 @@ struct FfnArgs {
   int max_unique;  // upper bound of the plan's n_unique (min(T*k, E)), sizes the grid
   float* h;        // [T*k][I] intermediate
   int32_t* status; // sticky status word (bounded waits record FT_ERR_TIMEOUT)
-  unsigned* gbar;  // [4] of the fused kernel: [2] finished-CTA count (0 between launches), [3] the launch
-                   // whose y is zeroed (0xffffffff between launches); [0], [1] unused
+  unsigned* gbar;  // [4] of the fused kernel: [2] finished-CTA count (copy-engine mode; 0 between
+                   // launches), [3] the event whose y is zeroed (copy-engine mode: 0xffffffff between
+                   // launches; SM pull: the last launch's event); [0], [1] unused
   const int32_t* ready_flags;  // copy-engine mode: wait for ready_flags[e % kRing] == e (e = plan event); or null
   int32_t* done_host;          // copy-engine mode: device address of the mapped [kRing] words where the
                                // FFN stores e at done_host[e % kRing] once it no longer reads its slots; or null
