@@ -146,7 +146,9 @@ size_t ft_expert_bytes(int32_t hidden, int32_t inter, int32_t wdtype);
  * the experts that do not fit stay in host RAM and are streamed from it),
  * portable across the process's contexts, content undefined.  The caller owns
  * it and frees it with ft_host_bank_free after the last cache that uses it is
- * destroyed.  Errors: FT_ERR_INVALID_ARG (bytes 0, null out), FT_ERR_OOM.
+ * destroyed.  Errors: FT_ERR_INVALID_ARG (bytes 0, null out), FT_ERR_OOM
+ * (*host is then NULL).  ft_host_bank_free(NULL) does nothing; FT_ERR_CUDA if
+ * the runtime refuses the pointer.
  */
 ft_status ft_host_bank_alloc(uint64_t bytes, void** host);
 ft_status ft_host_bank_free(void* host);
