@@ -73,7 +73,7 @@ constexpr int kMaxT = kDecodeMaxTokens;
 __host__ __device__ __forceinline__ int up(int v, int a) { return (v + a - 1) / a * a; }
 
 struct Lay {
-  int R, P, x_off, plan_off, w_off, hs_off, bar_off, ring_off, total;
+  int R, P, x_off, plan_off, w_off, hs_off, sc_off, bar_off, ring_off, total;
   __host__ __device__ Lay(int H, int I, int T, int wsize, int act_bytes, int max_unique, int rows) {
     R = kSlice / wsize;
     P = kStageF / (2 * H * wsize);  // row pairs (a Wg row and its Wu row) per phase-A stage
@@ -82,7 +82,8 @@ struct Lay {
     plan_off = up(T * H * act_bytes, 16);
     w_off = plan_off + up((2 * max_unique + 1 + rows) * 4, 16);  // unique_slot, u_offset, rows_by_u
     hs_off = w_off + up(rows * 4, 16);
-    bar_off = hs_off + up(kMaxT * R * 4, 16);
+    sc_off = hs_off + up(kMaxT * R * 4, 16);
+    bar_off = sc_off + (wsize == 1 ? up(3 * (H / 128) * 4, 16) : 0);  // fp8: the unit's block scales
     ring_off = up(bar_off + (2 * kStagesF + 2) * 8, 1024);
     total = ring_off + kStagesF * kStageF + 1024;  // + slack to align the ring to 1024 bytes
   }
@@ -196,6 +197,7 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
   int32_t* p_rows = p_off + a.max_unique + 1;
   float* p_w = reinterpret_cast<float*>(smem + lay.w_off);
   float* hs = reinterpret_cast<float*>(smem + lay.hs_off);  // [MR][R] h' of the current unit
+  float* s_sc = reinterpret_cast<float*>(smem + lay.sc_off);  // fp8: [Wg | Wu | Wd] block scales of the unit
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bar_off);
   uint64_t* empty = full + kStagesF;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStagesF);
@@ -335,6 +337,19 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
     const int row0 = p_off[u];
     const int nrows = min(p_off[u + 1] - row0, MR);
     const uint8_t* blob = a.pool + (long long)p_slot[u] * a.expert_bytes;
+    if constexpr (WT == FT_W_FP8E4M3_B128) {
+      // the unit's block scales, read once: its rows lie in one 128-row block of
+      // Wg and Wu (one scale per 128-wide K block each) and its Wd columns in one
+      // 128-column block (one scale per 128-row block of Wd)
+      const int rb = r0 >> 7;
+      for (int j = ctid; j < 3 * sblk_g; j += kCons * 32) {
+        const int idx = j < sblk_g       ? rb * sblk_g + j
+                        : j < 2 * sblk_g ? (I / 128) * sblk_g + rb * sblk_g + (j - sblk_g)
+                                         : sbase_d + (j - 2 * sblk_g) * sblk_d + rb;
+        s_sc[j] = scale_at(blob, scale_off, idx);
+      }
+      cons_sync();
+    }
     int tok[MR];
     float wq[MR];
     const uint8_t* xrow[MR];
@@ -368,8 +383,8 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
           float sg = 1.0f, su = 1.0f;
           if (WT == FT_W_FP8E4M3_B128) {
             const int cb = (c * EPC) >> 7;
-            sg = scale_at(blob, scale_off, (rr >> 7) * sblk_g + cb);
-            su = scale_at(blob, scale_off, (I / 128) * sblk_g + (rr >> 7) * sblk_g + cb);
+            sg = s_sc[cb];
+            su = s_sc[sblk_g + cb];
           }
 #pragma unroll
           for (int q = 0; q < MR; ++q) {
@@ -427,7 +442,7 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
         const uint8_t* box = ring + (size_t)s * kStageF + j * kBoxBytes;
         const int c = (bx + j) * kBoxRows + ctid;
         float sc = 1.0f;
-        if (WT == FT_W_FP8E4M3_B128) sc = scale_at(blob, scale_off, sbase_d + (c >> 7) * sblk_d + (r0 >> 7));
+        if (WT == FT_W_FP8E4M3_B128) sc = s_sc[2 * sblk_g + (c >> 7)];
         float acc[MR];
 #pragma unroll
         for (int q = 0; q < MR; ++q) acc[q] = 0.0f;
