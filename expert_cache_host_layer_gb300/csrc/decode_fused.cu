@@ -176,7 +176,8 @@ __device__ __forceinline__ uint4 box_get16(const uint8_t* box, int r, int i) {
   return *reinterpret_cast<const uint4*>(box + r * kSlice + ((i ^ ((r >> 1) & 3)) << 4));
 }
 
-// MR: most rows (tokens) of one expert: 1 for single-token decode, else 8.
+// MR: most rows (tokens) of one expert: T rounded up to 1, 4 or 8 (T <= 8), so
+// a batch of a few tokens does not carry eight rows' registers and predicates.
 // NCL: 16-byte chunks per lane of one Wg/Wu row (the row's chunks <= 32 NCL),
 // so the phase-A dot products unroll fully and every lane has NCL chunks of
 // loads in flight.
@@ -571,9 +572,11 @@ cudaError_t fused_typed(const FfnArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int nch = a.H * WSZ / 16;  // 16-byte chunks of one Wg/Wu row
   if (nch <= 64)
-    return a.T == 1 ? launch_typed<WT, 1, 2>(a, lay, map, s) : launch_typed<WT, kMaxT, 2>(a, lay, map, s);
+    return a.T == 1 ? launch_typed<WT, 1, 2>(a, lay, map, s)
+                    : a.T <= 4 ? launch_typed<WT, 4, 2>(a, lay, map, s) : launch_typed<WT, kMaxT, 2>(a, lay, map, s);
   if (nch > 256) return cudaErrorNotSupported;
-  return a.T == 1 ? launch_typed<WT, 1, 8>(a, lay, map, s) : launch_typed<WT, kMaxT, 8>(a, lay, map, s);
+  return a.T == 1 ? launch_typed<WT, 1, 8>(a, lay, map, s)
+                  : a.T <= 4 ? launch_typed<WT, 4, 8>(a, lay, map, s) : launch_typed<WT, kMaxT, 8>(a, lay, map, s);
 }
 
 }  // namespace
