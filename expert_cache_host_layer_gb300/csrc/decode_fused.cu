@@ -176,8 +176,10 @@ __device__ __forceinline__ uint4 box_get16(const uint8_t* box, int r, int i) {
   return *reinterpret_cast<const uint4*>(box + r * kSlice + ((i ^ ((r >> 1) & 3)) << 4));
 }
 
-// MR: most rows (tokens) of one expert: T rounded up to 1, 4 or 8 (T <= 8), so
-// a batch of a few tokens does not carry eight rows' registers and predicates.
+// MR: rows (tokens) of one expert handled together: 1 for single-token
+// decode, else 4; an expert with more rows (T up to 8) takes a second pass
+// over the staged weights, so a batch of a few tokens does not carry eight
+// rows' registers and predicates.
 // NCL: 16-byte chunks per lane of one Wg/Wu row (the row's chunks <= 32 NCL),
 // so the phase-A dot products unroll fully and every lane has NCL chunks of
 // loads in flight.
@@ -336,7 +338,7 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
   for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
     const int u = unit / upe, r0 = (unit - u * upe) * R;
     const int row0 = p_off[u];
-    const int nrows = min(p_off[u + 1] - row0, MR);
+    const int nrows_all = min(p_off[u + 1] - row0, kMaxT);  // T <= kMaxT rows at most
     const uint8_t* blob = a.pool + (long long)p_slot[u] * a.expert_bytes;
     if constexpr (WT == FT_W_FP8E4M3_B128) {
       // the unit's block scales, read once: its rows lie in one 128-row block of
@@ -351,16 +353,6 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
       }
       cons_sync();
     }
-    int tok[MR];
-    float wq[MR];
-    const uint8_t* xrow[MR];
-#pragma unroll
-    for (int q = 0; q < MR; ++q) {
-      const int row = q < nrows ? p_rows[row0 + q] : 0;
-      tok[q] = row / k;
-      wq[q] = q < nrows ? p_w[row] : 0.0f;
-      xrow[q] = xs + (size_t)tok[q] * H * act_bytes;
-    }
     // phase A: h' = w * silu(Wg x) * (Wu x) for the unit's R rows
     const int nch = (int)(row_g / 16);
     for (int r = r0, sidx = 0; r < r0 + R; r += P, ++sidx, ++i) {
@@ -371,6 +363,16 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
         const uint4* grow = reinterpret_cast<const uint4*>(ring + (size_t)s * kStageF + jp * row_g);
         const uint4* urow = reinterpret_cast<const uint4*>(ring + (size_t)s * kStageF + (P + jp) * row_g);
         const int rr = r + jp;
+        for (int g0 = 0; g0 < nrows_all; g0 += MR) {
+        const int nrows = min(nrows_all - g0, MR);
+        float wq[MR];
+        const uint8_t* xrow[MR];
+#pragma unroll
+        for (int q = 0; q < MR; ++q) {
+          const int row = q < nrows ? p_rows[row0 + g0 + q] : 0;
+          wq[q] = q < nrows ? p_w[row] : 0.0f;
+          xrow[q] = xs + (size_t)(row / k) * H * act_bytes;
+        }
         float ag[MR], au[MR];
 #pragma unroll
         for (int q = 0; q < MR; ++q) ag[q] = au[q] = 0.0f;
@@ -410,8 +412,9 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
           if (q < nrows) {
             const float g = warp_sum(ag[q]);
             const float v = warp_sum(au[q]);
-            if (lane == q) hs[q * R + (rr - r0)] = wq[q] * (g / (1.0f + expf(-g)) * v);
+            if (lane == q) hs[(g0 + q) * R + (rr - r0)] = wq[q] * (g / (1.0f + expf(-g)) * v);
           }
+        }
         }
       }
       release(&empty[s]);
@@ -444,6 +447,8 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
         const int c = (bx + j) * kBoxRows + ctid;
         float sc = 1.0f;
         if (WT == FT_W_FP8E4M3_B128) sc = s_sc[2 * sblk_g + (c >> 7)];
+        for (int g0 = 0; g0 < nrows_all; g0 += MR) {
+        const int nrows = min(nrows_all - g0, MR);
         float acc[MR];
 #pragma unroll
         for (int q = 0; q < MR; ++q) acc[q] = 0.0f;
@@ -454,7 +459,7 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
 #pragma unroll
           for (int q = 0; q < MR; ++q) {
             if (q < nrows) {
-              const float* hq = hs + q * R + ch * EPC;
+              const float* hq = hs + (g0 + q) * R + ch * EPC;
               float p0 = 0.0f, p1 = 0.0f;
 #pragma unroll
               for (int e = 0; e < EPC; e += 2) {
@@ -467,7 +472,8 @@ __global__ void __maxnreg__(96) ffn_fused_kernel(const __grid_constant__ CUtenso
         }
 #pragma unroll
         for (int q = 0; q < MR; ++q)
-          if (q < nrows) atomicAdd(a.y + (long long)tok[q] * H + c, sc * acc[q]);
+          if (q < nrows) atomicAdd(a.y + (long long)(p_rows[row0 + g0 + q] / k) * H + c, sc * acc[q]);
+        }
       }
       release(&empty[s]);
     }
@@ -573,10 +579,10 @@ cudaError_t fused_typed(const FfnArgs& a, cudaStream_t s) {
   const int nch = a.H * WSZ / 16;  // 16-byte chunks of one Wg/Wu row
   if (nch <= 64)
     return a.T == 1 ? launch_typed<WT, 1, 2>(a, lay, map, s)
-                    : a.T <= 4 ? launch_typed<WT, 4, 2>(a, lay, map, s) : launch_typed<WT, kMaxT, 2>(a, lay, map, s);
+                    : launch_typed<WT, 4, 2>(a, lay, map, s);
   if (nch > 256) return cudaErrorNotSupported;
   return a.T == 1 ? launch_typed<WT, 1, 8>(a, lay, map, s)
-                  : a.T <= 4 ? launch_typed<WT, 4, 8>(a, lay, map, s) : launch_typed<WT, kMaxT, 8>(a, lay, map, s);
+                  : launch_typed<WT, 4, 8>(a, lay, map, s);
 }
 
 }  // namespace
