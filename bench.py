@@ -298,7 +298,7 @@ def run_reference(args, w):
 # in-pipeline launches (64 GB bank, copies riding along) are not captured (too large for a full capture);
 # the all-hit launches of --ffn-only are (profiles/ffn_fused_kernel_qwen35b_decode_allhit.md).
 FFN_TRAFFIC_PER_LAUNCH = {}
-FFN_ONLY_TRAFFIC_PER_LAUNCH = {"qwen35b-a3b-shape-decode-b1": (50.393344e6 + 4.096e3 + 50.393344e6 + 4.608e3) / 2}
+FFN_ONLY_TRAFFIC_PER_LAUNCH = {"qwen35b-a3b-shape-decode-b1": (50.393856e6 + 1.28e3 + 50.3936e6 + 1.024e3) / 2}
 
 
 def prefill_measure(dev, peak_tflops, steps=2):
