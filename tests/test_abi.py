@@ -55,6 +55,16 @@ def test_checked_build_exports_the_same_symbols(lib_path, checked_lib_path):
         assert lib.ft_debug_set_key_slot(None, 0, 0) == 1  # FT_ERR_INVALID_ARG
 
 
+def test_host_bank_calls_validate_before_any_cuda_call(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    lib.ft_host_bank_alloc.argtypes = [ctypes.c_uint64, ctypes.POINTER(ctypes.c_void_p)]
+    lib.ft_host_bank_free.argtypes = [ctypes.c_void_p]
+    out = ctypes.c_void_p(1234)
+    assert lib.ft_host_bank_alloc(0, ctypes.byref(out)) == 1   # FT_ERR_INVALID_ARG: zero bytes
+    assert lib.ft_host_bank_alloc(4096, None) == 1             # FT_ERR_INVALID_ARG: null out
+    assert lib.ft_host_bank_free(None) == 0                   # freeing nothing is fine
+
+
 def test_binding_has_the_same_names(lib_path):
     import expert_cache_host_layer_gb300 as ft
     for n in declared_functions():
