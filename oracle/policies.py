@@ -125,3 +125,36 @@ def previous_step_prefetch_coverage(topk_trace, num_layers: int, num_experts: in
                 wasted_or_useful += len(not_res)
             prev[l] = np.unique(topk_trace[s, l])
     return misses, covered, wasted_or_useful
+
+
+def frequency_prefetch_coverage(topk_trace, num_layers: int, num_experts: int, num_slots: int, per_layer: int,
+                                warm_steps: int = 0):
+    """How many of the global LRU cache's misses a prefetch of each layer's
+    most often used experts could have hidden, and how much link traffic it
+    would add (the same page as previous_step_prefetch_coverage: predict the
+    next experts and stream them early; here the predictor is the routing
+    history instead of the last step).
+
+    Reading: before step s reaches layer l, the predictor names the
+    `per_layer` experts of layer l with the most uses in steps < s (ties: lower
+    expert index) among those not resident at that moment; a miss of that
+    event is covered if its expert was named.  Counted from step
+    `warm_steps` on.  Returns (misses, covered, prefetched)."""
+    from .cache import ExpertCacheOracle
+    steps = topk_trace.shape[0]
+    cache = ExpertCacheOracle(num_layers, num_experts, num_slots)
+    uses = np.zeros((num_layers, num_experts), dtype=np.int64)
+    misses = covered = prefetched = 0
+    for s in range(steps):
+        for l in range(num_layers):
+            order = sorted(range(num_experts), key=lambda e: (-uses[l, e], e))
+            named = [e for e in order if cache.key_to_slot[l * num_experts + e] < 0][:per_layer]
+            ev = cache.event(l, topk_trace[s, l])
+            if s >= warm_steps:
+                m = {int(e) for e in ev.miss_expert}
+                misses += len(m)
+                covered += len(m & set(named))
+                prefetched += len(named)
+            for e in np.unique(topk_trace[s, l]):
+                uses[l, int(e)] += 1
+    return misses, covered, prefetched

@@ -145,3 +145,56 @@ def test_previous_step_prefetch_covers_no_miss_on_the_decode_trace():
     misses, covered, predicted = policies.previous_step_prefetch_coverage(tr, w.num_layers, w.num_experts,
                                                                           w.num_slots)
     assert misses > 0 and covered == 0 and predicted == 0
+
+
+def test_frequency_prefetch_coverage_against_a_textbook_lru():
+    """k = 1 traces, recomputed with an OrderedDict LRU and plain use counts:
+    the predictor names the most-used non-resident experts of the layer
+    (ties: lower index); a miss is covered when its expert was named."""
+    import collections
+
+    from oracle import policies
+    rng = np.random.default_rng(11)
+    for L, E, C, P in ((4, 8, 3, 2), (5, 6, 3, 1), (3, 10, 5, 3)):
+        steps = 50
+        tr = rng.integers(0, E, size=(steps, L, 1, 1)).astype(np.int32)
+        got = policies.frequency_prefetch_coverage(tr, L, E, C, P, warm_steps=5)
+        lru = collections.OrderedDict()
+        uses = np.zeros((L, E), dtype=int)
+        m = c = p = 0
+        for s in range(steps):
+            for l in range(L):
+                order = sorted(range(E), key=lambda e: (-uses[l, e], e))
+                named = [e for e in order if l * E + e not in lru][:P]
+                e_now = int(tr[s, l, 0, 0])
+                key = l * E + e_now
+                hit = key in lru
+                if hit:
+                    lru.move_to_end(key)
+                else:
+                    if len(lru) == C:
+                        lru.popitem(last=False)
+                    lru[key] = True
+                if s >= 5:
+                    m += not hit
+                    c += (not hit) and e_now in named
+                    p += len(named)
+                uses[l, e_now] += 1
+        assert got == (m, c, p), (L, E, C, P)
+        assert 0 < got[1] <= got[0]
+
+
+def test_frequency_prefetch_costs_far_more_link_traffic_than_it_saves_on_the_decode_trace():
+    """On the 35B-shaped decode routing the misses are fresh draws from the
+    tail of each layer's expert popularity: naming the 8 most-used missing
+    experts per layer covers about a tenth of the misses while copying more
+    than fifty times as many blobs as it covers."""
+    from oracle import policies, routing
+    w = W.QWEN35B_DECODE
+    steps = 48
+    lg = W.router_logits(w.replace(steps=steps))
+    tr = np.stack([np.stack([routing.topk(lg[s, l], w.top_k) for l in range(w.num_layers)]) for s in range(steps)])
+    misses, covered, prefetched = policies.frequency_prefetch_coverage(tr, w.num_layers, w.num_experts,
+                                                                       w.num_slots, 8, warm_steps=16)
+    assert misses > 0 and covered < 0.25 * misses
+    assert prefetched > 50 * max(covered, 1)
