@@ -17,7 +17,8 @@ import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 CHECKED = os.environ.get("FT_CHECKED", "") == "1"
-LIB_PATH = os.path.join(_HERE, "_build_checked" if CHECKED else "_build", "libft.so")
+SANITIZED = os.environ.get("FT_SANITIZE", "") == "1"  # the host code built with UndefinedBehaviorSanitizer
+LIB_PATH = os.path.join(_HERE, "_build_checked" if CHECKED else "_build_ubsan" if SANITIZED else "_build", "libft.so")
 
 FT_OK, FT_ERR_INVALID_ARG, FT_ERR_CUDA, FT_ERR_OOM, FT_ERR_CAPACITY, FT_ERR_STATE, FT_ERR_TIMEOUT, \
     FT_ERR_CHECKED, FT_ERR_UNSUPPORTED = range(9)

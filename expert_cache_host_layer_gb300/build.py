@@ -26,6 +26,9 @@ OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libft.so")
 OUT_CHECKED = os.path.join(HERE, "_build_checked")
 LIB_CHECKED = os.path.join(OUT_CHECKED, "libft.so")
+OUT_UBSAN = os.path.join(HERE, "_build_ubsan")
+LIB_UBSAN = os.path.join(OUT_UBSAN, "libft.so")
+UBSAN = ["-Xcompiler", "-fsanitize=undefined", "-Xcompiler", "-fno-sanitize-recover=all"]
 INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -54,15 +57,18 @@ def up_to_date(lib: str = LIB) -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
-    out, lib = (OUT_CHECKED, LIB_CHECKED) if checked else (OUT, LIB)
+def build(force: bool = False, verbose: bool = False, checked: bool = False, ubsan: bool = False) -> str:
+    """checked: the bounds-checked build; ubsan: the host code compiled with
+    UndefinedBehaviorSanitizer (loaded with FT_SANITIZE=1; the host-sanitizer
+    test runs the CPU tests of the ABI against it)."""
+    out, lib = (OUT_CHECKED, LIB_CHECKED) if checked else (OUT_UBSAN, LIB_UBSAN) if ubsan else (OUT, LIB)
     if not force and up_to_date(lib):
         return lib
     os.makedirs(out, exist_ok=True)
     cc = nvcc()
     srcs = _sources()
     objs = [os.path.join(out, os.path.basename(s)[:-3] + ".o") for s in srcs]
-    extra = ["-DFT_CHECKED"] if checked else []
+    extra = (["-DFT_CHECKED"] if checked else []) + (UBSAN if ubsan else [])
 
     def compile_one(src_obj):
         src, obj = src_obj
@@ -78,7 +84,8 @@ def build(force: bool = False, verbose: bool = False, checked: bool = False) -> 
             if verbose and msg.strip():
                 print(msg, file=sys.stderr)
     tmp = lib + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-lpthread", "-ldl", "-lrt"]
+    cmd = [cc, *ARCH, "-shared", "-cudart", "static", *(UBSAN if ubsan else []), "-o", tmp, *objs, "-lpthread",
+           "-ldl", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
@@ -87,4 +94,5 @@ def build(force: bool = False, verbose: bool = False, checked: bool = False) -> 
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, checked="--checked" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, checked="--checked" in sys.argv,
+                ubsan="--ubsan" in sys.argv))

@@ -21,8 +21,12 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "synth.c")
-_OUT_DIR = os.path.join(_HERE, "_build")
+# SYNTH_SANITIZE=1: a build with AddressSanitizer and UndefinedBehaviorSanitizer
+# (the process must preload the ASan runtime), for the host-sanitizer test
+_SANITIZE = os.environ.get("SYNTH_SANITIZE", "") == "1"
+_OUT_DIR = os.path.join(_HERE, "_build_san" if _SANITIZE else "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "libsynth.so")
+_SAN_FLAGS = ["-fsanitize=address,undefined", "-fno-sanitize-recover=all", "-fno-omit-frame-pointer", "-g"]
 _lock = threading.Lock()
 _lib = None
 
@@ -36,7 +40,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O3", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
-                               "-o", tmp, _SRC, "-lm"])
+                               *(_SAN_FLAGS if _SANITIZE else []), "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
