@@ -31,6 +31,7 @@
 #include <vector>
 
 #include "ft_internal.h"
+#include <nvtx3/nvToolsExt.h>
 
 using namespace ft;
 
@@ -477,9 +478,26 @@ int capacity_bound(const ft_cache* c) {
   return (int)(2 * std::min<long long>(rows, c->E));
 }
 
+// An NVTX range around a library call (shown by profilers that collect NVTX;
+// free when none is attached), named after the call and carrying the layer.
+struct NvtxRange {
+  NvtxRange(const char* name, int layer) {
+    nvtxEventAttributes_t ev = {};
+    ev.version = NVTX_VERSION;
+    ev.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    ev.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    ev.message.ascii = name;
+    ev.payloadType = NVTX_PAYLOAD_TYPE_INT32;
+    ev.payload.iValue = layer;
+    nvtxRangePushEx(&ev);
+  }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
 }  // namespace
 
 // ============================================================== the C ABI
+
 extern "C" {
 
 size_t ft_expert_bytes(int32_t hidden, int32_t inter, int32_t wdtype) { return blob_bytes(hidden, inter, wdtype); }
@@ -741,6 +759,7 @@ ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t n
 
 ft_status ft_route_classify(ft_cache* c, int32_t layer, const float* logits, int32_t T, int32_t* topk_idx,
                             float* topk_w) {
+  NvtxRange nv("ft_route_classify", layer);
   if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
   if (layer < 0 || layer >= c->L) return fail(FT_ERR_INVALID_ARG, "layer %d out of range", layer);
   if (T < 0 || T > c->max_tokens) return fail(FT_ERR_INVALID_ARG, "T=%d outside 0..max_tokens=%d", T, c->max_tokens);
@@ -786,6 +805,7 @@ ft_status ft_route_classify(ft_cache* c, int32_t layer, const float* logits, int
 
 
 ft_status ft_fetch_misses(ft_cache* c, int32_t layer) {
+  NvtxRange nv("ft_fetch_misses", layer);
   if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
   if (layer < 0 || layer >= c->L) return fail(FT_ERR_INVALID_ARG, "layer %d out of range", layer);
   const int ev = c->layer_event[layer];
@@ -804,6 +824,7 @@ ft_status ft_fetch_misses(ft_cache* c, int32_t layer) {
 }
 
 ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, void* y) {
+  NvtxRange nv("ft_moe_forward", layer);
   if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
   if (layer < 0 || layer >= c->L) return fail(FT_ERR_INVALID_ARG, "layer %d out of range", layer);
   const int ev = c->layer_event[layer];
@@ -917,6 +938,7 @@ ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, v
 }
 
 ft_status ft_cache_resize(ft_cache* c, void* new_pool, int64_t new_num_slots) {
+  NvtxRange nv("ft_cache_resize", (int)new_num_slots);
   if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
   if (!new_pool || (reinterpret_cast<uintptr_t>(new_pool) & 255))
     return fail(FT_ERR_INVALID_ARG, "new_pool must be a non-null 256-byte aligned device pointer");
@@ -1246,6 +1268,7 @@ ft_status ft_step_graph_create(ft_cache* c, const float* const* logits, const vo
 }
 
 ft_status ft_step_graph_launch(ft_step_graph* g) {
+  NvtxRange nv("ft_step_graph_launch", -1);
   if (!g || !g->exec) return fail(FT_ERR_INVALID_ARG, "null step graph");
   ft_cache* c = g->c;
   const bool ce = c->cfg.fetch_mode == FT_FETCH_COPY_ENGINE;
