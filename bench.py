@@ -199,7 +199,8 @@ def oracle_sample(w: W.Workload, steps: int, workers: int, logits=None):
     and the LRU cache simulation run in order on one host thread (they are a
     sequential decision stream); the FFN of every layer event runs in a pool
     of `workers` spawned processes.  Oracle time = the decision stream's time
-    + the busiest worker's FFN time.  Returns (tokens/s, oracle seconds)."""
+    + the busiest worker's FFN time.  Returns (tokens/s, oracle seconds, CPU
+    seconds summed over the thread and the workers)."""
     import concurrent.futures
     import multiprocessing
 
@@ -237,7 +238,7 @@ def oracle_sample(w: W.Workload, steps: int, workers: int, logits=None):
             else:
                 os.environ[k] = v
     spent = t_dec + max(busy.values())
-    return steps * w.tokens / spent, spent
+    return steps * w.tokens / spent, spent, t_dec + sum(busy.values())
 
 
 def cpu_workers() -> int:
@@ -246,11 +247,12 @@ def cpu_workers() -> int:
 
 def cpu_baseline(w: W.Workload, steps: int):
     workers = cpu_workers()
-    v, dt = oracle_sample(w, steps, workers)
+    v, dt, cpu_s = oracle_sample(w, steps, workers)
     return {"value": v, "unit": "tokens/s", "cores": workers, "kind": "oracle",
             "sample": f"first {steps} decode steps x {w.num_layers} layers of {w.name} (cold cache): routing and "
                       f"LRU simulation in order on one thread, fp64 SwiGLU FFN of each layer event over "
-                      f"{workers} worker processes; {dt:.1f} s of oracle time (decisions + busiest worker)"}
+                      f"{workers} worker processes; {dt:.1f} s of oracle time (decisions + busiest worker), "
+                      f"{cpu_s:.1f} CPU-seconds in all"}
 
 
 def workload_config(w: W.Workload, world: int, n_blobs: int) -> dict:
@@ -274,7 +276,7 @@ def run_reference(args, w):
     logits = W.router_logits(w.replace(steps=args.cpu_steps))
     per = []
     for i in range(args.warmup + args.steps):
-        v, dt = oracle_sample(w, args.cpu_steps, workers, logits)
+        v, dt, _ = oracle_sample(w, args.cpu_steps, workers, logits)
         if i >= args.warmup:
             per.append(dt / args.cpu_steps)
     ms = 1e3 * statistics.mean(per)
