@@ -37,7 +37,8 @@
 // 64-byte swizzle) into the upper half of the stage's B area, and eight
 // converter warps (warps 6-13, one B row per thread) read them, multiply each
 // by its block's scale (staged in shared memory once per tile; a K block of 64
-// lies in one 128-wide scale block) and write fp16 into the
+// lies in one 128-wide scale block; one fp16 multiply per pair of weights
+// when every scale of the tile is an fp16 value) and write fp16 into the
 // 128-byte-swizzled layout the MMA reads, over the whole B area (all reads
 // happen before any write: a named barrier separates them), then release the
 // stage to the MMA.  fp16 rather than bf16 because an e4m3 value times a bf16
@@ -361,6 +362,41 @@ __device__ __forceinline__ TileInfo tile_info(const Smem& s, int n_u, int ntiles
   return t;
 }
 
+// One B row of a K block: 64 e4m3 weights (four 16-byte chunks of a 64-byte
+// swizzled fp8 row) times their block scale, written as fp16 into row r of the
+// 128-byte-swizzled 16-bit B tile.  kFast: the scale is an fp16 value, and one
+// fp16 multiply per pair rounds the exact product (an e4m3 value has 4
+// significant bits, the scale 8); else the product is formed in fp32 (exact)
+// and rounded to fp16.  Both give the exact product rounded once to fp16.
+template <bool kFast>
+__device__ __forceinline__ void dequant_row(const uint4 (&raw)[4], float scl, uint8_t* B, int r) {
+  const __half2 s2 = __float2half2_rn(scl);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // 16 fp8 -> 16 fp16 = two 16-byte chunks of the 16-bit row
+    const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+    uint32_t o[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[q] & 0xffffu), __NV_E4M3);
+      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[q] >> 16), __NV_E4M3);
+      __half2 ha, hb;
+      if (kFast) {
+        ha = __hmul2(__half2(lo), s2);
+        hb = __hmul2(__half2(hi), s2);
+      } else {
+        const float2 fa = __half22float2(__half2(lo)), fb = __half22float2(__half2(hi));
+        ha = __floats2half2_rn(fa.x * scl, fa.y * scl);
+        hb = __floats2half2_rn(fb.x * scl, fb.y * scl);
+      }
+      o[2 * q] = *reinterpret_cast<const uint32_t*>(&ha);
+      o[2 * q + 1] = *reinterpret_cast<const uint32_t*>(&hb);
+    }
+    const int j0 = 2 * i, j1 = 2 * i + 1;
+    *reinterpret_cast<uint4*>(B + r * 128 + ((j0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(B + r * 128 + ((j1 ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 // kGateUp: the gate/up + SwiGLU GEMM (A = grouped x rows, B = Wg/Wu rows);
 // else the down GEMM (A = h rows, B = Wd rows).  map_a and map_b load boxes of
 // 64 columns x 128 rows (x, h, Wg/Wu) or N rows (Wd); map_out stores 32-row
@@ -501,6 +537,7 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
         // from the slot once per tile instead of once per stage and row
         const int KB = KT / 2;
         asm volatile("bar.sync 5, %0;" ::"n"(kCvtWarps * 32) : "memory");  // the previous tile's are read
+        uint32_t inexact = 0;
         for (int i = ctid; i < 2 * KB; i += kCvtWarps * 32) {
           const int rb = i / KB, kb = i - rb * KB;
           float v = 0.0f;
@@ -510,8 +547,17 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
             v = __uint_as_float((uint32_t)__ldg(sc + idx) << 16);
           }
           s.s_scale[i] = v;
+          inexact |= __half2float(__float2half_rn(v)) != v;
         }
-        asm volatile("bar.sync 5, %0;" ::"n"(kCvtWarps * 32) : "memory");
+        // fast: every block scale of the tile is an fp16 value (a bf16 scale
+        // below 2^-14 or beyond fp16's range is not, and takes the fp32 route)
+        uint32_t fast;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, 5, %2, q;\n\t"
+            "selp.u32 %0, 0, 1, p;\n\t}"
+            : "=r"(fast)
+            : "r"(inexact), "n"(kCvtWarps * 32)
+            : "memory");
         for (int kt = 0; kt < KT; ++kt, ++it) {
           const int st = it % kStages;
           bool ok = true;
@@ -551,24 +597,8 @@ __global__ void __launch_bounds__(kFp8 ? kTcThreadsFp8 : kTcThreads, 1)
           for (int h = 0; h < kCvtRows; ++h) {
             const int r = ctid + h * (kCvtWarps * 32);
             if (r < N) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {  // 16 fp8 -> 16 fp16 = two 16-byte chunks of the 16-bit row
-                const uint32_t w4[4] = {raw[h][i].x, raw[h][i].y, raw[h][i].z, raw[h][i].w};
-                uint32_t o[8];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[q] & 0xffffu), __NV_E4M3);
-                  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[q] >> 16), __NV_E4M3);
-                  const float2 fa = __half22float2(__half2(lo)), fb = __half22float2(__half2(hi));
-                  const __half2 ha = __floats2half2_rn(fa.x * scl[h], fa.y * scl[h]);
-                  const __half2 hb2 = __floats2half2_rn(fb.x * scl[h], fb.y * scl[h]);
-                  o[2 * q] = *reinterpret_cast<const uint32_t*>(&ha);
-                  o[2 * q + 1] = *reinterpret_cast<const uint32_t*>(&hb2);
-                }
-                const int j0 = 2 * i, j1 = 2 * i + 1;  // 128-byte-swizzled 16-bit row r
-                *reinterpret_cast<uint4*>(B + r * 128 + ((j0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                *reinterpret_cast<uint4*>(B + r * 128 + ((j1 ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-              }
+              if (fast) dequant_row<true>(raw[h], scl[h], B, r);
+              else dequant_row<false>(raw[h], scl[h], B, r);
             }
           }
           fence_async_smem();  // the tensor core reads these rows through the async proxy

@@ -35,6 +35,24 @@ def bank_blob(bank: torch.Tensor, w: W.Workload, n_blobs: int, layer: int, exper
     return bank.numpy()[b * eb:(b + 1) * eb]
 
 
+def shift_fp8_scales(blobs: np.ndarray, w: W.Workload, n_blobs: int, shifts: tuple[int, int, int]) -> None:
+    """Multiply every bf16 block scale of Wg, Wu and Wd in `n_blobs` fp8 blobs
+    (uint8 array, runtime layout) by 2**shifts[0], 2**shifts[1], 2**shifts[2],
+    in place: an exact change of each scale's exponent field.  Both the GPU
+    path and the oracle then read the same, still valid, blobs."""
+    assert w.wdtype == synth.W_FP8
+    H, I, eb = w.hidden, w.inter, w.expert_bytes
+    g = (H // 128) * (I // 128)
+    for b in range(n_blobs):
+        off = b * eb + 3 * H * I
+        sc = blobs[off:off + 6 * g].view(np.uint16)
+        for m, sh in enumerate(shifts):
+            part = sc[m * g:(m + 1) * g]
+            e = (part.astype(np.int32) >> 7) & 0xFF
+            assert np.all((e == 0) | ((e + sh > 0) & (e + sh < 255))), "scale exponent out of range"
+            part[:] = np.where(e == 0, part, part.astype(np.int32) + (sh << 7)).astype(np.uint16)
+
+
 def to_act(x: np.ndarray, w: W.Workload, device) -> torch.Tensor:
     t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
     return t.to(device=device, dtype=torch.float32 if w.wdtype == synth.W_F32 else torch.bfloat16)
@@ -84,12 +102,14 @@ def oracle_ffn(w: W.Workload, bank, n_blobs, layer, x, idx, gates):
 def run_parity(w: W.Workload, steps: int | None = None, fetch_mode: int = 1, double_buffer: bool = True,
                bank_blobs: int | None = None, check_tables_every: int = 1, ffn_every: int = 1,
                check_slots: bool = True, copy_streams: int = 1, logits=None, device="cuda:0",
-               ffn_tokens=None, ffn_workers: int = 0):
+               ffn_tokens=None, ffn_workers: int = 0, fp8_scale_shifts=None):
     """Run `steps` steps of workload w through libft and the oracle.
 
     ffn_tokens: compare the FFN output on these token rows only; a callable
     ffn_tokens(layer, topk_idx) returns the rows for that layer event (None:
     every row).  Decisions are always compared in full.
+    fp8_scale_shifts: (Wg, Wu, Wd) powers of two applied to every block scale
+    of the bank before the run (shift_fp8_scales).
     ffn_workers: check the FFN outputs in that many spawned host processes
     (tests/oracle_worker.py) while the GPU run goes on; 0 checks inline.  Returns a report dict; raises AssertionError on the
     first mismatch.
@@ -98,6 +118,8 @@ def run_parity(w: W.Workload, steps: int | None = None, fetch_mode: int = 1, dou
     steps = steps or w.steps
     dev = torch.device(device)
     bank, n_blobs = make_bank(w, bank_blobs)
+    if fp8_scale_shifts is not None:
+        shift_fp8_scales(bank.numpy(), w, n_blobs, fp8_scale_shifts)
     if logits is None:
         logits = W.router_logits(w.replace(steps=steps))
     cache = ExpertCache(w.num_layers, w.num_experts, w.top_k, w.hidden, w.inter, w.wdtype, w.num_slots,

@@ -71,3 +71,14 @@ def test_fp8_prefill_parity(w):
     rep = run_parity(w, steps=1, double_buffer=True)
     assert rep["events"] == 2 and rep["ffn_checked"] == 2 and rep["slots_checked"] > 0
     print("fp8 prefill:", {k: rep[k] for k in ("max_err", "max_rms_err", "miss_rate")})
+
+
+def test_fp8_prefill_parity_scales_off_fp16():
+    # Wg and Wd block scales times 2^-6 (Wu times 2^6 keeps h at its usual size):
+    # every Wg and Wd row block then has a scale that is not an fp16 value, so
+    # every tile of both GEMMs dequantises through the fp32 product instead of
+    # the fp16 multiply the generated scales allow (tests/test_fp8_scale_fixture.py)
+    from tests.harness import run_parity
+    rep = run_parity(FP8_SMALL_PREFILL, steps=1, double_buffer=True, fp8_scale_shifts=(-6, 6, -6))
+    assert rep["events"] == 2 and rep["ffn_checked"] == 2
+    print("fp8 prefill, scales off the fp16 grid:", {k: rep[k] for k in ("max_err", "max_rms_err")})
