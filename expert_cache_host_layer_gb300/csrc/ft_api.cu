@@ -175,6 +175,7 @@ struct ft_cache {
   void* pf_xp = nullptr;              // bf16 x rows in grouped order [rows][H]
   void* pf_yp = nullptr;
   int32_t* pf_pos = nullptr;
+  int32_t* pf_hist = nullptr;          // [E][chunks of rows]: the row grouping's counts
   unsigned* gbar = nullptr;           // grid-barrier words of the fused FFN kernel
   bool fused_ok = true;               // false once the fused FFN kernel reported it cannot run
   // streams and events
@@ -468,7 +469,8 @@ uint64_t cache_device_bytes(const ft_cache_config& g, int64_t C) {
   b += dev_alloc(4 * (uint64_t)std::min(g.max_tokens, kDecodeMaxTokens) * g.top_k * I);
   b += dev_alloc(16);
   if (g.max_tokens > kDecodeMaxTokens && prefill_supported((int)H, (int)I, g.wdtype, (int)E))
-    b += dev_alloc(2 * rows * I) + dev_alloc(2 * rows * H) + dev_alloc(2 * rows * H) + dev_alloc(4 * rows);
+    b += dev_alloc(2 * rows * I) + dev_alloc(2 * rows * H) + dev_alloc(2 * rows * H) + dev_alloc(4 * rows) +
+         dev_alloc(4 * E * (uint64_t)group_chunks((long long)rows));
   if (g.fetch_mode == FT_FETCH_COPY_ENGINE) b += dev_alloc(4 * kRing);
   return b;
 }
@@ -551,6 +553,7 @@ ft_status ft_cache_destroy(ft_cache* c) {
   cudaFree(c->pf_xp);
   cudaFree(c->pf_yp);
   cudaFree(c->pf_pos);
+  cudaFree(c->pf_hist);
   cudaFree(c->gbar);
   if (c->ring_host) cudaFreeHost(c->ring_host);
   if (c->flag_src) cudaFreeHost(c->flag_src);
@@ -705,6 +708,7 @@ ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t n
       CU(cudaMalloc(&c->pf_xp, sizeof(uint16_t) * prows * c->H));
       CU(cudaMalloc(&c->pf_yp, sizeof(uint16_t) * prows * c->H));
       CU(cudaMalloc(&c->pf_pos, sizeof(int32_t) * prows));
+      CU(cudaMalloc(&c->pf_hist, sizeof(int32_t) * c->E * group_chunks(prows)));
     }
     CU(cudaMalloc(&c->gbar, 4 * sizeof(unsigned)));
     CU(cudaMemset(c->gbar, 0, 3 * sizeof(unsigned)));
@@ -862,6 +866,7 @@ ft_status ft_moe_forward(ft_cache* c, int32_t layer, const void* x, int32_t T, v
     PrefillArgs p{};
     p.hdr = pl.hdr; p.unique_expert = pl.unique_expert; p.unique_slot = pl.unique_slot; p.u_offset = pl.u_offset;
     p.topk_idx = pl.topk_idx; p.topk_w = pl.topk_w; p.rows_by_u = pl.rows_by_u; p.pos = c->pf_pos;
+    p.hist = c->pf_hist;
     p.x = x; p.xp = c->pf_xp; p.h = c->pf_h; p.yp = c->pf_yp; p.y = static_cast<float*>(y);
     p.pool = static_cast<const uint8_t*>(c->pool); p.expert_bytes = (long long)c->eb;
     p.H = c->H; p.I = c->I; p.k = c->k; p.T = T; p.E = c->E; p.status = c->tab.status; p.wdtype = c->wdtype;
@@ -1123,7 +1128,12 @@ ft_status ft_timing_enable(ft_cache* c, int32_t on) {
   if (!c) return fail(FT_ERR_INVALID_ARG, "null cache");
   ft_status s = sync_all(c);
   if (s != FT_OK) return s;
-  for (auto& t : c->timers) t.reset();
+  for (auto& t : c->timers) {
+    t.reset();
+    // the events exist before the first timed phase: creating a pool of them
+    // inside a timed window would count that host time as GPU time
+    if (on && !t.ensure()) return fail(FT_ERR_CUDA, "creating timing events failed");
+  }
   c->timing = on != 0;
   return FT_OK;
 }

@@ -203,6 +203,7 @@ struct PrefillArgs {
   const float* topk_w;       // [T*k]
   int32_t* rows_by_u;        // [T*k] out: rows grouped by unique expert
   int32_t* pos;              // [T*k] out: grouped place of each row
+  int32_t* hist;             // [E][group_chunks(T*k)] scratch of the row grouping
   const void* x;             // [T][H] bf16
   void* xp;                  // [T*k][H] bf16 scratch: the x row of each grouped row
   void* h;                   // [T*k][I] bf16 scratch
@@ -215,6 +216,7 @@ struct PrefillArgs {
   int wdtype;                // FT_W_BF16 or FT_W_FP8E4M3_B128
 };
 bool prefill_supported(int H, int I, int wdtype, int E);
+int group_chunks(long long rows);  // chunks of rows the prefill row grouping counts separately
 // marks (optional): events recorded before and after the gate/up GEMM, then
 // before and after the down GEMM.
 cudaError_t launch_prefill_ffn(const PrefillArgs& a, int num_slots, cudaStream_t s, int* launches,

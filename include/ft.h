@@ -329,7 +329,10 @@ int32_t ft_checked_build(void);
 ft_status ft_debug_set_key_slot(ft_cache* cache, int32_t key, int32_t slot);
 
 /* Enable (1) or disable (0) per-phase CUDA-event timing; enabling clears the
- * totals.  ft_get_timing waits for the streams and returns the totals. */
+ * totals and creates the events up front (no timed phase pays for creating
+ * them).  ft_get_timing waits for the streams and returns the totals.
+ * Errors: FT_ERR_INVALID_ARG (null cache), FT_ERR_CUDA (events could not be
+ * created), or an error the synchronisation reports. */
 ft_status ft_timing_enable(ft_cache* cache, int32_t on);
 ft_status ft_get_timing(ft_cache* cache, ft_timing* out);
 
