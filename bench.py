@@ -295,12 +295,23 @@ def run_reference(args, w):
 
 # --------------------------------------------------------------------- our arm
 
-# dram__bytes_read.sum + dram__bytes_write.sum per ffn_fused_kernel launch from an ncu capture, keyed by
-# workload; they belong to the kernel as captured: drop an entry whenever that kernel changes.  The
-# in-pipeline launches (64 GB bank, copies riding along) are not captured (too large for a full capture);
-# the all-hit launches of --ffn-only are (profiles/ffn_fused_kernel_qwen35b_decode_allhit.md).
-FFN_TRAFFIC_PER_LAUNCH = {}
+# dram__bytes_read.sum + dram__bytes_write.sum of ffn_fused_kernel launches from ncu captures, keyed by
+# workload; they belong to the kernel as captured: drop an entry whenever that kernel changes.
+# The all-hit launches of --ffn-only, per launch (profiles/ffn_fused_kernel_qwen35b_decode_allhit.md).
 FFN_ONLY_TRAFFIC_PER_LAUNCH = {"qwen35b-a3b-shape-decode-b1": (50.393856e6 + 1.28e3 + 50.3936e6 + 1.024e3) / 2}
+# The in-pipeline launches (copies riding along) of a small case of the same kernel, whose device memory
+# fits a capture (320 slots, a 640-blob bank; 6 launches, profiles/ffn_fused_kernel_qwen35b_decode_pipeline.md):
+# DRAM bytes read per unique expert, and DRAM bytes written per launch.  The blobs a launch copies in land
+# in the 129 MB L2 and reach DRAM after the launch, so its own writes are near zero; the reads scale with
+# the unique experts, which the full workload's traffic is scaled by.
+FFN_PIPELINE_TRAFFIC = {"qwen35b-a3b-shape-decode-b1": ((50.396e6 + 50.396e6 + 50.395e6 + 50.397e6 + 50.404e6
+                                                          + 50.404e6) / 6 / 8, (43e3 + 25e3 + 19e3) / 6)}
+
+
+def pipeline_traffic(name: str, mean_unique: float):
+    """DRAM bytes per in-pipeline FFN launch scaled from the small capture, or None."""
+    c = FFN_PIPELINE_TRAFFIC.get(name)
+    return None if c is None else c[0] * mean_unique + c[1]
 
 
 def prefill_measure(dev, peak_tflops, steps=2):
@@ -928,7 +939,10 @@ def run_ours(args, w):
                                    "pass",
                          "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": FFN_TRAFFIC_PER_LAUNCH.get(w.name),
+                         "traffic": pipeline_traffic(w.name, tp["ffn_read_bytes_per_launch"] / w.expert_bytes),
+                         "traffic_how": "DRAM bytes per unique expert read x the mean unique experts + the "
+                                        "writes per launch, from an ncu capture of a small case of this kernel "
+                                        "(the copied blobs' writes reach DRAM after the launch, from L2)",
                          "bytes_per_launch": bytes_launch,
                          "bytes_def": "n_unique x expert_bytes read + n_miss(next layer) x expert_bytes written",
                          "launch_us": tp["ffn_us_per_launch"], "ffn_only": ffn_alone,

@@ -46,3 +46,13 @@ def test_bound_takes_the_slower_resource_per_launch(bench):
     assert b["link_bound_launches"] == pytest.approx(2 / 3)
     assert bench.bound_of_launches(None, eb, 8000.0, 200.0) is None
     assert bench.bound_of_launches((nuniq, carried, window_ms), eb, 8000.0, None) is None
+
+
+def test_pipeline_traffic_scales_the_small_capture_by_unique_experts(bench):
+    per_unique, writes = bench.FFN_PIPELINE_TRAFFIC["qwen35b-a3b-shape-decode-b1"]
+    # the capture read each launch's 8 experts once: about 6.3 MB per unique expert
+    assert per_unique == pytest.approx(6291456 * 1.0017, rel=1e-3)
+    assert bench.pipeline_traffic("qwen35b-a3b-shape-decode-b1", 8.0) == pytest.approx(8 * per_unique + writes)
+    assert bench.pipeline_traffic("qwen35b-a3b-shape-decode-b1", 4.0) < bench.pipeline_traffic(
+        "qwen35b-a3b-shape-decode-b1", 8.0)
+    assert bench.pipeline_traffic("no-such-workload", 8.0) is None
