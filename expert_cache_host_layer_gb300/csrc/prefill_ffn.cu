@@ -188,6 +188,17 @@ int prefill_sms() {
   return n;
 }
 
+// One full wave of a grid-stride kernel: the CTAs of 256 threads an SM holds
+// at once (from its registers and shared memory) times the SMs, so no SM runs
+// a partial second wave.
+template <typename K>
+int full_wave(K kernel) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kPThreads, 0) != cudaSuccess || per_sm < 1)
+    per_sm = 4;
+  return per_sm * prefill_sms();
+}
+
 }  // namespace
 
 int group_chunks(long long rows) { return (int)((rows + kGChunk - 1) / kGChunk); }
@@ -205,12 +216,12 @@ cudaError_t launch_prefill_ffn(const PrefillArgs& a, int num_slots, cudaStream_t
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.wdtype == FT_W_FP8E4M3_B128)
-    permute_rows_kernel<true><<<8 * prefill_sms(), kPThreads, 0, s>>>(a);
+    permute_rows_kernel<true><<<full_wave(permute_rows_kernel<true>), kPThreads, 0, s>>>(a);
   else
-    permute_rows_kernel<false><<<8 * prefill_sms(), kPThreads, 0, s>>>(a);
+    permute_rows_kernel<false><<<full_wave(permute_rows_kernel<false>), kPThreads, 0, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = launch_prefill_gemms(a, num_slots, s, marks)) != cudaSuccess) return e;
-  combine_kernel<<<4 * prefill_sms(), kPThreads, 0, s>>>(a);
+  combine_kernel<<<full_wave(combine_kernel), kPThreads, 0, s>>>(a);
   *launches = 7;
   return cudaGetLastError();
 }
