@@ -135,8 +135,12 @@ __global__ void __launch_bounds__(kPThreads) permute_rows_kernel(PrefillArgs a) 
   const int lane = threadIdx.x & 31;
   const uint4* x = static_cast<const uint4*>(a.x);
   uint4* xp = static_cast<uint4*>(a.xp);
-  for (int p = (blockIdx.x * kPThreads + threadIdx.x) >> 5; p < R; p += (gridDim.x * kPThreads) >> 5) {
-    const int row = __ldg(&a.rows_by_u[p]);
+  const int stride = (gridDim.x * kPThreads) >> 5;
+  int p = (blockIdx.x * kPThreads + threadIdx.x) >> 5;
+  int row_next = p < R ? __ldg(&a.rows_by_u[p]) : 0;
+  for (; p < R; p += stride) {
+    const int row = row_next;  // the next row's index is in flight while this row moves
+    if (p + stride < R) row_next = __ldg(&a.rows_by_u[p + stride]);
     if (!checked_ok(row >= 0 && row < R, a.status)) continue;
     const int t = row / a.k;
     const uint4* src = x + (long long)t * n16;
