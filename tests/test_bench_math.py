@@ -1,6 +1,7 @@
 """CPU checks of the bench's derived measurements: the marginal host-link fit
 and the per-launch HBM-or-link bound (bench.py), on synthetic launch data
-whose answer is known."""
+whose answer is known, and the in-pipeline DRAM traffic scaled from a small
+capture."""
 import sys
 
 import numpy as np
