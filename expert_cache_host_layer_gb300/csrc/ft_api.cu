@@ -709,6 +709,7 @@ ft_status ft_cache_create(const ft_cache_config* cfg, void* slot_pool, int64_t n
       CU(cudaMalloc(&c->pf_yp, sizeof(uint16_t) * prows * c->H));
       CU(cudaMalloc(&c->pf_pos, sizeof(int32_t) * prows));
       CU(cudaMalloc(&c->pf_hist, sizeof(int32_t) * c->E * group_chunks(prows)));
+      prefill_init();
     }
     CU(cudaMalloc(&c->gbar, 4 * sizeof(unsigned)));
     CU(cudaMemset(c->gbar, 0, 3 * sizeof(unsigned)));

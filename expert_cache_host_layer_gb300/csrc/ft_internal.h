@@ -217,6 +217,7 @@ struct PrefillArgs {
 };
 bool prefill_supported(int H, int I, int wdtype, int E);
 int group_chunks(long long rows);  // chunks of rows the prefill row grouping counts separately
+void prefill_init();               // works out the prefill kernels' grids (call outside stream capture)
 // marks (optional): events recorded before and after the gate/up GEMM, then
 // before and after the down GEMM.
 cudaError_t launch_prefill_ffn(const PrefillArgs& a, int num_slots, cudaStream_t s, int* launches,

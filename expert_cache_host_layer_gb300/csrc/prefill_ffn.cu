@@ -203,7 +203,20 @@ int full_wave(K kernel) {
   return per_sm * prefill_sms();
 }
 
+// The three grids, worked out once per process (the first call comes from
+// cache creation, outside any stream capture).
+struct PrefillGrids {
+  int permute_f16, permute_bf16, combine;
+};
+const PrefillGrids& prefill_grids() {
+  static const PrefillGrids g = {full_wave(permute_rows_kernel<true>), full_wave(permute_rows_kernel<false>),
+                                 full_wave(combine_kernel)};
+  return g;
+}
+
 }  // namespace
+
+void prefill_init() { (void)prefill_grids(); }
 
 int group_chunks(long long rows) { return (int)((rows + kGChunk - 1) / kGChunk); }
 
@@ -220,12 +233,12 @@ cudaError_t launch_prefill_ffn(const PrefillArgs& a, int num_slots, cudaStream_t
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.wdtype == FT_W_FP8E4M3_B128)
-    permute_rows_kernel<true><<<full_wave(permute_rows_kernel<true>), kPThreads, 0, s>>>(a);
+    permute_rows_kernel<true><<<prefill_grids().permute_f16, kPThreads, 0, s>>>(a);
   else
-    permute_rows_kernel<false><<<full_wave(permute_rows_kernel<false>), kPThreads, 0, s>>>(a);
+    permute_rows_kernel<false><<<prefill_grids().permute_bf16, kPThreads, 0, s>>>(a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if ((e = launch_prefill_gemms(a, num_slots, s, marks)) != cudaSuccess) return e;
-  combine_kernel<<<full_wave(combine_kernel), kPThreads, 0, s>>>(a);
+  combine_kernel<<<prefill_grids().combine, kPThreads, 0, s>>>(a);
   *launches = 7;
   return cudaGetLastError();
 }
