@@ -8,7 +8,9 @@ have only fp16-valued scales, and the shifted bank of
 `test_fp8_prefill_parity_scales_off_fp16` has a scale off the fp16 grid in
 every Wg and Wd row block, so every gate/up and down tile takes the fp32
 route there.  They also check that the shift is the exact power-of-two
-change of the weights it claims to be, through the oracle's decoding.
+change of the weights it claims to be, through the oracle's decoding, and the
+arithmetic the one-multiply route rests on: for every e4m3 value and bf16
+scales on the fp16 grid, one rounding of the exact product to fp16.
 """
 import numpy as np
 
@@ -57,3 +59,29 @@ def test_shifted_scales_leave_the_fp16_grid_in_every_row_block():
         assert np.array_equal(u1, u0 * 2.0 ** 6)
         assert np.array_equal(d1, d0 * 2.0 ** -6)
         assert np.array_equal(shifted[sl][:3 * H * I], blobs[sl][:3 * H * I])  # the e4m3 codes are untouched
+
+
+def test_one_rounding_claim_behind_the_fp16_route():
+    """Every finite e4m3 value is an fp16 value, and so is a bf16 scale in
+    [2^-14, 2^15] (8 significant bits); their product has at most 12
+    significant bits, so rounding it once to fp16 (one fp16 multiply) gives
+    what the fp32 product rounded to fp16 gives.  A bf16 scale below 2^-14
+    can fall between fp16 values: rounding the scale first then differs."""
+    from oracle import fp8
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)  # 0x7F / 0xFF are NaN
+    w = fp8.decode_array(codes)
+    assert np.array_equal(w.astype(np.float16).astype(np.float64), w)
+    rng = np.random.default_rng(7)
+    mant = rng.integers(0, 128, size=200)
+    for exp in range(-14, 16):
+        s = (1.0 + mant / 128.0) * 2.0 ** exp          # bf16 values: 1 + 7 mantissa bits
+        assert np.array_equal(s.astype(np.float16).astype(np.float64), s)
+        with np.errstate(over="ignore"):                 # past fp16's range both sides give inf
+            prod = w[None, :] * s[:, None]               # exact in fp64
+            via_f32 = (w[None, :].astype(np.float32) * s[:, None].astype(np.float32)).astype(np.float16)
+            via_f16 = (w[None, :].astype(np.float16) * s[:, None].astype(np.float16))
+            assert np.array_equal(prod.astype(np.float16), via_f32)
+            assert np.array_equal(prod.astype(np.float16), via_f16)
+    small = (1.0 + 127 / 128.0) * 2.0 ** -20             # a bf16 scale off the fp16 grid
+    assert float(np.float16(small)) != small
+    assert (w * small).astype(np.float16).tolist() != (w.astype(np.float16) * np.float16(small)).tolist()
