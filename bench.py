@@ -297,10 +297,10 @@ def run_reference(args, w):
 
 # dram__bytes_read.sum + dram__bytes_write.sum of ffn_fused_kernel launches from ncu captures, keyed by
 # workload; they belong to the kernel as captured: drop an entry whenever that kernel changes.
-# The all-hit launches of --ffn-only, per launch (profiles/ffn_fused_kernel_qwen35b_decode_allhit.md).
+# The all-hit launches of --ffn-only, per launch (an ncu --set full capture of two launches).
 FFN_ONLY_TRAFFIC_PER_LAUNCH = {"qwen35b-a3b-shape-decode-b1": (50.393856e6 + 1.28e3 + 50.3936e6 + 1.024e3) / 2}
 # The in-pipeline launches (copies riding along) of a small case of the same kernel, whose device memory
-# fits a capture (320 slots, a 640-blob bank; 6 launches, profiles/ffn_fused_kernel_qwen35b_decode_pipeline.md):
+# fits a capture (320 slots, a 640-blob bank; 6 launches of the same kernel instantiation):
 # DRAM bytes read per unique expert, and DRAM bytes written per launch.  The blobs a launch copies in land
 # in the 129 MB L2 and reach DRAM after the launch, so its own writes are near zero; the reads scale with
 # the unique experts, which the full workload's traffic is scaled by.

@@ -1,7 +1,8 @@
-"""The bench commands quoted in profiles/*.md parse with today's bench.py (CPU).
+"""The bench commands quoted in the ncu summaries under profiles/ parse with
+today's bench.py (CPU).
 
-Each summary under profiles/ gives the command that produced its figures; a
-renamed or removed bench option would leave a command nobody can rerun.  The
+Each summary gives the command that produced its figures; a renamed or
+removed bench option would leave a command nobody can rerun.  The
 commands are joined across backslash line continuations, and every
 `python bench.py ...` in them is parsed by bench.py's own argument parser."""
 import glob
